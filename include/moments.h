@@ -1,0 +1,116 @@
+/*
+ * moments.h -- C ABI of libmoments.so, the GB300 (sm_103a) physical-frame state-moments
+ * operator and its recompute backward.
+ *
+ * The operation (burn-mamba, "mamba3/moments/recalculated.rs", trait
+ * Mamba3MomentsBackendExt::mamba3_state_moments_phys and moments_phys_fwd; backward in
+ * "mamba3/moments/backward.rs", moments_phys_bwd and its module header "Gradient math"):
+ *
+ *   per batch row b and head h, with a_t the cumulative da and h_{-1} = initial[b,h]:
+ *     h_t = exp(da[b,t,h]) h_{t-1} + sum_c xhat[b,t,c,h,:] (x) bhat[b,t,c,h,:]      (p x r)
+ *     c_t = derot_t(h_t)          on the r axis of every row: complex pairs by R(-theta)
+ *                                 (pairwise (2i,2i+1) or half-split (i, i+r/2)), or each
+ *                                 4-block left-multiplied by the unit quaternion Q
+ *     m2[b,h] = sum_{t < valid_len[b]} sum_p c_t[p,:]^T c_t[p,:]     [r, r]   (raw sum)
+ *     m1[b,h] = sum_{t < valid_len[b]} sum_p c_t[p,:]                [r]
+ *   The backward returns the gradients of <d_m2, m2> + <d_m1, m1> with respect to all five
+ *   inputs.  The state trajectory is never written to memory: chunk-boundary carries are
+ *   computed by a cheap chunk-level pass and each chunk is recomputed on chip.
+ *
+ * Conventions
+ *   - Every tensor is dense row-major (C order) with exactly the shapes given below.
+ *     xhat [b,s,C,h,p], bhat [b,s,C,h,r]: element type mm_problem.xb_dtype (fp32 or bf16).
+ *     da [b,s,h], initial [b,h,p,r], m2/d_m2 [b,h,r,r], m1/d_m1 [b,h,r]: fp32.
+ *     rot: fp32 [b,s,h,rope_dim/2] cumulative angles (MM_ROT_PAIRWISE / MM_ROT_HALF) or
+ *          [b,s,h,quat_blocks,4] cumulative quaternions (w,x,y,z) (MM_ROT_QUAT); may be
+ *          NULL when there is nothing to rotate (MM_ROT_NONE, rope_dim 0 or 0 blocks).
+ *     Gradients have their input's shape and element type (d_xhat/d_bhat in xb_dtype;
+ *     d_da, d_rot, d_initial fp32).
+ *   - valid_len is a HOST array of b int64 values.  Positions t >= valid_len[b] contribute
+ *     nothing and receive exactly zero gradient; values above s are clamped to s.
+ *   - chunk_len must divide s.  It sets the granularity of the chunk-boundary carries; the
+ *     result does not depend on it (the chunked recurrence is exact).
+ *   - All device pointers are owned by the caller.  The library never allocates, frees or
+ *     synchronises: every call only enqueues work on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and returns.  Outputs are overwritten, never accumulated.
+ *   - `workspace` is caller-owned device scratch of at least mm_workspace_bytes() bytes,
+ *     256-byte aligned.  Its contents need no initialisation and are clobbered.
+ *   - Calls are thread-compatible: concurrent calls need distinct workspaces.
+ *
+ * Errors: arguments are validated on the host before anything is enqueued; a failed
+ * validation returns an error and enqueues nothing.  MM_ERR_CUDA reports a launch error
+ * (the stream may then hold partial work).  Device-side faults surface on the stream like
+ * any CUDA error.
+ */
+#ifndef GB300_MOMENTS_H
+#define GB300_MOMENTS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MM_OK = 0,
+    MM_ERR_INVALID_ARG = 1, /* shape/flag inconsistency, null pointer, chunk_len not dividing s ... */
+    MM_ERR_UNSUPPORTED = 2, /* valid arguments outside what this build implements          */
+    MM_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than mm_workspace_bytes */
+    MM_ERR_CUDA = 4,        /* a CUDA launch or enqueue failed                              */
+    MM_ERR_NONFINITE = 5,   /* reserved: debug finiteness check                             */
+    MM_ERR_TIMEOUT = 6      /* reserved: a bounded device-side wait gave up                 */
+} mm_status;
+
+typedef enum { MM_F32 = 0, MM_BF16 = 1 } mm_dtype;
+
+typedef enum {
+    MM_ROT_NONE = 0,
+    MM_ROT_PAIRWISE = 1, /* complex pairs (2i, 2i+1), i < rope_dim/2 ("rotate_chunk", interleaved) */
+    MM_ROT_HALF = 2,     /* complex pairs (i, i + r/2), i < rope_dim/2 ("rotate_chunk", half-and-half) */
+    MM_ROT_QUAT = 3      /* 4-blocks (4k..4k+3) = (w,x,y,z), k < quat_blocks ("rotate_chunk", quaternion) */
+} mm_rot_kind;
+
+/* Kernel-path selection (mm_problem.flags). */
+#define MM_FLAG_FORCE_GENERIC 0x1u /* use the SIMT fp32 kernels even where the tensor-core path applies */
+
+typedef struct {
+    int64_t b, s, C, h, p, r; /* batch, padded sequence, channels, heads, per-head dim, state rank */
+    int64_t chunk_len;        /* l: divides s                                                     */
+    int32_t xb_dtype;         /* mm_dtype of xhat / bhat and of their gradients                   */
+    int32_t rot;              /* mm_rot_kind                                                      */
+    int64_t rope_dim;         /* complex kinds: rotated width, even; pairwise <= r, half <= r     */
+    int64_t quat_blocks;      /* quaternion kind: J, with 4*J <= r                                */
+    uint32_t flags;           /* MM_FLAG_*                                                        */
+    uint32_t reserved;
+} mm_problem;
+
+/* Bytes of device workspace a forward (backward = 0) or backward (backward != 0) call needs;
+ * 0 if the problem is invalid.  Host-only, enqueues nothing. */
+size_t mm_workspace_bytes(const mm_problem* prob, int backward);
+
+/* Forward: (m2, m1) of the operator above.
+ * Source: "recalculated.rs", Mamba3MomentsBackendExt::mamba3_state_moments_phys / moments_phys_fwd. */
+mm_status moments_fwd(const mm_problem* prob, const void* xhat, const void* bhat, const float* da,
+                      const float* rot, const float* initial, const int64_t* valid_len_host,
+                      float* m2, float* m1, void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward: the five input gradients for cotangents (d_m2, d_m1), recomputing every state
+ * from the leaf inputs (nothing is saved by the forward).  d_m2 need not be symmetric.
+ * Source: "backward.rs", moments_phys_bwd, MomentsGrads, module header "Gradient math". */
+mm_status moments_bwd(const mm_problem* prob, const void* xhat, const void* bhat, const float* da,
+                      const float* rot, const float* initial, const int64_t* valid_len_host,
+                      const float* d_m2, const float* d_m1, void* d_xhat, void* d_bhat, float* d_da,
+                      float* d_rot, float* d_initial, void* workspace, size_t ws_bytes, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* mm_status_string(mm_status status);
+
+/* Which kernel path a call with this problem takes: 0 = SIMT fp32, 1 = tcgen05 tensor-core
+ * path; -1 if the problem is invalid.  Host-only. */
+int mm_path(const mm_problem* prob, int backward);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GB300_MOMENTS_H */

@@ -1,0 +1,209 @@
+"""Thin ctypes binding of libmoments.so (argument marshalling only).
+
+Every step of the operator runs in the library's CUDA kernels; PyTorch only provides device
+memory and the current CUDA stream.  There is no CPU fallback: if the library is missing or
+the tensors are not on a CUDA device, the calls raise.
+
+Functions mirror the C ABI in ``include/moments.h``:
+
+* :func:`moments_fwd`  -> (m2 [b,h,r,r], m1 [b,h,r])
+* :func:`moments_bwd`  -> dict of d_xhat, d_bhat, d_da, d_rot, d_initial
+* :class:`Moments` / :func:`moments` -- a ``torch.autograd.Function`` that saves only the
+  five leaf inputs and recomputes everything in the backward.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+MM_F32, MM_BF16 = 0, 1
+ROT = {"none": 0, "pairwise": 1, "half": 2, "quat": 3}
+MM_FLAG_FORCE_GENERIC = 0x1
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda", 5: "nonfinite",
+          6: "timeout"}
+
+
+class MomentsError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: status {code} ({STATUS.get(code, '?')})")
+        self.code = code
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("s", ctypes.c_int64), ("C", ctypes.c_int64), ("h", ctypes.c_int64),
+                ("p", ctypes.c_int64), ("r", ctypes.c_int64), ("chunk_len", ctypes.c_int64),
+                ("xb_dtype", ctypes.c_int32), ("rot", ctypes.c_int32), ("rope_dim", ctypes.c_int64),
+                ("quat_blocks", ctypes.c_int64), ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libmoments.so (building it first when absent or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if build_if_missing and not _build.up_to_date():
+                _build.build()
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(f"libmoments.so not found at {_build.LIB}; run the build first")
+            lib = ctypes.CDLL(_build.LIB)
+            vp, i64p, fp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p
+            pp = ctypes.POINTER(Problem)
+            lib.mm_workspace_bytes.argtypes = [pp, ctypes.c_int]
+            lib.mm_workspace_bytes.restype = ctypes.c_size_t
+            lib.mm_path.argtypes = [pp, ctypes.c_int]
+            lib.mm_path.restype = ctypes.c_int
+            lib.mm_status_string.argtypes = [ctypes.c_int]
+            lib.mm_status_string.restype = ctypes.c_char_p
+            lib.moments_fwd.argtypes = [pp, vp, vp, fp, fp, fp, i64p, fp, fp, vp, ctypes.c_size_t, vp]
+            lib.moments_fwd.restype = ctypes.c_int
+            lib.moments_bwd.argtypes = [pp, vp, vp, fp, fp, fp, i64p, fp, fp, vp, vp, fp, fp, fp, vp,
+                                        ctypes.c_size_t, vp]
+            lib.moments_bwd.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+@dataclass(frozen=True)
+class Spec:
+    """Static description of a call: shapes plus rotation flags."""
+    b: int
+    s: int
+    C: int
+    h: int
+    p: int
+    r: int
+    chunk_len: int
+    rot: str = "none"
+    rope_dim: int = 0
+    quat_blocks: int = 0
+    dtype: str = "bf16"
+    force_generic: bool = False
+
+    def problem(self) -> Problem:
+        return Problem(self.b, self.s, self.C, self.h, self.p, self.r, self.chunk_len,
+                       MM_BF16 if self.dtype == "bf16" else MM_F32, ROT[self.rot], self.rope_dim,
+                       self.quat_blocks, MM_FLAG_FORCE_GENERIC if self.force_generic else 0, 0)
+
+    @staticmethod
+    def from_tensors(xhat, bhat, chunk_len, rot="none", rope_dim=0, quat_blocks=0, force_generic=False):
+        b, s, C, h, p = xhat.shape
+        r = bhat.shape[-1]
+        dt = "bf16" if xhat.dtype == torch.bfloat16 else "f32"
+        return Spec(b, s, C, h, p, r, chunk_len, rot, rope_dim, quat_blocks, dt, force_generic)
+
+
+def workspace_bytes(spec: Spec, backward: bool) -> int:
+    return int(load().mm_workspace_bytes(ctypes.byref(spec.problem()), 1 if backward else 0))
+
+
+def path(spec: Spec, backward: bool) -> int:
+    """0 = SIMT fp32 kernels, 1 = tcgen05 tensor-core kernels."""
+    return int(load().mm_path(ctypes.byref(spec.problem()), 1 if backward else 0))
+
+
+def alloc_workspace(spec: Spec, backward: bool, device) -> torch.Tensor:
+    n = max(workspace_bytes(spec, backward), 256)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check_dev(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise RuntimeError("libmoments runs on CUDA tensors only (no CPU fallback)")
+        if t is not None and not t.is_contiguous():
+            raise RuntimeError("libmoments expects contiguous tensors")
+
+
+def _valid_host(valid_len, b):
+    v = torch.as_tensor(valid_len, dtype=torch.int64).reshape(-1).cpu()
+    if v.numel() == 1 and b != 1:
+        v = v.expand(b)
+    return v.contiguous()
+
+
+def moments_fwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, *, workspace=None, stream=None,
+                out=None):
+    """Forward call; returns (m2, m1) fp32 on the inputs' device."""
+    lib = load()
+    _check_dev(xhat, bhat, da, rot, initial)
+    dev = xhat.device
+    m2, m1 = out if out is not None else (
+        torch.empty((spec.b, spec.h, spec.r, spec.r), dtype=torch.float32, device=dev),
+        torch.empty((spec.b, spec.h, spec.r), dtype=torch.float32, device=dev))
+    ws = workspace if workspace is not None else alloc_workspace(spec, False, dev)
+    vh = _valid_host(valid_len, spec.b)
+    st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.moments_fwd(ctypes.byref(spec.problem()), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot),
+                         _ptr(initial), ctypes.cast(vh.data_ptr(), ctypes.POINTER(ctypes.c_int64)),
+                         _ptr(m2), _ptr(m1), _ptr(ws), ws.numel(), ctypes.c_void_p(st))
+    if rc:
+        raise MomentsError(rc, "moments_fwd")
+    return m2, m1
+
+
+def moments_bwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, d_m2, d_m1, *, workspace=None,
+                stream=None, out=None):
+    """Backward call; returns dict d_xhat, d_bhat, d_da, d_rot, d_initial."""
+    lib = load()
+    _check_dev(xhat, bhat, da, rot, initial, d_m2, d_m1)
+    dev = xhat.device
+    if out is None:
+        out = dict(d_xhat=torch.empty_like(xhat), d_bhat=torch.empty_like(bhat), d_da=torch.empty_like(da),
+                   d_rot=torch.empty_like(rot) if rot is not None else None,
+                   d_initial=torch.empty_like(initial))
+    ws = workspace if workspace is not None else alloc_workspace(spec, True, dev)
+    vh = _valid_host(valid_len, spec.b)
+    st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.moments_bwd(ctypes.byref(spec.problem()), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot),
+                         _ptr(initial), ctypes.cast(vh.data_ptr(), ctypes.POINTER(ctypes.c_int64)),
+                         _ptr(d_m2), _ptr(d_m1), _ptr(out["d_xhat"]), _ptr(out["d_bhat"]),
+                         _ptr(out["d_da"]), _ptr(out["d_rot"]), _ptr(out["d_initial"]), _ptr(ws),
+                         ws.numel(), ctypes.c_void_p(st))
+    if rc:
+        raise MomentsError(rc, "moments_bwd")
+    return out
+
+
+class Moments(torch.autograd.Function):
+    """(m2, m1) with the recompute backward: only the five leaf inputs are saved."""
+
+    @staticmethod
+    def forward(ctx, xhat, bhat, da, rot, initial, valid_len, spec):
+        m2, m1 = moments_fwd(spec, xhat, bhat, da, rot, initial, valid_len)
+        ctx.save_for_backward(xhat, bhat, da, rot, initial)
+        ctx.valid_len = valid_len
+        ctx.spec = spec
+        return m2, m1
+
+    @staticmethod
+    def backward(ctx, d_m2, d_m1):
+        xhat, bhat, da, rot, initial = ctx.saved_tensors
+        sp = ctx.spec
+        d_m2 = torch.zeros((sp.b, sp.h, sp.r, sp.r), device=xhat.device) if d_m2 is None else d_m2.contiguous()
+        d_m1 = torch.zeros((sp.b, sp.h, sp.r), device=xhat.device) if d_m1 is None else d_m1.contiguous()
+        g = moments_bwd(ctx.spec, xhat, bhat, da, rot, initial, ctx.valid_len, d_m2, d_m1)
+        return g["d_xhat"], g["d_bhat"], g["d_da"], g["d_rot"], g["d_initial"], None, None
+
+
+def moments(xhat, bhat, da, rot, initial, valid_len, chunk_len, rot_kind="none", rope_dim=0, quat_blocks=0):
+    """Differentiable (m2, m1); see :class:`Moments`."""
+    spec = Spec.from_tensors(xhat, bhat, chunk_len, rot_kind, rope_dim, quat_blocks)
+    return Moments.apply(xhat, bhat, da, rot, initial, valid_len, spec)

@@ -1,0 +1,227 @@
+// abi.cu -- the extern "C" boundary of libmoments.so: validation, workspace layout, dispatch.
+// Declarations and the full contract: include/moments.h.
+#include <cstring>
+
+#include "../../include/moments.h"
+#include "common.cuh"
+#include "fast.h"
+#include "generic.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kTrajSlots = 320;  // blocks of the SIMT backward (>= 2 per SM on 152 SMs)
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+    size_t Hc = 0, Dn = 0, E = 0, dsym = 0, traj = 0, fast = 0, total = 0;
+};
+
+bool valid_problem(const mm_problem* P) {
+    if (!P) return false;
+    if (P->b < 1 || P->s < 1 || P->C < 1 || P->h < 1 || P->p < 1 || P->r < 1 || P->chunk_len < 1) return false;
+    if (P->s % P->chunk_len) return false;
+    if (P->xb_dtype != MM_F32 && P->xb_dtype != MM_BF16) return false;
+    switch (P->rot) {
+        case MM_ROT_NONE: break;
+        case MM_ROT_PAIRWISE:
+            if (P->rope_dim < 0 || P->rope_dim % 2 || P->rope_dim > P->r) return false;
+            break;
+        case MM_ROT_HALF:
+            if (P->rope_dim < 0 || P->rope_dim % 2 || P->r % 2 || P->rope_dim / 2 > P->r / 2) return false;
+            break;
+        case MM_ROT_QUAT:
+            if (P->quat_blocks < 0 || 4 * P->quat_blocks > P->r) return false;
+            break;
+        default: return false;
+    }
+    // sizes the kernels index with 32-bit block coordinates
+    if (P->h > 65535 || P->b > 65535 || P->s / P->chunk_len > (int64_t)1 << 30) return false;
+    if (P->p > 4096 || P->r > 4096 || P->C > 4096 || P->chunk_len > 65536 || P->s > ((int64_t)1 << 31) - 1)
+        return false;
+    return true;
+}
+
+int rot_width(const mm_problem* P) {
+    if (P->rot == MM_ROT_PAIRWISE || P->rot == MM_ROT_HALF) return (int)(P->rope_dim / 2);
+    if (P->rot == MM_ROT_QUAT) return (int)(4 * P->quat_blocks);
+    return 0;
+}
+
+void fill_params(const mm_problem* P, const int64_t* valid_host, MMParams* out) {
+    std::memset(out, 0, sizeof(*out));
+    out->b = (int)P->b; out->s = (int)P->s; out->C = (int)P->C; out->h = (int)P->h;
+    out->p = (int)P->p; out->r = (int)P->r; out->l = (int)P->chunk_len;
+    out->nc = (int)(P->s / P->chunk_len);
+    out->rot = P->rot;
+    out->na = (P->rot == MM_ROT_PAIRWISE || P->rot == MM_ROT_HALF) ? (int)(P->rope_dim / 2) : 0;
+    out->J = (P->rot == MM_ROT_QUAT) ? (int)P->quat_blocks : 0;
+    out->rw = rot_width(P);
+    for (int64_t i = 0; i < P->b && valid_host; ++i) {
+        int64_t v = valid_host[i];
+        out->valid[i] = (int)(v < 0 ? 0 : (v > P->s ? P->s : v));
+    }
+}
+
+int smem_optin_limit() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 232448; }
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 232448;
+    }
+    return v;
+}
+
+bool use_fast(const mm_problem* P, const MMParams& M, int backward) {
+    if (P->flags & MM_FLAG_FORCE_GENERIC) return false;
+    return fast_supported(M, P->xb_dtype == MM_BF16, backward);
+}
+
+Layout layout(const mm_problem* P, int backward) {
+    Layout L;
+    MMParams M;
+    fill_params(P, nullptr, &M);
+    const size_t pr = (size_t)P->p * P->r;
+    const size_t nbh = (size_t)P->b * P->h;
+    const size_t nc = (size_t)(P->s / P->chunk_len);
+    size_t off = 0;
+    L.Hc = off; off = align_up(off + sizeof(float) * nbh * nc * pr);
+    L.Dn = off; off = align_up(off + sizeof(float) * nbh * nc);
+    if (backward) {
+        L.E = off; off = align_up(off + sizeof(float) * nbh * nc * pr);
+        L.dsym = off; off = align_up(off + sizeof(float) * nbh * (size_t)P->r * P->r);
+    }
+    if (use_fast(P, M, backward)) {
+        L.fast = off; off = align_up(off + fast_scratch_bytes(M, backward));
+    } else if (backward) {
+        L.traj = off; off = align_up(off + sizeof(float) * (size_t)kTrajSlots * P->chunk_len * pr);
+    }
+    L.total = off;
+    return L;
+}
+
+template <typename T>
+T* at(void* base, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(base) + off); }
+
+mm_status common_checks(const mm_problem* P, const void* xhat, const void* bhat, const float* da,
+                        const float* rot, const float* initial, const int64_t* valid, void* ws,
+                        size_t ws_bytes, int backward, Layout* L) {
+    if (!valid_problem(P)) return MM_ERR_INVALID_ARG;
+    if (!xhat || !bhat || !da || !initial || !valid) return MM_ERR_INVALID_ARG;
+    if (rot_width(P) > 0 && !rot) return MM_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < P->b; ++i)
+        if (valid[i] < 0) return MM_ERR_INVALID_ARG;
+    if (P->b > MM_MAX_B) return MM_ERR_UNSUPPORTED;
+    *L = layout(P, backward);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) || ws_bytes < L->total) return MM_ERR_WORKSPACE;
+    return MM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mm_workspace_bytes(const mm_problem* prob, int backward) {
+    if (!valid_problem(prob)) return 0;
+    return layout(prob, backward).total;
+}
+
+int mm_path(const mm_problem* prob, int backward) {
+    if (!valid_problem(prob)) return -1;
+    MMParams M;
+    fill_params(prob, nullptr, &M);
+    return use_fast(prob, M, backward) ? 1 : 0;
+}
+
+const char* mm_status_string(mm_status s) {
+    switch (s) {
+        case MM_OK: return "ok";
+        case MM_ERR_INVALID_ARG: return "invalid argument";
+        case MM_ERR_UNSUPPORTED: return "unsupported problem for this build";
+        case MM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MM_ERR_CUDA: return "CUDA launch error";
+        case MM_ERR_NONFINITE: return "non-finite values detected";
+        case MM_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+mm_status moments_fwd(const mm_problem* prob, const void* xhat, const void* bhat, const float* da,
+                      const float* rot, const float* initial, const int64_t* valid_len_host, float* m2,
+                      float* m1, void* workspace, size_t ws_bytes, void* stream) {
+    Layout L;
+    mm_status st = common_checks(prob, xhat, bhat, da, rot, initial, valid_len_host, workspace, ws_bytes, 0, &L);
+    if (st != MM_OK) return st;
+    if (!m2 || !m1) return MM_ERR_INVALID_ARG;
+    MMParams M;
+    fill_params(prob, valid_len_host, &M);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool bf16 = prob->xb_dtype == MM_BF16;
+    const bool fast = use_fast(prob, M, 0);
+    if (!fast && !generic_supported(M, smem_optin_limit())) return MM_ERR_UNSUPPORTED;
+    const size_t nbh = (size_t)prob->b * prob->h;
+    if (cudaMemsetAsync(m2, 0, sizeof(float) * nbh * prob->r * prob->r, cs) != cudaSuccess ||
+        cudaMemsetAsync(m1, 0, sizeof(float) * nbh * prob->r, cs) != cudaSuccess) {
+        cudaGetLastError();
+        return MM_ERR_CUDA;
+    }
+    GenericPtrs A{};
+    A.xhat = xhat; A.bhat = bhat; A.da = da; A.rot = rot; A.initial = initial; A.m2 = m2; A.m1 = m1;
+    A.Hc = at<float>(workspace, L.Hc);
+    A.Dn = at<float>(workspace, L.Dn);
+    cudaError_t e = fast ? fast_fwd(M, A, at<char>(workspace, L.fast), cs) : generic_fwd(M, bf16, A, cs);
+    if (e != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
+    return MM_OK;
+}
+
+mm_status moments_bwd(const mm_problem* prob, const void* xhat, const void* bhat, const float* da,
+                      const float* rot, const float* initial, const int64_t* valid_len_host,
+                      const float* d_m2, const float* d_m1, void* d_xhat, void* d_bhat, float* d_da,
+                      float* d_rot, float* d_initial, void* workspace, size_t ws_bytes, void* stream) {
+    Layout L;
+    mm_status st = common_checks(prob, xhat, bhat, da, rot, initial, valid_len_host, workspace, ws_bytes, 1, &L);
+    if (st != MM_OK) return st;
+    if (!d_m2 || !d_m1 || !d_xhat || !d_bhat || !d_da || !d_initial) return MM_ERR_INVALID_ARG;
+    if (rot_width(prob) > 0 && !d_rot) return MM_ERR_INVALID_ARG;
+    MMParams M;
+    fill_params(prob, valid_len_host, &M);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool bf16 = prob->xb_dtype == MM_BF16;
+    const bool fast = use_fast(prob, M, 1);
+    if (!fast && !generic_supported(M, smem_optin_limit())) return MM_ERR_UNSUPPORTED;
+    const size_t es = bf16 ? 2 : 4;
+    const size_t ntok = (size_t)prob->b * prob->s;
+    const size_t nx = ntok * prob->C * prob->h * prob->p, nb = ntok * prob->C * prob->h * prob->r;
+    const size_t nrot = ntok * prob->h * (size_t)rot_width(prob);
+    GenericPtrs A{};
+    A.xhat = xhat; A.bhat = bhat; A.da = da; A.rot = rot; A.initial = initial;
+    A.dm2 = d_m2; A.dm1 = d_m1; A.dxhat = d_xhat; A.dbhat = d_bhat; A.dda = d_da; A.drot = d_rot;
+    A.dinit = d_initial;
+    A.Hc = at<float>(workspace, L.Hc);
+    A.Dn = at<float>(workspace, L.Dn);
+    A.E = at<float>(workspace, L.E);
+    A.dsym = at<float>(workspace, L.dsym);
+    cudaError_t e;
+    if (fast) {
+        e = fast_bwd(M, A, at<char>(workspace, L.fast), cs);
+    } else {
+        // every gradient position not written by a kernel must read zero
+        if (cudaMemsetAsync(d_xhat, 0, es * nx, cs) != cudaSuccess ||
+            cudaMemsetAsync(d_bhat, 0, es * nb, cs) != cudaSuccess ||
+            cudaMemsetAsync(d_da, 0, sizeof(float) * ntok * prob->h, cs) != cudaSuccess ||
+            (nrot && cudaMemsetAsync(d_rot, 0, sizeof(float) * nrot, cs) != cudaSuccess)) {
+            cudaGetLastError();
+            return MM_ERR_CUDA;
+        }
+        A.traj = at<float>(workspace, L.traj);
+        int64_t chunks = (int64_t)prob->b * prob->h * (prob->s / prob->chunk_len);
+        int grid = (int)(chunks < kTrajSlots ? chunks : kTrajSlots);
+        e = generic_bwd(M, bf16, A, grid, cs);
+    }
+    if (e != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
+    return MM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,34 @@
+// generic.h -- host entry points of the SIMT fp32 kernels (generic.cu).
+#pragma once
+#include "common.cuh"
+
+struct GenericPtrs {
+    const void* xhat;
+    const void* bhat;
+    const float* da;
+    const float* rot;
+    const float* initial;
+    float* m2;
+    float* m1;
+    const float* dm2;
+    const float* dm1;
+    void* dxhat;
+    void* dbhat;
+    float* dda;
+    float* drot;
+    float* dinit;
+    // workspace carve-outs
+    float* Hc;    // [b,h,nc,p,r] carries
+    float* Dn;    // [b,h,nc] chunk decays
+    float* E;     // [b,h,nc,p,r] carry cotangents
+    float* dsym;  // [b,h,r,r] d_m2 + d_m2^T
+    float* traj;  // [grid, l, p, r] per-block chunk state scratch
+};
+
+size_t generic_fwd_smem(const MMParams& P);
+size_t generic_bwd_smem(const MMParams& P);
+size_t generic_correct_smem(const MMParams& P);
+size_t generic_end_smem(const MMParams& P);
+bool generic_supported(const MMParams& P, int smem_limit);
+cudaError_t generic_fwd(const MMParams& P, bool bf16, const GenericPtrs& A, cudaStream_t st);
+cudaError_t generic_bwd(const MMParams& P, bool bf16, const GenericPtrs& A, int grid, cudaStream_t st);

@@ -1,0 +1,121 @@
+"""Host-side checks of libmoments.so that need no GPU: it builds for sm_103a, loads, exports
+every symbol include/moments.h declares, sizes workspaces, and rejects bad arguments before
+enqueuing anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from state_space_model_chunk_gb300 import binding
+from state_space_model_chunk_gb300.binding import Problem, Spec
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if hdr.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", hdr)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+\*?([a-z_][a-z0-9_]*)\s*\(",
+                                text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = binding.load()
+    names = declared_functions()
+    assert {"moments_fwd", "moments_bwd", "mm_workspace_bytes", "mm_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    lib = binding.load()
+    for code in range(7):
+        assert lib.mm_status_string(code)
+    assert lib.mm_status_string(99) == b"unknown status"
+
+
+def base_spec(**kw):
+    d = dict(b=2, s=64, C=1, h=2, p=8, r=16, chunk_len=16, rot="pairwise", rope_dim=8, dtype="f32")
+    d.update(kw)
+    return Spec(**d)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(s=60),                      # chunk_len does not divide s
+    dict(rope_dim=7),                # odd rope_dim
+    dict(rope_dim=18),               # pairwise wider than r
+    dict(rot="half", r=15, rope_dim=2),   # half-split needs even r
+    dict(rot="half", rope_dim=18),   # rope_dim / 2 > r / 2
+    dict(rot="quat", quat_blocks=5), # 4 J > r
+    dict(b=0), dict(p=0), dict(chunk_len=0),
+])
+def test_workspace_query_rejects_invalid(bad):
+    assert binding.workspace_bytes(base_spec(**bad), False) == 0
+    assert binding.workspace_bytes(base_spec(**bad), True) == 0
+    assert binding.path(base_spec(**bad), True) == -1
+
+
+def test_workspace_grows_with_backward_and_is_aligned():
+    f, b = binding.workspace_bytes(base_spec(), False), binding.workspace_bytes(base_spec(), True)
+    assert 0 < f < b and f % 256 == 0 and b % 256 == 0
+
+
+def _call_fwd(spec, ptrs, valid, ws_bytes):
+    lib = binding.load()
+    v = (ctypes.c_int64 * spec.b)(*valid)
+    return lib.moments_fwd(ctypes.byref(spec.problem()), *ptrs[:5], v, ptrs[5], ptrs[6],
+                           ptrs[7], ws_bytes, None)
+
+
+FAKE = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(8)]  # never dereferenced
+
+
+def test_fwd_rejects_before_enqueue():
+    lib = binding.load()
+    spec = base_spec()
+    ws = binding.workspace_bytes(spec, False)
+    bad = Spec(**{**spec.__dict__, "s": 60})
+    assert _call_fwd(bad, FAKE, [60, 60], ws) == 1
+    assert _call_fwd(spec, FAKE, [60, -1], ws) == 1               # negative valid_len
+    nul = list(FAKE)
+    nul[0] = None
+    assert _call_fwd(spec, nul, [60, 60], ws) == 1               # null xhat
+    assert _call_fwd(spec, FAKE, [60, 60], ws - 256) == 3        # workspace too small
+    mis = list(FAKE)
+    mis[7] = ctypes.c_void_p(0x1010)                              # misaligned workspace
+    assert _call_fwd(spec, mis, [60, 60], ws) == 3
+    norot = list(FAKE)
+    norot[3] = None                                               # rot missing but rope_dim > 0
+    assert _call_fwd(spec, norot, [60, 60], ws) == 1
+    big = Spec(**{**spec.__dict__, "b": 600})                      # beyond the parameter block
+    assert _call_fwd(big, FAKE, [1] * 600, binding.workspace_bytes(big, False)) == 2
+
+
+def test_bwd_rejects_before_enqueue():
+    lib = binding.load()
+    spec = base_spec()
+    ws = binding.workspace_bytes(spec, True)
+    v = (ctypes.c_int64 * 2)(60, 60)
+    args = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(14)]
+    args[9] = None  # d_xhat missing
+    rc = lib.moments_bwd(ctypes.byref(spec.problem()), *args[:5], v, *args[5:12], None, ws, None)
+    assert rc in (1, 3)
+    rc = lib.moments_bwd(ctypes.byref(Spec(**{**spec.__dict__, "rope_dim": 3}).problem()),
+                         *[ctypes.c_void_p(0x1000)] * 5, v, *[ctypes.c_void_p(0x1000)] * 7,
+                         ctypes.c_void_p(0x100000), ws, None)
+    assert rc == 1
+
+
+def test_no_cpu_fallback():
+    """The product path refuses CPU tensors instead of computing anything on the host."""
+    import torch
+    x = torch.zeros(1, 16, 1, 1, 8)
+    b = torch.zeros(1, 16, 1, 1, 16)
+    with pytest.raises(RuntimeError):
+        binding.moments_fwd(base_spec(b=1, s=16), x, b, torch.zeros(1, 16, 1), torch.zeros(1, 16, 1, 4),
+                            torch.zeros(1, 1, 8, 16), [16])

@@ -1,0 +1,159 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element by element,
+normwise per output tensor (fp32 inputs <= 1e-4, bf16 inputs <= 2e-2), plus exact zeros for
+every gradient position at or past valid_len."""
+import numpy as np
+import pytest
+import torch
+
+from state_space_model_chunk_gb300 import binding
+from state_space_model_chunk_gb300.binding import Spec
+from state_space_model_chunk_gb300.synthetic import WORKLOADS, Workload, make_inputs, slice_bh
+
+from helpers import GRADS, oracle_bwd, oracle_fwd, rel_err, tolerance
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def spec_of(w, force_generic=False):
+    return Spec(w.b, w.s, w.C, w.h, w.p, w.r, w.chunk_len, w.rot, w.rope_dim, w.quat_blocks, w.dtype,
+                force_generic)
+
+
+def run_gpu(w, inp, force_generic=False):
+    d = {k: v.to(DEV) for k, v in inp.items() if k != "valid_len"}
+    spec = spec_of(w, force_generic)
+    rot = d["rot"] if d["rot"].numel() else None
+    m2, m1 = binding.moments_fwd(spec, d["xhat"], d["bhat"], d["da"], rot, d["initial"], inp["valid_len"])
+    g = binding.moments_bwd(spec, d["xhat"], d["bhat"], d["da"], rot, d["initial"], inp["valid_len"],
+                            d["d_m2"], d["d_m1"])
+    torch.cuda.synchronize()
+    out = dict(m2=m2.cpu(), m1=m1.cpu())
+    for k in GRADS:
+        out[k] = g[k].cpu() if g[k] is not None else torch.zeros(0)
+    return out
+
+
+def check_against_oracle(w, inp, got, label=""):
+    tol = tolerance(w)
+    m2, m1 = oracle_fwd(w, inp)
+    ref = oracle_bwd(w, inp)
+    ref.update(m2=m2, m1=m1)
+    errs = {}
+    for k in ("m2", "m1") + GRADS:
+        r = ref[k]
+        if r.size == 0:
+            continue
+        errs[k] = rel_err(got[k].to(torch.float64).numpy(), r)
+    bad = {k: v for k, v in errs.items() if not (v <= tol)}
+    assert not bad, f"{label} rel errs above {tol}: {bad} (all: {errs})"
+    # positions at or past valid_len carry exactly zero gradient
+    for bb in range(w.b):
+        v = int(min(inp["valid_len"][bb], w.s))
+        for k in ("d_xhat", "d_bhat", "d_da", "d_rot"):
+            t = got[k]
+            if t.numel() and v < w.s:
+                assert torch.count_nonzero(t[bb, v:]) == 0, (label, k, bb)
+    return errs
+
+
+SMALL = [
+    WORKLOADS["tiny_fp32"],
+    WORKLOADS["halfsplit_s1024"],
+    WORKLOADS["quat_s2048"].scaled(name="quat_small", b=2, s=256, h=2),
+    WORKLOADS["large_s4096"].scaled(name="large_small", b=2, s=256, h=2, valid="fixed:200"),
+    WORKLOADS["ragged_s16384"].scaled(name="ragged_small", b=3, s=512, h=2),
+    WORKLOADS["large_s4096"].scaled(name="large_fp32_small", b=1, s=128, h=2, dtype="f32", xb_scale="unit"),
+    WORKLOADS["halfsplit_s1024"].scaled(name="half_partial_rope", b=2, s=192, h=3, rope_dim=20, chunk_len=32),
+    WORKLOADS["large_s4096"].scaled(name="pairwise_r96_c3", b=2, s=128, C=3, h=2, r=96, rope_dim=40),
+    WORKLOADS["quat_s2048"].scaled(name="quat_partial_blocks", b=2, s=128, h=2, quat_blocks=20, C=2),
+    WORKLOADS["tiny_fp32"].scaled(name="norot_odd", b=2, s=48, C=3, h=3, p=5, r=12, chunk_len=12, rot="none",
+                                  rope_dim=0, valid="fixed:37"),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_parity_small(w):
+    inp = make_inputs(w)
+    got = run_gpu(w, inp)
+    check_against_oracle(w, inp, got, w.name)
+
+
+@pytest.mark.parametrize("w", [SMALL[2], SMALL[3], SMALL[4]], ids=["quat", "large", "ragged"])
+def test_parity_generic_path_bf16(w):
+    """The SIMT path on bf16 inputs (forced), same bar."""
+    inp = make_inputs(w)
+    got = run_gpu(w, inp, force_generic=True)
+    check_against_oracle(w, inp, got, w.name + "/generic")
+
+
+@pytest.mark.parametrize("valid", [(0, 256), (256, 0), (1, 255), (64, 65), (1000, 129)])
+def test_parity_valid_len_edges(valid):
+    w = WORKLOADS["large_s4096"].scaled(name="edges", b=2, s=256, h=2, C=2)
+    inp = make_inputs(w)
+    inp["valid_len"] = torch.tensor(valid, dtype=torch.int64)
+    got = run_gpu(w, inp)
+    check_against_oracle(w, inp, got, f"edges{valid}")
+    if valid[0] == 0:
+        assert torch.count_nonzero(got["m2"][0]) == 0 and torch.count_nonzero(got["d_initial"][0]) == 0
+
+
+@pytest.mark.parametrize("l", [1, 8, 256])
+def test_parity_chunk_len_extremes(l):
+    w = WORKLOADS["large_s4096"].scaled(name=f"l{l}", b=1, s=256, h=2, C=2, chunk_len=l, valid="fixed:250")
+    inp = make_inputs(w)
+    got = run_gpu(w, inp)
+    check_against_oracle(w, inp, got, w.name)
+
+
+FULL = ["quat_s2048", "large_s4096", "ragged_s16384"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_parity_full_size_sampled(name):
+    """Full-size workloads in the bench's launch configuration; the oracle checks 6 seeded
+    (batch row, head) pairs one by one (each pair is an independent problem)."""
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    got = run_gpu(w, inp)
+    rng = np.random.default_rng(1234)
+    pairs = sorted({(int(rng.integers(w.b)), int(rng.integers(w.h))) for _ in range(6)})
+    subs = [slice_bh(inp, bb, hh) for bb, hh in pairs]
+    stacked = {k: torch.cat([s[k] for s in subs], dim=0) for k in subs[0]}
+    ws = w.scaled(b=len(pairs), h=1)
+    m2, m1 = oracle_fwd(ws, stacked)
+    ref = oracle_bwd(ws, stacked)
+    ref.update(m2=m2, m1=m1)
+    tol = tolerance(w)
+    for i, (bb, hh) in enumerate(pairs):
+        mine = dict(m2=got["m2"][bb, hh], m1=got["m1"][bb, hh], d_xhat=got["d_xhat"][bb, :, :, hh],
+                    d_bhat=got["d_bhat"][bb, :, :, hh], d_da=got["d_da"][bb, :, hh],
+                    d_rot=got["d_rot"][bb, :, hh], d_initial=got["d_initial"][bb, hh])
+        theirs = dict(m2=ref["m2"][i, 0], m1=ref["m1"][i, 0], d_xhat=ref["d_xhat"][i, :, :, 0],
+                      d_bhat=ref["d_bhat"][i, :, :, 0], d_da=ref["d_da"][i, :, 0],
+                      d_rot=ref["d_rot"][i, :, 0], d_initial=ref["d_initial"][i, 0])
+        for k in theirs:
+            e = rel_err(mine[k].to(torch.float64).numpy(), theirs[k])
+            assert e <= tol, (name, (bb, hh), k, e)
+        v = int(min(inp["valid_len"][bb], w.s))
+        for k in ("d_xhat", "d_bhat", "d_da", "d_rot"):
+            if v < w.s:
+                assert torch.count_nonzero(mine[k][v:]) == 0, (name, k)
+
+
+def test_autograd_function_matches_direct_calls():
+    w = SMALL[3]
+    inp = make_inputs(w)
+    d = {k: v.to(DEV) for k, v in inp.items() if k != "valid_len"}
+    leaves = {k: d[k].clone().float().requires_grad_(True) if k in ("da", "rot", "initial")
+              else d[k].clone().requires_grad_(True) for k in ("xhat", "bhat", "da", "rot", "initial")}
+    m2, m1 = binding.moments(leaves["xhat"], leaves["bhat"], leaves["da"], leaves["rot"], leaves["initial"],
+                             inp["valid_len"], w.chunk_len, w.rot, w.rope_dim, w.quat_blocks)
+    (m2 * d["d_m2"]).sum().add((m1 * d["d_m1"]).sum()).backward()
+    direct = run_gpu(w, inp)
+    assert torch.allclose(m2.detach().cpu(), direct["m2"], rtol=1e-5, atol=1e-5)
+    for k in ("xhat", "bhat", "da", "rot", "initial"):
+        a = leaves[k].grad.float().cpu()
+        b = direct["d_" + k].float()
+        assert torch.allclose(a, b, rtol=1e-5, atol=1e-5), k
