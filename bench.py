@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Throughput of the fused moments forward + recompute backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = moments_fwd + moments_bwd over one batch of the workload (default ``large_s4096``:
+b=8, s=4096, C=4, h=32, p=64, r=128, chunk_len=64, pairwise rope_dim 64, bf16 operands),
+inputs resident in HBM (1.7 GB of operands, far larger than L2, so no flush is needed).
+The metric is tokens/s with tokens = sum_b valid_len[b] (every head of a token counted once).
+Under torchrun each rank runs an independent replica on its own GPU (the operator shards over
+batch rows with no exchange), and ``value`` is all ranks' tokens over the slowest rank's time.
+
+Printed (rank 0, one JSON line): value/ms_per_step from CUDA events on the launching stream;
+``e2e`` through the same C ABI with host buffers (pinned H2D of every input and D2H of m2/m1
+inside the timed region); ``roofline`` of the dominant kernel from per-kernel CUDA events
+recorded inside the library during the timed region; ``cpu_baseline`` = the fp64 oracle on a
+bounded sample of the same workload on the host cores; ``clocks`` sampled with nvidia-smi
+during the timed region; ``gpu_launches`` = library kernel launches in the timed region.
+``--impl reference`` times the oracle itself (CPU) on the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from state_space_model_chunk_gb300 import binding  # noqa: E402
+from state_space_model_chunk_gb300.synthetic import WORKLOADS, make_inputs, slice_bh  # noqa: E402
+
+SM_COUNT_GB300 = 152
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="large_s4096", choices=sorted(WORKLOADS))
+    ap.add_argument("--force-generic", action="store_true", help="time the SIMT kernels")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def tokens_of(inp, s):
+    return int(torch.clamp(inp["valid_len"], 0, s).sum())
+
+
+# ----------------------------------------------------------------- algorithmic counts
+def kernel_flops_per_token_head(name, w):
+    """Dense-contraction + recurrence flops one kernel must do per processed token-head."""
+    p, r, C = w.p, w.r, w.C
+    if name in ("fwd_chunk", "tc_fwd_chunk"):
+        return 2 * p * r * r + 2 * C * p * r + 2 * p * r          # Gram m2, writes, decay step
+    if name in ("bwd_chunk", "tc_bwd_chunk"):
+        return 2 * p * r * r + 6 * C * p * r + 4 * p * r          # d_c, writes + d_xhat + d_bhat, 2 recurrences
+    if name in ("chunk_end", "tc_chunk_end"):
+        return 2 * C * p * r + 2 * p * r
+    if name in ("correct", "tc_correct"):
+        return 6 * C * p * r
+    return 0
+
+
+def kernel_bytes_per_token_head(name, w):
+    e = 2 if w.dtype == "bf16" else 4
+    p, r, C = w.p, w.r, w.C
+    rot = 4 * (w.rope_dim // 2) if w.rot in ("pairwise", "half") else 16 * w.quat_blocks
+    io = C * (p + r) * e
+    if name in ("fwd_chunk", "tc_fwd_chunk"):
+        return io + 4 + rot + 4 * p * r / w.chunk_len
+    if name in ("bwd_chunk", "tc_bwd_chunk"):
+        return 2 * io + 8 + 2 * rot + 8 * p * r / w.chunk_len
+    if name in ("chunk_end", "tc_chunk_end"):
+        return io + 4 + 4 * p * r / w.chunk_len
+    if name in ("correct", "tc_correct"):
+        return 3 * io + 8 + 12 * p * r / w.chunk_len
+    if name in ("carry_scan", "cot_scan"):
+        return 12 * p * r / w.chunk_len
+    return 0
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, \
+        "fallback"
+
+
+# ----------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, inp, pairs, seq):
+    """Run the oracle (fwd + bwd) on (b,h) pairs over the first `seq` tokens; returns seconds."""
+    import oracle
+    subs = [slice_bh(inp, bb, hh) for bb, hh in pairs]
+    st = {k: torch.cat([s[k] for s in subs], 0) for k in subs[0]}
+    f = lambda t: t.to(torch.float64).numpy()
+    x, bh, da = f(st["xhat"][:, :seq]), f(st["bhat"][:, :seq]), f(st["da"][:, :seq])
+    rot = f(st["rot"][:, :seq])
+    vl = np.minimum(st["valid_len"].numpy(), seq)
+    t0 = time.perf_counter()
+    oracle.moments_fwd(x, bh, da, rot, f(st["initial"]), vl, rot_kind=w.rot, rope_dim=w.rope_dim,
+                       quat_blocks=w.quat_blocks)
+    oracle.moments_bwd(x, bh, da, rot, f(st["initial"]), vl, f(st["d_m2"]), f(st["d_m1"]), rot_kind=w.rot,
+                       rope_dim=w.rope_dim, quat_blocks=w.quat_blocks)
+    return time.perf_counter() - t0, int(vl.sum())
+
+
+def cpu_baseline(w, inp, budget_s=15.0):
+    import oracle
+    oracle.build()
+    threads = oracle.threads()
+    rng = np.random.default_rng(0)
+    # calibrate on a short prefix, then size the sample to about `budget_s` seconds
+    pairs = [(int(rng.integers(w.b)), int(rng.integers(w.h))) for _ in range(threads)]
+    probe = min(w.s, 256)
+    dt, _ = oracle_sample(w, inp, pairs, probe)
+    seq = int(min(w.s, max(probe, probe * budget_s / max(dt, 1e-3))))
+    seq = max(w.chunk_len, seq // w.chunk_len * w.chunk_len)
+    dt, toks = oracle_sample(w, inp, pairs, seq)
+    value = toks / w.h / dt  # token-head work divided by heads = tokens of the metric
+    return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(pairs)} (b,h) pairs x first {seq} tokens of {w.name}, fp64 fwd+bwd, "
+                      f"{dt:.1f} s; tokens = token-heads / h"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    threads = oracle.threads()
+    rng = np.random.default_rng(0)
+    pairs = [(int(rng.integers(w.b)), int(rng.integers(w.h))) for _ in range(threads)]
+    seq = min(w.s, 256)
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, pairs, seq)
+    tot_t, tot_tok = 0.0, 0
+    for _ in range(args.steps):
+        dt, toks = oracle_sample(w, inp, pairs, seq)
+        tot_t += dt
+        tot_tok += toks
+    value = tot_tok / w.h / tot_t
+    sample = f"per step {len(pairs)} (b,h) pairs x first {seq} tokens of {w.name}, fp64 fwd+bwd"
+    print(json.dumps({
+        "impl": "reference", "metric": "moments fwd+bwd tokens/s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "b": w.b, "s": w.s, "C": w.C, "h": w.h, "p": w.p, "r": w.r,
+                   "chunk_len": w.chunk_len, "rotation": w.rot},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------------- ours
+def collect_kernels(lib):
+    nk = 16
+    tot = (ctypes.c_double * nk)()
+    cnt = (ctypes.c_int64 * nk)()
+    lib.mm_profile_collect.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), ctypes.c_int]
+    lib.mm_kernel_name.restype = ctypes.c_char_p
+    nkern = lib.mm_profile_collect(tot, cnt, nk)
+    kernels = {}
+    for i in range(max(nkern, 0)):
+        if cnt[i]:
+            kernels[lib.mm_kernel_name(i).decode()] = (tot[i], int(cnt[i]))
+    return kernels
+
+
+def run_ours(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)   # every rank runs its own replica of the workload (weak scaling)
+    ntok = tokens_of(inp, w.s)
+    spec = binding.Spec(w.b, w.s, w.C, w.h, w.p, w.r, w.chunk_len, w.rot, w.rope_dim, w.quat_blocks, w.dtype,
+                        args.force_generic)
+    lib = binding.load()
+    d = {k: v.to(dev) for k, v in inp.items() if k != "valid_len"}
+    rot = d["rot"] if d["rot"].numel() else None
+    ws_f = binding.alloc_workspace(spec, False, dev)
+    ws_b = binding.alloc_workspace(spec, True, dev)
+    m2 = torch.empty((w.b, w.h, w.r, w.r), device=dev)
+    m1 = torch.empty((w.b, w.h, w.r), device=dev)
+    grads = dict(d_xhat=torch.empty_like(d["xhat"]), d_bhat=torch.empty_like(d["bhat"]),
+                 d_da=torch.empty_like(d["da"]), d_rot=torch.empty_like(d["rot"]) if rot is not None else None,
+                 d_initial=torch.empty_like(d["initial"]))
+    stream = torch.cuda.current_stream(dev)
+    vl = inp["valid_len"]
+
+    def step(src):
+        r_ = src["rot"] if rot is not None else None
+        binding.moments_fwd(spec, src["xhat"], src["bhat"], src["da"], r_, src["initial"], vl, workspace=ws_f,
+                            out=(m2, m1))
+        binding.moments_bwd(spec, src["xhat"], src["bhat"], src["da"], r_, src["initial"], vl, src["d_m2"],
+                            src["d_m1"], workspace=ws_b, out=grads)
+
+    warm = max(args.warmup, 3)
+    for _ in range(warm):
+        step(d)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    lib.mm_profile_enable(1)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(d)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    lib.mm_profile_enable(0)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    clk = clocks.stop()
+    kernels = collect_kernels(lib)
+    launches = sum(c for _, c in kernels.values())
+    lib.mm_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    dev_status = [int(lib.mm_device_status(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(stream.cuda_stream)))
+                  for ws in (ws_f, ws_b)]
+
+    t = torch.tensor([ms], device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = world * ntok / (ms_max / 1e3)
+
+    # ---- e2e: host buffers through the same C ABI, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.pin_memory() for k, v in inp.items() if k != "valid_len"}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        m2h = torch.empty_like(m2, device="cpu").pin_memory()
+        m1h = torch.empty_like(m1, device="cpu").pin_memory()
+        d2h = m2h.numel() * 4 + m1h.numel() * 4
+        dd = {k: torch.empty_like(v) for k, v in d.items()}
+        e_steps = max(1, min(args.steps, 10))
+        for _ in range(2):
+            for k in dd:
+                dd[k].copy_(host[k], non_blocking=True)
+            step(dd)
+            m2h.copy_(m2, non_blocking=True)
+            m1h.copy_(m1, non_blocking=True)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            for k in dd:
+                dd[k].copy_(host[k], non_blocking=True)
+            step(dd)
+            m2h.copy_(m2, non_blocking=True)
+            m1h.copy_(m1, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = torch.tensor([e0.elapsed_time(e1) / e_steps], device=dev)
+        if dist:
+            dist.all_reduce(ems, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * ntok / (float(ems.item()) / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": float(ems.item()), "steps": e_steps}
+        del dd
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = measured_peaks()
+    roof = None
+    if kernels:
+        name, (tms, nl) = max(kernels.items(), key=lambda kv: kv[1][0])
+        token_heads = sum(min(int(v), w.s) for v in vl) * w.h
+        per_launch_ms = tms / nl
+        fl = kernel_flops_per_token_head(name, w) * token_heads
+        by = kernel_bytes_per_token_head(name, w) * token_heads
+        sm_mhz = clk.get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
+        if name.startswith("tc_") and fl:
+            achieved = fl / (per_launch_ms / 1e3) / 1e12
+            pk = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+            roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
+                    "traffic": None, "kernel": name,
+                    "peak_source": f"{peak_src} cuBLAS bf16 dense, sustained (kernel timed inside a step)",
+                    "flops_per_launch": fl, "ms_per_launch": per_launch_ms}
+        elif fl:
+            achieved = fl / (per_launch_ms / 1e3) / 1e12
+            pk = SM_COUNT_GB300 * 128 * 2 * sm_mhz * 1e6 / 1e12
+            roof = {"bound": "alu", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
+                    "traffic": None, "kernel": name,
+                    "peak_source": f"fp32 FMA: 152 SMs x 128 lanes x 2 flop x {sm_mhz:.0f} MHz (median sampled)",
+                    "flops_per_launch": fl, "ms_per_launch": per_launch_ms}
+        else:
+            achieved = by / (per_launch_ms / 1e3) / 1e9
+            pk = peaks["hbm_gbs"]
+            roof = {"bound": "hbm", "achieved": achieved, "peak": pk, "unit": "GB/s", "frac": achieved / pk,
+                    "traffic": None, "kernel": name, "peak_source": f"{peak_src} HBM copy",
+                    "bytes_per_launch": by, "ms_per_launch": per_launch_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp)
+
+    if rank == 0:
+        line = {
+            "metric": "moments fwd+bwd tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": warm, "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "b": w.b, "s": w.s, "C": w.C, "h": w.h, "p": w.p, "r": w.r,
+                       "chunk_len": w.chunk_len, "rotation": w.rot, "rope_dim": w.rope_dim,
+                       "quat_blocks": w.quat_blocks, "tokens_per_step": ntok,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "path_fwd": "tcgen05" if binding.path(spec, False) == 1 else "simt",
+                       "path_bwd": "tcgen05" if binding.path(spec, True) == 1 else "simt",
+                       "l2": "inputs larger than L2 (operands 1.7 GB), no flush"},
+            "e2e": e2e, "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu, "clocks": clk,
+            "kernels_ms_per_step": {k: v[0] / args.steps for k, v in kernels.items()},
+            "device_status": dev_status,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -110,6 +110,22 @@ const char* mm_status_string(mm_status status);
  * path; -1 if the problem is invalid.  Host-only. */
 int mm_path(const mm_problem* prob, int backward);
 
+/* ---- optional kernel timing (diagnostics; not needed to use the operator) ----
+ * mm_profile_enable(1) clears previous records and makes every later call record a CUDA event
+ * pair around each kernel it launches, on the call's stream (host overhead: a few microseconds
+ * per launch).  mm_profile_enable(0) stops recording and keeps the records.
+ * mm_profile_collect() waits for the recorded events and writes, per kernel id in [0, n), the
+ * summed device milliseconds and the launch count; it returns the number of kernel ids (or -1
+ * on a CUDA error).  mm_kernel_name() names a kernel id.  Process-global; not for concurrent use. */
+void mm_profile_enable(int on);
+int mm_profile_collect(double* total_ms, int64_t* launches, int n);
+const char* mm_kernel_name(int id);
+
+/* Reads the device error word a previous call left in `workspace` (synchronises `stream`).
+ * MM_OK, or MM_ERR_TIMEOUT if a bounded device-side wait of a tensor-core kernel gave up (the
+ * outputs of that call are then invalid), or MM_ERR_CUDA.  Diagnostic; calls never need it. */
+mm_status mm_device_status(const void* workspace, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,16 +1,20 @@
 // abi.cu -- the extern "C" boundary of libmoments.so: validation, workspace layout, dispatch.
 // Declarations and the full contract: include/moments.h.
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "../../include/moments.h"
 #include "common.cuh"
 #include "fast.h"
 #include "generic.h"
+#include "prof.h"
 
 namespace {
 
 constexpr size_t kAlign = 256;
 constexpr int kTrajSlots = 320;  // blocks of the SIMT backward (>= 2 per SM on 152 SMs)
+constexpr size_t kHeader = 256;  // workspace header: device error word at offset 0
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -83,17 +87,20 @@ Layout layout(const mm_problem* P, int backward) {
     Layout L;
     MMParams M;
     fill_params(P, nullptr, &M);
+    const bool fast = use_fast(P, M, backward);
+    // the tensor-core path keeps its carries at a fixed 64-token granularity
+    const size_t l_eff = fast ? (size_t)fastk_chunk() : (size_t)P->chunk_len;
     const size_t pr = (size_t)P->p * P->r;
     const size_t nbh = (size_t)P->b * P->h;
-    const size_t nc = (size_t)(P->s / P->chunk_len);
-    size_t off = 0;
+    const size_t nc = (size_t)P->s / l_eff;
+    size_t off = kHeader;  // header: device error word
     L.Hc = off; off = align_up(off + sizeof(float) * nbh * nc * pr);
     L.Dn = off; off = align_up(off + sizeof(float) * nbh * nc);
     if (backward) {
         L.E = off; off = align_up(off + sizeof(float) * nbh * nc * pr);
         L.dsym = off; off = align_up(off + sizeof(float) * nbh * (size_t)P->r * P->r);
     }
-    if (use_fast(P, M, backward)) {
+    if (fast) {
         L.fast = off; off = align_up(off + fast_scratch_bytes(M, backward));
     } else if (backward) {
         L.traj = off; off = align_up(off + sizeof(float) * (size_t)kTrajSlots * P->chunk_len * pr);
@@ -121,6 +128,42 @@ mm_status common_checks(const mm_problem* P, const void* xhat, const void* bhat,
 
 }  // namespace
 
+// ------------------------------------------------------------------ optional profiling
+namespace {
+struct ProfRec { int kid; cudaEvent_t a, b; };
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_recs;
+std::vector<cudaEvent_t> g_pool;
+int g_open[KID_COUNT];
+cudaEvent_t take_event() {
+    if (!g_pool.empty()) { cudaEvent_t e = g_pool.back(); g_pool.pop_back(); return e; }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) { cudaGetLastError(); return nullptr; }
+    return e;
+}
+const char* kKernelNames[KID_COUNT] = {
+    "chunk_end", "carry_scan", "fwd_chunk", "dsym", "bwd_chunk", "cot_scan", "correct",
+    "tc_fwd_chunk", "tc_chunk_end", "tc_bwd_chunk", "tc_correct"};
+}  // namespace
+
+void mm_prof_mark(int kid, int begin, cudaStream_t st) {
+    if (!g_prof_on) return;
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    cudaEvent_t e = take_event();
+    if (!e) return;
+    cudaEventRecord(e, st);
+    if (begin) {
+        g_recs.push_back(ProfRec{kid, e, nullptr});
+        g_open[kid] = (int)g_recs.size() - 1;
+    } else if (g_open[kid] >= 0) {
+        g_recs[g_open[kid]].b = e;
+        g_open[kid] = -1;
+    } else {
+        g_pool.push_back(e);
+    }
+}
+
 extern "C" {
 
 size_t mm_workspace_bytes(const mm_problem* prob, int backward) {
@@ -133,6 +176,46 @@ int mm_path(const mm_problem* prob, int backward) {
     MMParams M;
     fill_params(prob, nullptr, &M);
     return use_fast(prob, M, backward) ? 1 : 0;
+}
+
+void mm_profile_enable(int on) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    if (!on) { g_prof_on = false; return; }  // stop recording, keep the records for collection
+    for (auto& r : g_recs) {
+        if (r.a) g_pool.push_back(r.a);
+        if (r.b) g_pool.push_back(r.b);
+    }
+    g_recs.clear();
+    for (int i = 0; i < KID_COUNT; ++i) g_open[i] = -1;
+    g_prof_on = true;
+}
+
+int mm_profile_collect(double* total_ms, int64_t* launches, int n) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    for (int i = 0; i < n && i < KID_COUNT; ++i) { total_ms[i] = 0.0; launches[i] = 0; }
+    for (auto& r : g_recs) {
+        if (!r.a || !r.b || r.kid >= n) continue;
+        if (cudaEventSynchronize(r.b) != cudaSuccess) { cudaGetLastError(); return -1; }
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) { cudaGetLastError(); return -1; }
+        total_ms[r.kid] += ms;
+        launches[r.kid] += 1;
+    }
+    return KID_COUNT;
+}
+
+const char* mm_kernel_name(int id) { return (id >= 0 && id < KID_COUNT) ? kKernelNames[id] : "?"; }
+
+mm_status mm_device_status(const void* workspace, void* stream) {
+    if (!workspace) return MM_ERR_INVALID_ARG;
+    int v = 0;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+        cudaStreamSynchronize(cs) != cudaSuccess) {
+        cudaGetLastError();
+        return MM_ERR_CUDA;
+    }
+    return v ? MM_ERR_TIMEOUT : MM_OK;
 }
 
 const char* mm_status_string(mm_status s) {
@@ -171,6 +254,8 @@ mm_status moments_fwd(const mm_problem* prob, const void* xhat, const void* bhat
     A.xhat = xhat; A.bhat = bhat; A.da = da; A.rot = rot; A.initial = initial; A.m2 = m2; A.m1 = m1;
     A.Hc = at<float>(workspace, L.Hc);
     A.Dn = at<float>(workspace, L.Dn);
+    A.err = at<int>(workspace, 0);
+    if (cudaMemsetAsync(A.err, 0, sizeof(int), cs) != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
     cudaError_t e = fast ? fast_fwd(M, A, at<char>(workspace, L.fast), cs) : generic_fwd(M, bf16, A, cs);
     if (e != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
     return MM_OK;
@@ -203,6 +288,8 @@ mm_status moments_bwd(const mm_problem* prob, const void* xhat, const void* bhat
     A.Dn = at<float>(workspace, L.Dn);
     A.E = at<float>(workspace, L.E);
     A.dsym = at<float>(workspace, L.dsym);
+    A.err = at<int>(workspace, 0);
+    if (cudaMemsetAsync(A.err, 0, sizeof(int), cs) != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
     cudaError_t e;
     if (fast) {
         e = fast_bwd(M, A, at<char>(workspace, L.fast), cs);

@@ -9,3 +9,4 @@ bool fast_supported(const MMParams& P, bool bf16, int backward);
 size_t fast_scratch_bytes(const MMParams& P, int backward);
 cudaError_t fast_fwd(const MMParams& P, const GenericPtrs& A, char* scratch, cudaStream_t st);
 cudaError_t fast_bwd(const MMParams& P, const GenericPtrs& A, char* scratch, cudaStream_t st);
+int fastk_chunk();  // internal chunk length of the tensor-core path

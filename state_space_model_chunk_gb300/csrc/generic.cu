@@ -10,6 +10,7 @@
 // trajectory outlives one chunk (the backward keeps one chunk in a per-block scratch slot).
 #include "common.cuh"
 #include "generic.h"
+#include "prof.h"
 
 namespace {
 
@@ -529,9 +530,13 @@ template <typename T>
 static cudaError_t carries(const MMParams& P, const T* x, const T* bh, const float* da, const float* init,
                            float* Hc, float* Dn, cudaStream_t st) {
     dim3 gch(P.nc, P.h, P.b);
+    mm_prof_mark(KID_CHUNK_END, 1, st);
     k_chunk_end<T><<<gch, NT, generic_end_smem(P), st>>>(P, x, bh, da, Hc, Dn);
+    mm_prof_mark(KID_CHUNK_END, 0, st);
     dim3 gsc((P.p * P.r + 127) / 128, P.h, P.b);
+    mm_prof_mark(KID_CARRY_SCAN, 1, st);
     k_carry_scan<<<gsc, 128, 0, st>>>(P, init, Hc, Dn);
+    mm_prof_mark(KID_CARRY_SCAN, 0, st);
     return cudaGetLastError();
 }
 
@@ -543,7 +548,9 @@ static cudaError_t fwd_impl(const MMParams& P, const GenericPtrs& A, cudaStream_
     const T* bh = (const T*)A.bhat;
     if ((e = carries<T>(P, x, bh, A.da, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
     dim3 gch(P.nc, P.h, P.b);
+    mm_prof_mark(KID_FWD_CHUNK, 1, st);
     k_fwd_chunk<T><<<gch, NT, generic_fwd_smem(P), st>>>(P, x, bh, A.da, A.rot, A.Hc, A.m2, A.m1);
+    mm_prof_mark(KID_FWD_CHUNK, 0, st);
     return cudaGetLastError();
 }
 
@@ -556,15 +563,49 @@ static cudaError_t bwd_impl(const MMParams& P, const GenericPtrs& A, int grid, c
     if ((e = carries<T>(P, x, bh, A.da, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
     int64_t nbh = (int64_t)P.b * P.h;
     int64_t tot = nbh * P.r * P.r;
+    mm_prof_mark(KID_DSYM, 1, st);
     k_dsym<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(A.dm2, A.dsym, nbh, P.r);
+    mm_prof_mark(KID_DSYM, 0, st);
+    mm_prof_mark(KID_BWD_CHUNK, 1, st);
     k_bwd_chunk<T><<<grid, NT, generic_bwd_smem(P), st>>>(P, x, bh, A.da, A.rot, A.Hc, A.dsym, A.dm1,
                                                            (T*)A.dxhat, (T*)A.dbhat, A.dda, A.drot,
                                                            A.E, A.traj);
+    mm_prof_mark(KID_BWD_CHUNK, 0, st);
     dim3 gsc((P.p * P.r + 127) / 128, P.h, P.b);
+    mm_prof_mark(KID_COT_SCAN, 1, st);
     k_cot_scan<<<gsc, 128, 0, st>>>(P, A.E, A.Dn, A.dinit);
+    mm_prof_mark(KID_COT_SCAN, 0, st);
     dim3 gch(P.nc, P.h, P.b);
+    mm_prof_mark(KID_CORRECT, 1, st);
     k_correct<T><<<gch, NT, generic_correct_smem(P), st>>>(P, x, bh, A.da, A.Hc, A.E, (T*)A.dxhat,
                                                             (T*)A.dbhat, A.dda);
+    mm_prof_mark(KID_CORRECT, 0, st);
+    return cudaGetLastError();
+}
+
+cudaError_t generic_carry_scan(const MMParams& P, const float* initial, float* Hc, const float* Dn,
+                               cudaStream_t st) {
+    dim3 gsc((P.p * P.r + 127) / 128, P.h, P.b);
+    mm_prof_mark(KID_CARRY_SCAN, 1, st);
+    k_carry_scan<<<gsc, 128, 0, st>>>(P, initial, Hc, Dn);
+    mm_prof_mark(KID_CARRY_SCAN, 0, st);
+    return cudaGetLastError();
+}
+
+cudaError_t generic_cot_scan(const MMParams& P, float* E, const float* Dn, float* dinit, cudaStream_t st) {
+    dim3 gsc((P.p * P.r + 127) / 128, P.h, P.b);
+    mm_prof_mark(KID_COT_SCAN, 1, st);
+    k_cot_scan<<<gsc, 128, 0, st>>>(P, E, Dn, dinit);
+    mm_prof_mark(KID_COT_SCAN, 0, st);
+    return cudaGetLastError();
+}
+
+cudaError_t generic_dsym(const MMParams& P, const float* dm2, float* dsym, cudaStream_t st) {
+    int64_t nbh = (int64_t)P.b * P.h;
+    int64_t tot = nbh * P.r * P.r;
+    mm_prof_mark(KID_DSYM, 1, st);
+    k_dsym<<<(unsigned)((tot + 255) / 256), 256, 0, st>>>(dm2, dsym, nbh, P.r);
+    mm_prof_mark(KID_DSYM, 0, st);
     return cudaGetLastError();
 }
 

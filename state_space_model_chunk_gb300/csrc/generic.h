@@ -23,6 +23,7 @@ struct GenericPtrs {
     float* E;     // [b,h,nc,p,r] carry cotangents
     float* dsym;  // [b,h,r,r] d_m2 + d_m2^T
     float* traj;  // [grid, l, p, r] per-block chunk state scratch
+    int* err;     // device error word (tensor-core path)
 };
 
 size_t generic_fwd_smem(const MMParams& P);
@@ -32,3 +33,7 @@ size_t generic_end_smem(const MMParams& P);
 bool generic_supported(const MMParams& P, int smem_limit);
 cudaError_t generic_fwd(const MMParams& P, bool bf16, const GenericPtrs& A, cudaStream_t st);
 cudaError_t generic_bwd(const MMParams& P, bool bf16, const GenericPtrs& A, int grid, cudaStream_t st);
+cudaError_t generic_carry_scan(const MMParams& P, const float* initial, float* Hc, const float* Dn,
+                               cudaStream_t st);
+cudaError_t generic_cot_scan(const MMParams& P, float* E, const float* Dn, float* dinit, cudaStream_t st);
+cudaError_t generic_dsym(const MMParams& P, const float* dm2, float* dsym, cudaStream_t st);
