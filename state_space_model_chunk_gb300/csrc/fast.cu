@@ -1,8 +1,147 @@
-// fast.cu -- tcgen05 tensor-core path (not yet enabled: every problem takes the SIMT path).
-#include "fast.h"
+// fast.cu -- host side of the tcgen05 path: eligibility, tensor-map encoding, dispatch.
+#include <cuda.h>
 
-bool fast_supported(const MMParams&, bool, int) { return false; }
+#include <cstring>
+
+#include "fast.h"
+#include "fast_common.cuh"
+#include "generic.h"
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+cudaError_t encode(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank, const void* base, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, dt, rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+MMParams internal_params(const MMParams& P0) {
+    MMParams P = P0;
+    P.l = fastk::FL;
+    P.nc = P.s / fastk::FL;
+    return P;
+}
+
+}  // namespace
+
+namespace fastk {
+
+int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            n = 148;
+        }
+    }
+    return n;
+}
+
+cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, const float* rot, const float* da,
+                        TensorMaps* maps) {
+    const cuuint64_t bs = (cuuint64_t)P.b * P.s;
+    cudaError_t e;
+    {   // xhat as [b*s, C, h, p] bf16; box = the C rows of one (token, head)
+        cuuint64_t dims[4] = {(cuuint64_t)P.p, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
+        cuuint64_t str[3] = {(cuuint64_t)P.p * 2, (cuuint64_t)P.h * P.p * 2, (cuuint64_t)P.C * P.h * P.p * 2};
+        cuuint32_t box[4] = {64, 1, (cuuint32_t)P.C, 1};
+        if ((e = encode(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, xhat, dims, str, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
+    }
+    {   // bhat as [b*s, C, h, r/64, 64] bf16; box = one 64-wide half of the C rows
+        cuuint64_t dims[5] = {64, (cuuint64_t)P.r / 64, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
+        cuuint64_t str[4] = {128, (cuuint64_t)P.r * 2, (cuuint64_t)P.h * P.r * 2, (cuuint64_t)P.C * P.h * P.r * 2};
+        cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)P.C, 1};
+        if ((e = encode(&maps->b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bhat, dims, str, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
+    }
+    if (P.rw > 0) {  // rot as [b*s, h, rw] fp32; box = one (token, head)
+        cuuint64_t dims[3] = {(cuuint64_t)P.rw, (cuuint64_t)P.h, bs};
+        cuuint64_t str[2] = {(cuuint64_t)P.rw * 4, (cuuint64_t)P.h * P.rw * 4};
+        cuuint32_t box[3] = {(cuuint32_t)P.rw, 1, 1};
+        if ((e = encode(&maps->rot, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, rot, dims, str, box,
+                        CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+            return e;
+    } else {
+        std::memset(&maps->rot, 0, sizeof(maps->rot));
+    }
+    {   // da as [b*s, h] fp32; box = 4 heads of one token (16 bytes)
+        cuuint64_t dims[2] = {(cuuint64_t)P.h, bs};
+        cuuint64_t str[1] = {(cuuint64_t)P.h * 4};
+        cuuint32_t box[2] = {4, 1};
+        if ((e = encode(&maps->da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, da, dims, str, box,
+                        CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace fastk
+
+int fastk_chunk() { return fastk::FL; }
+
+bool fast_supported(const MMParams& P, bool bf16, int backward) {
+    if (!bf16 || backward) return false;
+    if (P.p != 64 || (P.r != 64 && P.r != 128) || P.C < 1 || P.C > 8) return false;
+    if (P.s % fastk::FL || P.h % 4 || P.b > MM_MAX_B) return false;
+    // rows of angles / quaternions are copied as 16-byte multiples, at most 128 floats
+    if (P.rw % 4 || P.rw > 128) return false;
+    if (!encode_fn()) return false;
+    return true;
+}
+
 size_t fast_scratch_bytes(const MMParams&, int) { return 0; }
-cudaError_t fast_fwd(const MMParams&, const GenericPtrs&, char*, cudaStream_t) { return cudaErrorNotSupported; }
+
+cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char*, cudaStream_t st) {
+    using namespace fastk;
+    const MMParams P = internal_params(P0);
+    FastArgs fa;
+    std::memset(&fa, 0, sizeof(fa));
+    fa.P = P;
+    fa.layoutB = (P.rot == ROT_HALF && P.r == 64) ? 1 : 0;
+    fa.items = count_items(P);
+    fa.Hc = A.Hc;
+    fa.Dn = A.Dn;
+    fa.m2 = A.m2;
+    fa.m1 = A.m1;
+    fa.err = A.err;
+    if (fa.items == 0) return cudaSuccess;  // nothing valid: m2 / m1 stay zero
+    TensorMaps maps;
+    cudaError_t e = encode_maps(P, A.xhat, A.bhat, A.rot, A.da, &maps);
+    if (e != cudaSuccess) return e;
+    const int grid = fa.items < sm_count() ? fa.items : sm_count();
+    if ((e = launch_tc_fwd(CHUNK_END, fa, maps, grid, st)) != cudaSuccess) return e;
+    if ((e = generic_carry_scan(P, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
+    return launch_tc_fwd(FWD_MOMENTS, fa, maps, grid, st);
+}
+
 cudaError_t fast_bwd(const MMParams&, const GenericPtrs&, char*, cudaStream_t) { return cudaErrorNotSupported; }
-int fastk_chunk() { return 64; }

@@ -1,0 +1,224 @@
+// fast_common.cuh -- pieces shared by the tensor-core kernels: launch arguments, the work-item
+// enumeration (pairs of 64-token chunks of one (batch row, head)), the per-thread column
+// groups of a 128-column row, and the register-level de-rotation / its transpose.
+#pragma once
+#include <cuda.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace fastk {
+
+constexpr int FL = 64;   // internal chunk length of the tensor-core path
+constexpr int NCW = 8;   // compute warps (two threads per 128-column row)
+enum { FWD_MOMENTS = 0, CHUNK_END = 1 };
+
+struct FastArgs {
+    MMParams P;     // internal chunking: l = 64, nc = s / 64
+    int layoutB;    // 1: half-split rotation with r = 64 (partner columns 32 apart)
+    int items;      // work items (chunk pairs) of the whole problem
+    float* Hc;      // [b,h,nc,p,r] chunk carries / chunk-end states
+    float* Dn;      // [b,h,nc] chunk decays
+    float* m2;
+    float* m1;
+    int* err;       // device error word (0 = fine)
+};
+
+struct TensorMaps {
+    CUtensorMap x, b, rot, da;
+};
+
+__host__ __device__ inline int pairs_of(const MMParams& P, int bb) { return (mm_processed(P, bb) + 1) / 2; }
+
+__host__ inline int count_items(const MMParams& P) {
+    int n = 0;
+    for (int bb = 0; bb < P.b; ++bb) n += P.h * pairs_of(P, bb);
+    return n;
+}
+
+struct Item {
+    int bb, hh, k;   // batch row, head, pair index (chunks 2k and 2k+1)
+    int proc;        // processed chunks of the row
+    int T[2];        // valid tokens of both chunks (T[0] >= T[1])
+    bool exists[2];  // chunk inside the sequence
+    bool seg_first, seg_last;  // first / last item of this CTA's run on (bb, hh)
+};
+
+__device__ inline void locate(const FastArgs& A, int item, int& bb, int& hh, int& k) {
+    const MMParams& P = A.P;
+    int base = 0;
+    for (bb = 0; bb < P.b - 1; ++bb) {
+        int cnt = P.h * pairs_of(P, bb);
+        if (item < base + cnt) break;
+        base += cnt;
+    }
+    const int np = pairs_of(P, bb);
+    const int rem = item - base;
+    hh = rem / np;
+    k = rem - hh * np;
+}
+
+__device__ inline int item_begin(const FastArgs& A, int cta) {
+    return (int)(((int64_t)cta * A.items) / gridDim.x);
+}
+
+__device__ inline Item decode_item(const FastArgs& A, int item) {
+    const MMParams& P = A.P;
+    Item I;
+    locate(A, item, I.bb, I.hh, I.k);
+    I.proc = mm_processed(P, I.bb);
+    for (int ch = 0; ch < 2; ++ch) {
+        const int n = 2 * I.k + ch;
+        I.exists[ch] = n < P.nc;
+        I.T[ch] = n < I.proc ? mm_chunk_rows(P, I.bb, n) : 0;
+    }
+    const int it0 = item_begin(A, blockIdx.x), it1 = item_begin(A, blockIdx.x + 1);
+    I.seg_first = true;
+    I.seg_last = true;
+    if (item > it0) {
+        int b2, h2, k2;
+        locate(A, item - 1, b2, h2, k2);
+        I.seg_first = !(b2 == I.bb && h2 == I.hh);
+    }
+    if (item + 1 < it1) {
+        int b2, h2, k2;
+        locate(A, item + 1, b2, h2, k2);
+        I.seg_last = !(b2 == I.bb && h2 == I.hh);
+    }
+    return I;
+}
+
+struct TokenInfo {
+    bool seg_first, seg_last;
+};
+
+// Flat walk over the tokens of a CTA's items (the MMA issuer's view).
+struct TokenWalk {
+    const FastArgs& A;
+    int it, it1, t;
+    Item I;
+    __device__ TokenWalk(const FastArgs& a, int i0, int i1) : A(a), it(i0), it1(i1), t(0) {
+        if (it < it1) I = decode_item(A, it);
+    }
+    __device__ uint32_t total_tokens() const {
+        uint32_t n = 0;
+        for (int i = it; i < it1; ++i) n += (uint32_t)decode_item(A, i).T[0];
+        return n;
+    }
+    __device__ TokenInfo next() {
+        while (t >= I.T[0] && it + 1 < it1) {
+            ++it;
+            t = 0;
+            I = decode_item(A, it);
+        }
+        TokenInfo ti{I.seg_first && t == 0, I.seg_last && t == I.T[0] - 1};
+        ++t;
+        return ti;
+    }
+};
+
+// Transaction bytes of one chunk's share of a stage: C rows of xhat (64 bf16), C rows of each
+// 64-wide half of bhat, one token's rotation parameters and one 16-byte group of da.
+__host__ __device__ inline uint32_t stage_bytes(const FastArgs& A) {
+    const MMParams& P = A.P;
+    return 128u * P.C + (uint32_t)(P.r / 64) * 128u * P.C + 4u * P.rw + 16u;
+}
+
+// The four 16-column groups of a 128-column row that one thread owns.  Rotation partners
+// always fall in the same thread: pairs (2i, 2i+1); half-split pairs (i, i + 64) for r = 128
+// (layout A) or (i, i + 32) for r = 64 (layout B); quaternion 4-blocks.
+__device__ inline void col_groups(int layoutB, int half, int (&G)[4]) {
+    if (!layoutB) {
+        G[0] = 2 * half; G[1] = 2 * half + 1; G[2] = 4 + 2 * half; G[3] = 5 + 2 * half;
+    } else {
+        G[0] = half; G[1] = 2 + half; G[2] = 4 + 2 * half; G[3] = 5 + 2 * half;
+    }
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void hamilton(float qw, float qx, float qy, float qz, float vw, float vx, float vy,
+                                         float vz, float& ow, float& ox, float& oy, float& oz) {
+    ow = qw * vw - qx * vx - qy * vy - qz * vz;
+    ox = qw * vx + qx * vw + qy * vz - qz * vy;
+    oy = qw * vy - qx * vz + qy * vw + qz * vx;
+    oz = qw * vz + qx * vy - qy * vx + qz * vw;
+}
+
+// out = R_t v on this thread's columns: the de-rotation R(-theta) / Q (x) . (TR = false) or its
+// transpose R(+theta) / conj(Q) (x) . (TR = true).  coef holds cos at [0,128) and sin at
+// [128,256) of the chunk's angles; quat the chunk's raw [J][4] quaternions.
+template <bool TR>
+__device__ __forceinline__ void rotate_regs(const MMParams& P, int layoutB, const int (&G)[4],
+                                            const float (&v)[4][16], const float* coef, const float* quat,
+                                            float (&out)[4][16]) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) out[g][e] = v[g][e];
+    if (P.rot == ROT_PAIRWISE) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                const int k = 16 * G[g] + e;
+                if (k < 2 * P.na) {
+                    const float cs = coef[k >> 1], sn = TR ? -coef[128 + (k >> 1)] : coef[128 + (k >> 1)];
+                    const float x = v[g][e], y = v[g][e + 1];
+                    out[g][e] = cs * x + sn * y;
+                    out[g][e + 1] = -sn * x + cs * y;
+                }
+            }
+    } else if (P.rot == ROT_HALF) {
+        if (!layoutB) {
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+                const int ga = pr, gb = pr + 2;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int k = 16 * G[ga] + e;
+                    if (k < P.na) {
+                        const float cs = coef[k], sn = TR ? -coef[128 + k] : coef[128 + k];
+                        const float x = v[ga][e], y = v[gb][e];
+                        out[ga][e] = cs * x + sn * y;
+                        out[gb][e] = -sn * x + cs * y;
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int k = 16 * G[0] + e;
+                if (k < P.na) {
+                    const float cs = coef[k], sn = TR ? -coef[128 + k] : coef[128 + k];
+                    const float x = v[0][e], y = v[1][e];
+                    out[0][e] = cs * x + sn * y;
+                    out[1][e] = -sn * x + cs * y;
+                }
+            }
+        }
+    } else if (P.rot == ROT_QUAT) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const int blk = (16 * G[g] + e) >> 2;
+                if (blk < P.J) {
+                    const float* Q = quat + 4 * blk;
+                    const float qx = TR ? -Q[1] : Q[1], qy = TR ? -Q[2] : Q[2], qz = TR ? -Q[3] : Q[3];
+                    hamilton(Q[0], qx, qy, qz, v[g][e], v[g][e + 1], v[g][e + 2], v[g][e + 3], out[g][e],
+                             out[g][e + 1], out[g][e + 2], out[g][e + 3]);
+                }
+            }
+    }
+}
+
+// host helpers
+cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, const float* rot, const float* da,
+                        TensorMaps* maps);
+int sm_count();
+cudaError_t launch_tc_fwd(int mode, const FastArgs& args, const TensorMaps& maps, int grid, cudaStream_t st);
+
+}  // namespace fastk

@@ -1,0 +1,394 @@
+// fast_fwd.cu -- tcgen05 / TMA forward of the state-moments operator (bf16 operands, p = 64,
+// r in {64, 128}, C <= 8).
+//
+// One persistent CTA per SM walks a contiguous range of work items; an item is a pair of
+// 64-token chunks of one (batch row, head).  The two chunks share the 128 TMEM lanes:
+// row m = (chunk ch, per-head index p), so every per-token quantity is a 128 x r tile.
+//
+//   warp 8 (TMA)    : per token, xhat/bhat rows of both chunks (128-byte swizzle), the
+//                     token's rotation parameters and da, into a 4-stage ring.
+//   warp 9 (MMA)    : W_t = sum_c xhat_tc (x) bhat_tc for both chunks as ONE block-diagonal
+//                     MMA (M = 128 rows, N = 128, K = 16 = (chunk, channel) rows), into one of
+//                     two TMEM accumulators; then the moment MMAs m2 += c^T [c | 1] over the
+//                     128 rows (8 x K=16 steps, N = 144: column 128 of the ones block gives m1).
+//   warps 0-7       : two threads per row (64 columns each).  h = e^{da} h + W in fp32
+//                     registers (the chunk recurrence h~[t] = d_t h_- + sum_j L[t,j] W_j
+//                     unrolled), de-rotation in registers, masking, bf16 c rows into the
+//                     swizzled smem tile that both moment operands read.
+//
+// The same kernel in "chunk-end" mode starts every chunk from zero and writes the chunk-end
+// state Delta_n = sum_j exp(a_last - a_j) W_j and D_n = exp(a_last) ("backward.rs",
+// boundary_carries), which the carry scan turns into the chunk-entry carries.
+//
+// Every wait is bounded; a wait that gives up sets the workspace error word and the CTA winds
+// down (compute warps keep stepping through their loops so named barriers stay matched).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "fast.h"
+#include "fast_common.cuh"
+#include "prof.h"
+#include "tc.cuh"
+
+namespace fastfwd {
+
+using namespace fastk;
+
+constexpr int NTHR = 320;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int NS = 4;  // staging ring depth
+
+// shared memory map (bytes from a 1024-aligned base)
+constexpr uint32_t C_BYTES = 49152;                    // c tile: 2 x 16 KB halves + 16 KB ones block
+constexpr uint32_t OFF_C = 0;                          // 2 c tiles
+constexpr uint32_t OFF_X = 2 * C_BYTES;                // NS x 4 KB  (16 K-rows x 128 (ch,p))
+constexpr uint32_t OFF_B = OFF_X + NS * 4096;          // NS x 4 KB  (16 K-rows x 128 r)
+constexpr uint32_t OFF_ROT = OFF_B + NS * 4096;        // NS x 2 chunks x 512 B raw rotation
+constexpr uint32_t OFF_DA = OFF_ROT + NS * 1024;       // NS x 2 chunks x 128 B slots (4 heads of da)
+constexpr uint32_t OFF_COEF = OFF_DA + NS * 256;       // 2 x 2 chunks x 256 floats (cos | sin)
+constexpr uint32_t OFF_CTL = OFF_COEF + 2 * 2 * 256 * 4;
+constexpr uint32_t SMEM_BYTES = OFF_CTL + 256 + 1024;
+
+struct Ctl {
+    uint64_t full[NS], empty[NS];
+    uint64_t wfull[2], wfree[2];
+    uint64_t cfull[2], cfree[2];
+    uint64_t segdone, segfree, fin;
+    uint32_t tbase;
+    int abort;
+};
+static_assert(sizeof(Ctl) <= 256, "control block");
+// tensor copies need 128-byte aligned shared destinations (1024 for the swizzled tiles)
+static_assert(OFF_X % 1024 == 0 && OFF_B % 1024 == 0 && OFF_C % 1024 == 0, "swizzled tiles");
+static_assert(OFF_ROT % 128 == 0 && OFF_DA % 128 == 0 && OFF_CTL % 8 == 0, "tensor-copy slots");
+
+constexpr uint32_t TM_W = 0, TM_M2 = 256, TM_COLS = 512;
+
+__device__ __forceinline__ void fail(Ctl* ctl, int* err, int code) {
+    ctl->abort = 1;
+    atomicExch(err, code);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NTHR, 1)
+    tc_fwd_kernel(const __grid_constant__ FastArgs A, const __grid_constant__ CUtensorMap tmx,
+                  const __grid_constant__ CUtensorMap tmb, const __grid_constant__ CUtensorMap tmr,
+                  const __grid_constant__ CUtensorMap tmd) {
+    extern __shared__ unsigned char smraw[];
+    unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    Ctl* ctl = reinterpret_cast<Ctl*>(sm + OFF_CTL);
+    const MMParams& P = A.P;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int R = P.r;
+
+    // ---- work range of this CTA
+    const int it0 = item_begin(A, blockIdx.x), it1 = item_begin(A, blockIdx.x + 1);
+
+    // ---- one-time set-up: zero the staged operand tiles, the ones block, barriers, TMEM
+    for (uint32_t i = tid; i < (OFF_ROT - OFF_X) / 16; i += NTHR)
+        reinterpret_cast<uint4*>(sm + OFF_X)[i] = make_uint4(0, 0, 0, 0);
+    if (MODE == FWD_MOMENTS) {
+        // ones block of both c tiles: column 128 (first column of the block) = 1.0, rest 0
+        for (uint32_t i = tid; i < 2 * 128; i += NTHR) {
+            const uint32_t buf = i >> 7, row = i & 127;
+            unsigned char* base = sm + OFF_C + buf * C_BYTES + 32768;
+            for (uint32_t j = 0; j < 8; ++j) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (j == 0) v.x = 0x3F80u;  // bf16(1.0) in the low half of the first word
+                *reinterpret_cast<uint4*>(base + tc::sw128_chunk(128, 0, row, j)) = v;
+            }
+        }
+    }
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            tc::mbar_init(&ctl->full[s], 1);
+            tc::mbar_init(&ctl->empty[s], 1 + NCW);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&ctl->wfull[i], 1);
+            tc::mbar_init(&ctl->wfree[i], NCW);
+            tc::mbar_init(&ctl->cfull[i], NCW);
+            tc::mbar_init(&ctl->cfree[i], 1);
+        }
+        tc::mbar_init(&ctl->segdone, 1);
+        tc::mbar_init(&ctl->segfree, NCW);
+        tc::mbar_init(&ctl->fin, 1);
+        ctl->abort = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&ctl->tbase, TM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = ctl->tbase;
+    volatile int* abort = &ctl->abort;
+
+    if (warp == WARP_TMA) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            uint32_t q = 0;
+            for (int it = it0; it < it1 && !*abort; ++it) {
+                Item I = decode_item(A, it);
+                for (int t = 0; t < I.T[0] && !*abort; ++t, ++q) {
+                    const uint32_t s = q % NS, u = q / NS;
+                    if (u >= 1 && !tc::mbar_wait(&ctl->empty[s], (u - 1) & 1, abort)) {
+                        fail(ctl, A.err, 11);
+                        break;
+                    }
+                    uint32_t bytes = 0;
+                    for (int ch = 0; ch < 2; ++ch)
+                        if (I.exists[ch]) bytes += stage_bytes(A);
+                    tc::mbar_arrive_expect_tx(&ctl->full[s], bytes);
+                    for (int ch = 0; ch < 2; ++ch) {
+                        if (!I.exists[ch]) continue;
+                        const int row = I.bb * P.s + (2 * I.k + ch) * FL + t;
+                        tc::tma_load_4d(sm + OFF_X + s * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row, &ctl->full[s]);
+                        for (int a = 0; a < R / 64; ++a)
+                            tc::tma_load_5d(sm + OFF_B + s * 4096 + a * 2048 + ch * 1024, &tmb, 0, a, I.hh, 0, row,
+                                            &ctl->full[s]);
+                        if (P.rw)
+                            tc::tma_load_3d(sm + OFF_ROT + s * 1024 + ch * 512, &tmr, 0, I.hh, row, &ctl->full[s]);
+                        tc::tma_load_2d(sm + OFF_DA + s * 256 + ch * 128, &tmd, I.hh & ~3, row, &ctl->full[s]);
+                    }
+                }
+            }
+            // drain: every issued stage must land before the CTA exits (own bounded wait,
+            // independent of the abort flag)
+            int never = 0;
+            for (uint32_t s = 0; s < NS && q > s; ++s) {
+                const uint32_t last = (q - 1 - s) / NS;  // last use index of stage s
+                tc::mbar_wait(&ctl->full[s], last & 1, &never, 1u << 20);
+            }
+        }
+    } else if (warp == WARP_MMA) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            const uint32_t idW = tc::idesc_bf16(128, 128, 1, 1);
+            const uint32_t idM = tc::idesc_bf16(128, 144, 1, 1);
+            const uint32_t xs0 = tc::smem_u32(sm + OFF_X), bs0 = tc::smem_u32(sm + OFF_B);
+            const uint32_t cs0 = tc::smem_u32(sm + OFF_C);
+            TokenWalk walk(A, it0, it1);
+            // W for flat token qq: stage qq % NS, accumulator qq % 2
+            auto issue_w = [&](uint32_t qq) -> bool {
+                const uint32_t s = qq % NS, u = qq / NS, wb = qq & 1, uw = qq >> 1;
+                if (!tc::mbar_wait(&ctl->full[s], u & 1, abort)) return false;
+                if (uw >= 1 && !tc::mbar_wait(&ctl->wfree[wb], (uw - 1) & 1, abort)) return false;
+                tc::tc_fence_after();
+                const uint64_t ad = tc::sdesc_sw128(xs0 + s * 4096, 2048, 1024);
+                const uint64_t bd = tc::sdesc_sw128(bs0 + s * 4096, 2048, 1024);
+                tc::mma_bf16(tbase + TM_W + wb * 128, ad, bd, idW, 0);
+                tc::mma_commit(&ctl->wfull[wb]);
+                tc::mma_commit(&ctl->empty[s]);
+                return true;
+            };
+            const uint32_t ntok = walk.total_tokens();
+            bool ok = ntok == 0 || issue_w(0);
+            uint32_t seg = 0;
+            for (uint32_t q = 0; ok && q < ntok; ++q) {
+                const TokenInfo ti = walk.next();
+                if (q + 1 < ntok && !issue_w(q + 1)) { ok = false; break; }
+                if (MODE == FWD_MOMENTS) {
+                    const uint32_t cb = q & 1, uc = q >> 1;
+                    if (!tc::mbar_wait(&ctl->cfull[cb], uc & 1, abort)) { ok = false; break; }
+                    if (ti.seg_first && seg >= 1 && !tc::mbar_wait(&ctl->segfree, (seg - 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t cbase = cs0 + cb * C_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t d = tc::sdesc_sw128(cbase + ks * 2048, 16384, 1024);
+                        tc::mma_bf16(tbase + TM_M2, d, d, idM, (ti.seg_first && ks == 0) ? 0u : 1u);
+                    }
+                    tc::mma_commit(&ctl->cfree[cb]);
+                    if (ti.seg_last) {
+                        tc::mma_commit(&ctl->segdone);
+                        ++seg;
+                    }
+                }
+            }
+            if (!ok) fail(ctl, A.err, 12);
+            tc::mma_commit(&ctl->fin);
+            int never = 0;  // in-flight MMAs must finish before the TMEM is released
+            tc::mbar_wait(&ctl->fin, 0, &never, 1u << 20);
+        }
+    } else {
+        // ================================================================ compute warps
+        const int half = warp >> 2;              // which 64 columns of the row
+        const int m = ((warp & 3) << 5) + lane;  // TMEM lane = row (chunk, p)
+        const int ch = m >> 6, pp = m & 63;
+        int G[4];
+        col_groups(A.layoutB, half, G);
+        const uint32_t lane_addr = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+        float S[4][16];
+        uint32_t q = 0, seg = 0;
+        bool ok = true;
+        for (int it = it0; it < it1; ++it) {
+            const Item I = decode_item(A, it);
+            const int Tch = I.T[ch];
+            const int n = 2 * I.k + ch;
+            // chunk-entry carry (forward) or zero (chunk-end mode)
+            if (MODE == FWD_MOMENTS && Tch > 0) {
+                const float* src = A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4) {
+                        const int col = 16 * G[g] + e;
+                        const float4 v =
+                            col < R ? *reinterpret_cast<const float4*>(src + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        S[g][e] = v.x; S[g][e + 1] = v.y; S[g][e + 2] = v.z; S[g][e + 3] = v.w;
+                    }
+            } else {
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) S[g][e] = 0.f;
+            }
+            float dsum = 0.f;
+            for (int t = 0; t < I.T[0]; ++t, ++q) {
+                const uint32_t s = q % NS, u = q / NS;
+                ok &= tc::mbar_wait(&ctl->full[s], u & 1, abort);
+                const float da = reinterpret_cast<const float*>(sm + OFF_DA + s * 256 + ch * 128)[I.hh & 3];
+                const float et = __expf(da);
+                dsum += da;
+                const float* rawrot = reinterpret_cast<const float*>(sm + OFF_ROT + s * 1024);
+                float* coef = reinterpret_cast<float*>(sm + OFF_COEF + (q & 1) * 2048);
+                if (MODE == FWD_MOMENTS && (P.rot == ROT_PAIRWISE || P.rot == ROT_HALF)) {
+                    // cos / sin of both chunks' angles, shared by the 256 compute threads
+                    for (int i = tid; i < 2 * P.na; i += NCW * 32) {
+                        const int c2 = i / P.na, a = i - c2 * P.na;
+                        float sv, cv;
+                        sincosf(rawrot[c2 * 128 + a], &sv, &cv);
+                        coef[c2 * 256 + a] = cv;
+                        coef[c2 * 256 + 128 + a] = sv;
+                    }
+                    named_barrier_sync(1, NCW * 32);
+                }
+                // W_t for this row from TMEM
+                const uint32_t wb = q & 1, uw = q >> 1;
+                ok &= tc::mbar_wait(&ctl->wfull[wb], uw & 1, abort);
+                tc::tc_fence_after();
+                float W[4][16];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) tc::tmem_ld16(lane_addr + TM_W + wb * 128 + 16 * G[g], W[g]);
+                tc::tmem_wait_ld();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ctl->wfree[wb]);
+                const bool live = t < Tch;
+                if (live) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) S[g][e] = fmaf(et, S[g][e], W[g][e]);
+                }
+                if (MODE == FWD_MOMENTS) {
+                    float c[4][16];
+                    rotate_regs<false>(P, A.layoutB, G, S, coef + ch * 256, rawrot + ch * 128, c);
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&ctl->empty[s]);
+                    const uint32_t cb = q & 1, uc = q >> 1;
+                    if (uc >= 1) ok &= tc::mbar_wait(&ctl->cfree[cb], (uc - 1) & 1, abort);
+                    unsigned char* ct = sm + OFF_C + cb * C_BYTES;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const uint32_t hv = G[g] >> 2, j0 = 2 * (G[g] & 3);
+#pragma unroll
+                        for (int hj = 0; hj < 2; ++hj) {
+                            uint4 v = make_uint4(0, 0, 0, 0);
+                            if (live) {
+                                v.x = tc::pack_bf16x2(c[g][8 * hj + 0], c[g][8 * hj + 1]);
+                                v.y = tc::pack_bf16x2(c[g][8 * hj + 2], c[g][8 * hj + 3]);
+                                v.z = tc::pack_bf16x2(c[g][8 * hj + 4], c[g][8 * hj + 5]);
+                                v.w = tc::pack_bf16x2(c[g][8 * hj + 6], c[g][8 * hj + 7]);
+                            }
+                            *reinterpret_cast<uint4*>(ct + tc::sw128_chunk(128, hv, m, j0 + hj)) = v;
+                        }
+                    }
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&ctl->cfull[cb]);
+                } else {
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&ctl->empty[s]);
+                }
+            }
+            if (MODE == CHUNK_END) {
+                if (Tch > 0 && half == 0 && pp == 0)
+                    A.Dn[((int64_t)I.bb * P.h + I.hh) * P.nc + n] = __expf(dsum);
+                if (n + 1 < I.proc) {  // the last processed chunk's end state is never consumed
+                    float* dst = A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4) {
+                            const int col = 16 * G[g] + e;
+                            if (col < R)
+                                *reinterpret_cast<float4*>(dst + col) =
+                                    make_float4(S[g][e], S[g][e + 1], S[g][e + 2], S[g][e + 3]);
+                        }
+                }
+            } else if (I.seg_last) {
+                // flush the (b,h) moment accumulator: lanes are rows r1 of m2
+                ok &= tc::mbar_wait(&ctl->segdone, seg & 1, abort);
+                tc::tc_fence_after();
+                float* M2 = A.m2 + ((int64_t)I.bb * P.h + I.hh) * P.r * P.r;
+                float* M1 = A.m1 + ((int64_t)I.bb * P.h + I.hh) * P.r;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float v[16];
+                    const int c0 = 64 * half + 16 * g;
+                    tc::tmem_ld16(lane_addr + TM_M2 + c0, v);
+                    tc::tmem_wait_ld();
+                    if (m < R && c0 < R) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) atomicAdd(M2 + (int64_t)m * P.r + c0 + e, v[e]);
+                    }
+                }
+                if (half == 0) {
+                    float v[8];
+                    tc::tmem_ld8(lane_addr + TM_M2 + 128, v);
+                    tc::tmem_wait_ld();
+                    if (m < R) atomicAdd(M1 + m, v[0]);
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ctl->segfree);
+                ++seg;
+            }
+        }
+        if (!ok) fail(ctl, A.err, 13);
+    }
+    // ---- teardown
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tbase, TM_COLS);
+    }
+}
+
+}  // namespace fastfwd
+
+// ----------------------------------------------------------------------------- host side
+namespace fastk {
+
+cudaError_t launch_tc_fwd(int mode, const FastArgs& args, const TensorMaps& maps, int grid, cudaStream_t st) {
+    using namespace fastfwd;
+    auto kern = mode == FWD_MOMENTS ? tc_fwd_kernel<FWD_MOMENTS> : tc_fwd_kernel<CHUNK_END>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int kid = mode == FWD_MOMENTS ? KID_FAST_FWD : KID_FAST_END;
+    mm_prof_mark(kid, 1, st);
+    kern<<<grid, NTHR, SMEM_BYTES, st>>>(args, maps.x, maps.b, maps.rot, maps.da);
+    mm_prof_mark(kid, 0, st);
+    return cudaGetLastError();
+}
+
+}  // namespace fastk

@@ -21,9 +21,17 @@ def spec_of(w, force_generic=False):
                 force_generic)
 
 
+def expected_fast(w, backward):
+    """Whether the tensor-core kernels implement this workload (else the SIMT kernels run)."""
+    rw = w.rope_dim // 2 if w.rot in ("pairwise", "half") else (4 * w.quat_blocks if w.rot == "quat" else 0)
+    return (w.dtype == "bf16" and w.p == 64 and w.r in (64, 128) and 1 <= w.C <= 8 and w.s % 64 == 0
+            and w.h % 4 == 0 and rw % 4 == 0 and rw <= 128 and not backward)
+
+
 def run_gpu(w, inp, force_generic=False):
     d = {k: v.to(DEV) for k, v in inp.items() if k != "valid_len"}
     spec = spec_of(w, force_generic)
+    assert binding.path(spec, False) == (0 if force_generic else int(expected_fast(w, False))), w.name
     rot = d["rot"] if d["rot"].numel() else None
     m2, m1 = binding.moments_fwd(spec, d["xhat"], d["bhat"], d["da"], rot, d["initial"], inp["valid_len"])
     g = binding.moments_bwd(spec, d["xhat"], d["bhat"], d["da"], rot, d["initial"], inp["valid_len"],
@@ -61,13 +69,13 @@ def check_against_oracle(w, inp, got, label=""):
 SMALL = [
     WORKLOADS["tiny_fp32"],
     WORKLOADS["halfsplit_s1024"],
-    WORKLOADS["quat_s2048"].scaled(name="quat_small", b=2, s=256, h=2),
-    WORKLOADS["large_s4096"].scaled(name="large_small", b=2, s=256, h=2, valid="fixed:200"),
-    WORKLOADS["ragged_s16384"].scaled(name="ragged_small", b=3, s=512, h=2),
+    WORKLOADS["quat_s2048"].scaled(name="quat_small", b=2, s=256, h=4),
+    WORKLOADS["large_s4096"].scaled(name="large_small", b=2, s=256, h=4, valid="fixed:200"),
+    WORKLOADS["ragged_s16384"].scaled(name="ragged_small", b=3, s=512, h=4),
     WORKLOADS["large_s4096"].scaled(name="large_fp32_small", b=1, s=128, h=2, dtype="f32", xb_scale="unit"),
     WORKLOADS["halfsplit_s1024"].scaled(name="half_partial_rope", b=2, s=192, h=3, rope_dim=20, chunk_len=32),
     WORKLOADS["large_s4096"].scaled(name="pairwise_r96_c3", b=2, s=128, C=3, h=2, r=96, rope_dim=40),
-    WORKLOADS["quat_s2048"].scaled(name="quat_partial_blocks", b=2, s=128, h=2, quat_blocks=20, C=2),
+    WORKLOADS["quat_s2048"].scaled(name="quat_partial_blocks", b=2, s=128, h=4, quat_blocks=20, C=2),
     WORKLOADS["tiny_fp32"].scaled(name="norot_odd", b=2, s=48, C=3, h=3, p=5, r=12, chunk_len=12, rot="none",
                                   rope_dim=0, valid="fixed:37"),
 ]
@@ -90,7 +98,7 @@ def test_parity_generic_path_bf16(w):
 
 @pytest.mark.parametrize("valid", [(0, 256), (256, 0), (1, 255), (64, 65), (1000, 129)])
 def test_parity_valid_len_edges(valid):
-    w = WORKLOADS["large_s4096"].scaled(name="edges", b=2, s=256, h=2, C=2)
+    w = WORKLOADS["large_s4096"].scaled(name="edges", b=2, s=256, h=4, C=2)
     inp = make_inputs(w)
     inp["valid_len"] = torch.tensor(valid, dtype=torch.int64)
     got = run_gpu(w, inp)
@@ -101,7 +109,7 @@ def test_parity_valid_len_edges(valid):
 
 @pytest.mark.parametrize("l", [1, 8, 256])
 def test_parity_chunk_len_extremes(l):
-    w = WORKLOADS["large_s4096"].scaled(name=f"l{l}", b=1, s=256, h=2, C=2, chunk_len=l, valid="fixed:250")
+    w = WORKLOADS["large_s4096"].scaled(name=f"l{l}", b=1, s=256, h=4, C=2, chunk_len=l, valid="fixed:250")
     inp = make_inputs(w)
     got = run_gpu(w, inp)
     check_against_oracle(w, inp, got, w.name)
