@@ -126,6 +126,24 @@ const char* mm_kernel_name(int id);
  * outputs of that call are then invalid), or MM_ERR_CUDA.  Diagnostic; calls never need it. */
 mm_status mm_device_status(const void* workspace, void* stream);
 
+/* ---- forward without a caller-provided workspace ----
+ * The source pages have no counterpart to this call; it exists for callers that cannot
+ * allocate device memory: code inside a host framework whose caching allocator owns every
+ * device allocation, latency-critical loops where cudaMalloc / cudaFree may synchronise the
+ * device, or plain C callers that hold only their input and output buffers.
+ * It computes exactly what moments_fwd() computes, with the same arguments minus the workspace.
+ * The scratch is a fixed 16 MiB array that the library keeps in device memory on every GPU that
+ * loads it, until the process exits.  Problems whose forward workspace (mm_workspace_bytes(prob,
+ * 0)) exceeds 16 MiB are rejected with MM_ERR_WORKSPACE before anything is enqueued.  The call
+ * allocates nothing.  The first call on each device looks up the array's device address with
+ * that device current; make that first call before any stream capture.  Every call on a device
+ * shares the one array: calls that can overlap on the GPU (other streams, other host threads)
+ * race on it, so the caller must serialise them.  The array keeps the previous call's contents;
+ * each call initialises everything it reads. */
+mm_status moments_fwd_noalloc(const mm_problem* prob, const void* xhat, const void* bhat, const float* da,
+                              const float* rot, const float* initial, const int64_t* valid_len_host,
+                              float* m2, float* m1, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

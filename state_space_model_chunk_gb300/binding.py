@@ -182,6 +182,29 @@ def moments_bwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, d_m2, d_m1,
     return out
 
 
+def moments_fwd_noalloc(spec: Spec, xhat, bhat, da, rot, initial, valid_len, *, stream=None, out=None):
+    """Forward through ``moments_fwd_noalloc``: no workspace is passed or allocated; the library
+    uses its fixed 16 MiB device scratch (for callers that cannot allocate).  Calls that could
+    overlap on the GPU must be serialised by the caller."""
+    lib = load()
+    fn = lib.moments_fwd_noalloc
+    fn.argtypes = [ctypes.POINTER(Problem)] + [ctypes.c_void_p] * 5 + [ctypes.POINTER(ctypes.c_int64)] + \
+        [ctypes.c_void_p] * 3
+    fn.restype = ctypes.c_int
+    _check_dev(xhat, bhat, da, rot, initial)
+    dev = xhat.device
+    m2, m1 = out if out is not None else (
+        torch.empty((spec.b, spec.h, spec.r, spec.r), dtype=torch.float32, device=dev),
+        torch.empty((spec.b, spec.h, spec.r), dtype=torch.float32, device=dev))
+    vh = _valid_host(valid_len, spec.b)
+    st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+    rc = fn(ctypes.byref(spec.problem()), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot), _ptr(initial),
+            ctypes.cast(vh.data_ptr(), ctypes.POINTER(ctypes.c_int64)), _ptr(m2), _ptr(m1), ctypes.c_void_p(st))
+    if rc:
+        raise MomentsError(rc, "moments_fwd_noalloc")
+    return m2, m1
+
+
 class Moments(torch.autograd.Function):
     """(m2, m1) with the recompute backward: only the five leaf inputs are saved."""
 
