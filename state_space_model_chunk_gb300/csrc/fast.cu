@@ -101,6 +101,10 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
         if ((e = encode(&maps->da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, da, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
             return e;
+        cuuint32_t box64[2] = {4, 64};  // 4 heads x one 64-token chunk
+        if ((e = encode(&maps->da64, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, da, dims, str, box64,
+                        CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+            return e;
     }
     return cudaSuccess;
 }
@@ -110,7 +114,8 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
 int fastk_chunk() { return fastk::FL; }
 
 bool fast_supported(const MMParams& P, bool bf16, int backward) {
-    if (!bf16 || backward) return false;
+    if (!bf16) return false;
+    if (backward && P.C > 4) return false;  // two tokens' channel rows per K=16 step of the prefix
     if (P.p != 64 || (P.r != 64 && P.r != 128) || P.C < 1 || P.C > 8) return false;
     if (P.s % fastk::FL || P.h % 4 || P.b > MM_MAX_B) return false;
     // rows of angles / quaternions are copied as 16-byte multiples, at most 128 floats
@@ -119,7 +124,7 @@ bool fast_supported(const MMParams& P, bool bf16, int backward) {
     return true;
 }
 
-size_t fast_scratch_bytes(const MMParams&, int) { return 0; }
+size_t fast_scratch_bytes(const MMParams&, int backward) { return backward ? fastk::bwd_anchor_bytes() : 0; }
 
 cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char*, cudaStream_t st) {
     using namespace fastk;
@@ -144,4 +149,46 @@ cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char*, cudaStream
     return launch_tc_fwd(FWD_MOMENTS, fa, maps, grid, st);
 }
 
-cudaError_t fast_bwd(const MMParams&, const GenericPtrs&, char*, cudaStream_t) { return cudaErrorNotSupported; }
+cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cudaStream_t st) {
+    using namespace fastk;
+    const MMParams P = internal_params(P0);
+    FastArgs fa;
+    std::memset(&fa, 0, sizeof(fa));
+    fa.P = P;
+    fa.layoutB = (P.rot == ROT_HALF && P.r == 64) ? 1 : 0;
+    fa.items = count_items(P);
+    fa.Hc = A.Hc;
+    fa.Dn = A.Dn;
+    fa.err = A.err;
+    cudaError_t e;
+    // positions at or past valid_len get exactly zero gradient; everything before is written
+    const size_t es = 2;
+    for (int bb = 0; bb < P.b; ++bb) {
+        const size_t v = (size_t)P.valid[bb], tail = (size_t)P.s - v;
+        if (!tail) continue;
+        const size_t row0 = (size_t)bb * P.s + v;
+        if ((e = cudaMemsetAsync(static_cast<char*>(A.dxhat) + es * row0 * P.C * P.h * P.p, 0,
+                                 es * tail * P.C * P.h * P.p, st)) != cudaSuccess ||
+            (e = cudaMemsetAsync(static_cast<char*>(A.dbhat) + es * row0 * P.C * P.h * P.r, 0,
+                                 es * tail * P.C * P.h * P.r, st)) != cudaSuccess ||
+            (e = cudaMemsetAsync(A.dda + row0 * P.h, 0, sizeof(float) * tail * P.h, st)) != cudaSuccess)
+            return e;
+        if (P.rw && (e = cudaMemsetAsync(A.drot + row0 * P.h * P.rw, 0, sizeof(float) * tail * P.h * P.rw, st)) !=
+                        cudaSuccess)
+            return e;
+    }
+    if (fa.items == 0)  // nothing valid: every gradient, d_initial included, is zero
+        return cudaMemsetAsync(A.dinit, 0, sizeof(float) * (size_t)P.b * P.h * P.p * P.r, st);
+    TensorMaps maps;
+    if ((e = encode_maps(P, A.xhat, A.bhat, A.rot, A.da, &maps)) != cudaSuccess) return e;
+    int grid = fa.items < sm_count() ? fa.items : sm_count();
+    if ((e = launch_tc_fwd(CHUNK_END, fa, maps, grid, st)) != cudaSuccess) return e;
+    if ((e = generic_carry_scan(P, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
+    if (grid > kMaxBwdGrid) grid = kMaxBwdGrid;
+    float* anchors = reinterpret_cast<float*>(scratch);
+    if ((e = launch_tc_bwd(0, fa, A.E, anchors, A.dm2, A.dm1, A.dxhat, A.dbhat, A.dda, A.drot, maps, grid, st)) !=
+        cudaSuccess)
+        return e;
+    if ((e = generic_cot_scan(P, A.E, A.Dn, A.dinit, st)) != cudaSuccess) return e;
+    return launch_tc_bwd(1, fa, A.E, anchors, A.dm2, A.dm1, A.dxhat, A.dbhat, A.dda, A.drot, maps, grid, st);
+}

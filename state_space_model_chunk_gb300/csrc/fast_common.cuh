@@ -25,8 +25,10 @@ struct FastArgs {
 };
 
 struct TensorMaps {
-    CUtensorMap x, b, rot, da;
+    CUtensorMap x, b, rot, da, da64;  // da: 4 heads x 1 token; da64: 4 heads x 64 tokens
 };
+
+constexpr int kMaxBwdGrid = 160;  // CTAs of the backward kernels (anchor slots in the workspace)
 
 __host__ __device__ inline int pairs_of(const MMParams& P, int bb) { return (mm_processed(P, bb) + 1) / 2; }
 
@@ -220,5 +222,9 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
                         TensorMaps* maps);
 int sm_count();
 cudaError_t launch_tc_fwd(int mode, const FastArgs& args, const TensorMaps& maps, int grid, cudaStream_t st);
+size_t bwd_anchor_bytes();
+cudaError_t launch_tc_bwd(int mode, const FastArgs& fa, float* E, float* anchors, const float* dm2, const float* dm1,
+                          void* dx, void* db, float* dda, float* drot, const TensorMaps& maps, int grid,
+                          cudaStream_t st);
 
 }  // namespace fastk

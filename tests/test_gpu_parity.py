@@ -25,13 +25,14 @@ def expected_fast(w, backward):
     """Whether the tensor-core kernels implement this workload (else the SIMT kernels run)."""
     rw = w.rope_dim // 2 if w.rot in ("pairwise", "half") else (4 * w.quat_blocks if w.rot == "quat" else 0)
     return (w.dtype == "bf16" and w.p == 64 and w.r in (64, 128) and 1 <= w.C <= 8 and w.s % 64 == 0
-            and w.h % 4 == 0 and rw % 4 == 0 and rw <= 128 and not backward)
+            and w.h % 4 == 0 and rw % 4 == 0 and rw <= 128 and (not backward or w.C <= 4))
 
 
 def run_gpu(w, inp, force_generic=False):
     d = {k: v.to(DEV) for k, v in inp.items() if k != "valid_len"}
     spec = spec_of(w, force_generic)
     assert binding.path(spec, False) == (0 if force_generic else int(expected_fast(w, False))), w.name
+    assert binding.path(spec, True) == (0 if force_generic else int(expected_fast(w, True))), w.name
     rot = d["rot"] if d["rot"].numel() else None
     m2, m1 = binding.moments_fwd(spec, d["xhat"], d["bhat"], d["da"], rot, d["initial"], inp["valid_len"])
     g = binding.moments_bwd(spec, d["xhat"], d["bhat"], d["da"], rot, d["initial"], inp["valid_len"],
