@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--force-generic", action="store_true", help="time the SIMT kernels")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size (profiling runs)")
     return ap.parse_args()
 
 
@@ -248,6 +249,8 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
+    if args.batch:
+        w = w.scaled(b=args.batch)
     inp = make_inputs(w)   # every rank runs its own replica of the workload (weak scaling)
     ntok = tokens_of(inp, w.s)
     spec = binding.Spec(w.b, w.s, w.C, w.h, w.p, w.r, w.chunk_len, w.rot, w.rope_dim, w.quat_blocks, w.dtype,
