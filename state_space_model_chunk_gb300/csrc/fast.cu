@@ -161,7 +161,12 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     fa.Dn = A.Dn;
     fa.err = A.err;
     cudaError_t e;
-    // positions at or past valid_len get exactly zero gradient; everything before is written
+    // d_da and d_rot are accumulated by the kernels (sums over rows and over two passes): start
+    // from zero.  d_xhat / d_bhat at positions at or past valid_len are exactly zero; every
+    // position before is written.
+    const size_t bs = (size_t)P.b * P.s;
+    if ((e = cudaMemsetAsync(A.dda, 0, sizeof(float) * bs * P.h, st)) != cudaSuccess) return e;
+    if (P.rw && (e = cudaMemsetAsync(A.drot, 0, sizeof(float) * bs * P.h * P.rw, st)) != cudaSuccess) return e;
     const size_t es = 2;
     for (int bb = 0; bb < P.b; ++bb) {
         const size_t v = (size_t)P.valid[bb], tail = (size_t)P.s - v;
@@ -170,11 +175,7 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
         if ((e = cudaMemsetAsync(static_cast<char*>(A.dxhat) + es * row0 * P.C * P.h * P.p, 0,
                                  es * tail * P.C * P.h * P.p, st)) != cudaSuccess ||
             (e = cudaMemsetAsync(static_cast<char*>(A.dbhat) + es * row0 * P.C * P.h * P.r, 0,
-                                 es * tail * P.C * P.h * P.r, st)) != cudaSuccess ||
-            (e = cudaMemsetAsync(A.dda + row0 * P.h, 0, sizeof(float) * tail * P.h, st)) != cudaSuccess)
-            return e;
-        if (P.rw && (e = cudaMemsetAsync(A.drot + row0 * P.h * P.rw, 0, sizeof(float) * tail * P.h * P.rw, st)) !=
-                        cudaSuccess)
+                                 es * tail * P.C * P.h * P.r, st)) != cudaSuccess)
             return e;
     }
     if (fa.items == 0)  // nothing valid: every gradient, d_initial included, is zero

@@ -17,12 +17,16 @@
 //            reductions over p, G = derot^T(d_c), the cotangent recurrence g_t = G_t + e_{t+1}
 //            g_{t+1} in registers, d_da_{t+1} = e_{t+1} <g_{t+1}, h_t>, and d_xhat = g bhat^T,
 //            d_bhat = g^T xhat as N = 16 MMAs.  After the chunk: e_n = e_0 g_0.
+//            The span is software-pipelined: while the CUDA cores finish the cotangent work of
+//            token t, the tensor cores already run d_c of token t-1 and the prefix of t-2.
 // CORR   -- adds the carry cotangent dH = dH(n+1) of every chunk but the last processed one:
 //   d_xhat_jc += sc_j dH bhat_jc, d_bhat_jc += sc_j dH^T xhat_jc (the same N = 16 MMAs with the
 //   constant bf16 dH tile), d_da_s += D_n <dH, h_-> + sum_{j<s} sc_j <dH, W_j>, sc_j = e^{a_last-a_j}.
 //
-// Warp roles: 0-7 compute (two threads per row, 64 columns each), 8 TMA, 9 MMA.  Every wait is
-// bounded; a timeout sets the workspace error word and the CTA winds down.
+// Warp roles: 0-7 compute (two threads per row, 64 columns each, handled as two 32-column
+// passes whose rotation partners stay inside the pass), 8 TMA, 9 MMA.  d_rot and d_da are summed
+// over p with warp transpose-reductions and added to global memory (zeroed by the host).  Every
+// wait is bounded; a timeout sets the workspace error word and the CTA winds down.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -53,13 +57,12 @@ constexpr uint32_t OFF_RING = OFF_PB;            // ring stage s: X at +8 KB s, 
 constexpr uint32_t OFF_ROT = 196608;             // span rotation rows, 8 tokens x 2 chunks x 512 B
 constexpr uint32_t OFF_IDA = 204800;             // item da: 2 chunks x 64 tokens x 4 heads fp32
 constexpr uint32_t OFF_ACUM = 206848;            // cumulative da, 2 chunks x 64 fp32
-constexpr uint32_t OFF_COEF = 207360;            // 2 bufs x 2 chunks x 256 fp32 (cos | sin)
-constexpr uint32_t OFF_M1 = 211456;              // d_m1 [128] fp32
-constexpr uint32_t OFF_RED = 211968;             // 2 bufs x 2 chunks x 128 fp32 d_rot partials
-constexpr uint32_t OFF_RDA = 214016;             // 2 bufs x 2 chunks fp32 d_da partials (+ pad)
-constexpr uint32_t OFF_OM = 214144;              // correction: 2 chunks x 64 fp32 omega_j
-constexpr uint32_t OFF_BASE = 214656;            // correction: 2 chunks fp32 base terms (+ pad)
-constexpr uint32_t OFF_CTL = 214784;
+constexpr uint32_t OFF_COEF = 207360;            // span cos|sin: 8 tokens x 2 chunks x 128 fp32
+constexpr uint32_t OFF_LT = 215552;              // span decay matrix L: 2 chunks x 8 x 8 fp32
+constexpr uint32_t OFF_M1 = 216064;              // d_m1 [128] fp32
+constexpr uint32_t OFF_OM = 216576;              // correction: 2 chunks x 64 fp32 omega_j
+constexpr uint32_t OFF_MISC = 217088;            // correction: dot / base terms
+constexpr uint32_t OFF_CTL = 217216;
 constexpr uint32_t SMEM_BYTES = OFF_CTL + 512 + 1024;
 static_assert(OFF_SX % 1024 == 0 && OFF_SB % 1024 == 0 && OFF_PB % 1024 == 0 && OFF_PA % 1024 == 0, "tiles");
 static_assert(OFF_ROT % 128 == 0 && OFF_IDA % 128 == 0 && OFF_CTL % 8 == 0, "tensor-copy slots");
@@ -93,8 +96,8 @@ struct BwdArgs {
     const float* dm1;   // [b,h,r]
     __nv_bfloat16* dx;  // d_xhat
     __nv_bfloat16* db;  // d_bhat
-    float* dda;         // d_da
-    float* drot;        // d_rot
+    float* dda;         // d_da (zeroed by the host; LOCAL and CORR add into it)
+    float* drot;        // d_rot (zeroed by the host; LOCAL adds into it)
 };
 
 __device__ __forceinline__ void fail(Ctl* ctl, int* err, int code) {
@@ -102,11 +105,11 @@ __device__ __forceinline__ void fail(Ctl* ctl, int* err, int code) {
     atomicExch(err, code);
 }
 
-// Sum of 32 per-lane values across the warp, transposed: on return v[0] of lane L holds the sum
-// over all lanes of the original v[L].
-__device__ __forceinline__ void transpose_reduce32(float (&v)[32], int lane) {
+// Sum of 16 per-lane values across the warp, transposed: on return v[0] of lane L holds the sum
+// over all lanes of the original v[L & 15].
+__device__ __forceinline__ void transpose_reduce16(float (&v)[16], int lane) {
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
+    for (int off = 8; off >= 1; off >>= 1) {
         const bool upper = (lane & off) != 0;
 #pragma unroll
         for (int i = 0; i < off; ++i) {
@@ -115,58 +118,104 @@ __device__ __forceinline__ void transpose_reduce32(float (&v)[32], int lane) {
             v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Read this thread's 64 columns of row m of a bf16 [128 x 128] swizzled tile as floats.
-__device__ __forceinline__ void read_tile_row(const unsigned char* tile, int m, const int (&G)[4],
-                                              float (&v)[4][16]) {
+// 16 columns (group gcol of 16) of row m of a bf16 [128 x 128] swizzled tile, as floats / from floats.
+__device__ __forceinline__ void read_tile16(const unsigned char* tile, int m, int gcol, float (&v)[16]) {
+    const uint32_t hv = gcol >> 2, j0 = 2 * (gcol & 3);
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const uint32_t hv = G[g] >> 2, j0 = 2 * (G[g] & 3);
-#pragma unroll
-        for (int hj = 0; hj < 2; ++hj) {
-            const uint4 w = *reinterpret_cast<const uint4*>(tile + tc::sw128_chunk(128, hv, m, j0 + hj));
-            v[g][8 * hj + 0] = bf16lo(w.x); v[g][8 * hj + 1] = bf16hi(w.x);
-            v[g][8 * hj + 2] = bf16lo(w.y); v[g][8 * hj + 3] = bf16hi(w.y);
-            v[g][8 * hj + 4] = bf16lo(w.z); v[g][8 * hj + 5] = bf16hi(w.z);
-            v[g][8 * hj + 6] = bf16lo(w.w); v[g][8 * hj + 7] = bf16hi(w.w);
-        }
+    for (int hj = 0; hj < 2; ++hj) {
+        const uint4 w = *reinterpret_cast<const uint4*>(tile + tc::sw128_chunk(128, hv, m, j0 + hj));
+        v[8 * hj + 0] = bf16lo(w.x); v[8 * hj + 1] = bf16hi(w.x);
+        v[8 * hj + 2] = bf16lo(w.y); v[8 * hj + 3] = bf16hi(w.y);
+        v[8 * hj + 4] = bf16lo(w.z); v[8 * hj + 5] = bf16hi(w.z);
+        v[8 * hj + 6] = bf16lo(w.w); v[8 * hj + 7] = bf16hi(w.w);
     }
 }
-__device__ __forceinline__ void write_tile_row(unsigned char* tile, int m, const int (&G)[4], const float (&v)[4][16],
-                                               bool zero) {
+__device__ __forceinline__ void write_tile16(unsigned char* tile, int m, int gcol, const float (&v)[16], bool zero) {
+    const uint32_t hv = gcol >> 2, j0 = 2 * (gcol & 3);
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const uint32_t hv = G[g] >> 2, j0 = 2 * (G[g] & 3);
-#pragma unroll
-        for (int hj = 0; hj < 2; ++hj) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (!zero) {
-                w.x = tc::pack_bf16x2(v[g][8 * hj + 0], v[g][8 * hj + 1]);
-                w.y = tc::pack_bf16x2(v[g][8 * hj + 2], v[g][8 * hj + 3]);
-                w.z = tc::pack_bf16x2(v[g][8 * hj + 4], v[g][8 * hj + 5]);
-                w.w = tc::pack_bf16x2(v[g][8 * hj + 6], v[g][8 * hj + 7]);
-            }
-            *reinterpret_cast<uint4*>(tile + tc::sw128_chunk(128, hv, m, j0 + hj)) = w;
+    for (int hj = 0; hj < 2; ++hj) {
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (!zero) {
+            w.x = tc::pack_bf16x2(v[8 * hj + 0], v[8 * hj + 1]);
+            w.y = tc::pack_bf16x2(v[8 * hj + 2], v[8 * hj + 3]);
+            w.z = tc::pack_bf16x2(v[8 * hj + 4], v[8 * hj + 5]);
+            w.w = tc::pack_bf16x2(v[8 * hj + 6], v[8 * hj + 7]);
         }
+        *reinterpret_cast<uint4*>(tile + tc::sw128_chunk(128, hv, m, j0 + hj)) = w;
     }
-}
-__device__ __forceinline__ void tmem_ld_row(uint32_t addr, const int (&G)[4], float (&v)[4][16]) {
-#pragma unroll
-    for (int g = 0; g < 4; ++g) tc::tmem_ld16(addr + 16 * G[g], v[g]);
-    tc::tmem_wait_ld();
 }
 
-// Parity helpers: a barrier that completes once per use; `n` = number of completed uses waited so far.
+// Slots of a 32-column pass: rotation partners stay inside (half-split, r = 64: slots 0/1).
+template <int LAYB>
+__device__ __forceinline__ int slot_a(int pass) { return LAYB ? 2 * pass : pass; }
+template <int LAYB>
+__device__ __forceinline__ int slot_b(int pass) { return LAYB ? 2 * pass + 1 : pass + 2; }
+
+// (out_a, out_b) = rotation of the two slots of a pass: de-rotation R(-theta) / Q (x) . (TR =
+// false) or its transpose (TR = true).  cf: cos at [0,64), sin at [64,128) of this token and
+// chunk's angles; qt: its raw quaternions.  ka / kb: first column of slot a / b.
+template <int ROTK, int LAYB, bool TR>
+__device__ __forceinline__ void rot_pass(const MMParams& P, int pass, int ka, int kb, float (&a)[16], float (&b)[16],
+                                         const float* cf, const float* qt) {
+    if (ROTK == ROT_PAIRWISE) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            float(&v)[16] = s ? b : a;
+            const int k0 = s ? kb : ka;
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                const int i = (k0 + e) >> 1;
+                if (i < P.na) {
+                    const float cs = cf[i], sn = TR ? -cf[64 + i] : cf[64 + i];
+                    const float x = v[e], y = v[e + 1];
+                    v[e] = cs * x + sn * y;
+                    v[e + 1] = -sn * x + cs * y;
+                }
+            }
+        }
+    } else if (ROTK == ROT_HALF) {
+        if (LAYB && pass == 1) return;  // padding columns of r = 64
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int i = ka + e;
+            if (i < P.na) {
+                const float cs = cf[i], sn = TR ? -cf[64 + i] : cf[64 + i];
+                const float x = a[e], y = b[e];
+                a[e] = cs * x + sn * y;
+                b[e] = -sn * x + cs * y;
+            }
+        }
+    } else if (ROTK == ROT_QUAT) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            float(&v)[16] = s ? b : a;
+            const int k0 = s ? kb : ka;
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const int blk = (k0 + e) >> 2;
+                if (blk < P.J) {
+                    const float* Q = qt + 4 * blk;
+                    const float qx = TR ? -Q[1] : Q[1], qy = TR ? -Q[2] : Q[2], qz = TR ? -Q[3] : Q[3];
+                    hamilton(Q[0], qx, qy, qz, v[e], v[e + 1], v[e + 2], v[e + 3], v[e], v[e + 1], v[e + 2], v[e + 3]);
+                }
+            }
+        }
+    }
+}
+
+// Parity helper: a barrier that completes once per use.
 struct Phase {
     uint32_t n = 0;
     __device__ uint32_t next() { return (n++) & 1; }
 };
 
-template <int MODE>
+template <int MODE, int ROTK, int LAYB>
 __global__ void __launch_bounds__(NTHR, 1)
     tc_bwd_kernel(const __grid_constant__ BwdArgs B, const __grid_constant__ CUtensorMap tmx,
                   const __grid_constant__ CUtensorMap tmb, const __grid_constant__ CUtensorMap tmr,
@@ -328,6 +377,34 @@ __global__ void __launch_bounds__(NTHR, 1)
                 if (free_g) tc::mma_commit(&ctl->gfree);
                 return true;
             };
+            auto issue_prefix = [&](int o) -> bool {
+                if (!tc::mbar_wait(&ctl->pafull, ph_pafull.next(), abort)) return false;
+                if (npre >= 1 && !tc::mbar_wait(&ctl->pfree, ph_pfree.next(), abort)) return false;
+                tc::tc_fence_after();
+                const int nk = o / 2 + 1;
+                for (int kq = 0; kq < nk; ++kq)
+                    tc::mma_bf16(tbase + TM_P, tc::sdesc_sw128(s_pa + kq * 2048u, 8192, 1024),
+                                 tc::sdesc_sw128(s_pb + kq * 2048u, 8192, 1024), idPre, kq > 0);
+                ++npre;
+                tc::mma_commit(&ctl->pfull);
+                tc::mma_commit(&ctl->pafree);
+                return true;
+            };
+            auto issue_dc = [&]() -> bool {
+                if (!tc::mbar_wait(&ctl->cfull, ph_cfull.next(), abort)) return false;
+                if (ndc >= 1 && !tc::mbar_wait(&ctl->dcfree, ph_dcfree.next(), abort)) return false;
+                tc::tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t koff = (ks >> 2) * 16384u + 32u * (ks & 3);
+                    tc::mma_bf16(tbase + TM_DC, tc::sdesc_sw128(s_c + koff, 16, 1024),
+                                 tc::sdesc_sw128(s_ds + koff, 16, 1024), idDC, ks > 0);
+                }
+                ++ndc;
+                tc::mma_commit(&ctl->dcfull);
+                tc::mma_commit(&ctl->cfree);
+                return true;
+            };
             for (int it = it0; it < it1 && ok; ++it) {
                 const Item I = decode_item(A, it);
                 for (int t = 0; t < I.T[0] && ok; ++t, ++q) {
@@ -351,35 +428,15 @@ __global__ void __launch_bounds__(NTHR, 1)
                 if (MODE == LOCAL && ok) {
                     const int nsp = (I.T[0] + SPAN - 1) / SPAN;
                     for (int sg = nsp - 1; sg >= 0 && ok; --sg) {
-                        const int s0 = sg * SPAN, len = min(SPAN, I.T[0] - s0);
+                        const int len = min(SPAN, I.T[0] - sg * SPAN);
                         if (!(ok = tc::mbar_wait(&ctl->pbready, ph_pbready.next(), abort))) break;
+                        // pipelined order, matching the compute warps' signals
+                        ok = issue_prefix(len - 1) && issue_dc();
+                        if (ok && len >= 2) ok = issue_prefix(len - 2);
                         for (int o = len - 1; o >= 0 && ok; --o) {
-                            // prefix states of token s0 + o
-                            if (!(ok = tc::mbar_wait(&ctl->pafull, ph_pafull.next(), abort))) break;
-                            if (npre >= 1 && !(ok = tc::mbar_wait(&ctl->pfree, ph_pfree.next(), abort))) break;
-                            tc::tc_fence_after();
-                            const int nk = o / 2 + 1;
-                            for (int kq = 0; kq < nk; ++kq)
-                                tc::mma_bf16(tbase + TM_P, tc::sdesc_sw128(s_pa + kq * 2048u, 8192, 1024),
-                                             tc::sdesc_sw128(s_pb + kq * 2048u, 8192, 1024), idPre, kq > 0);
-                            ++npre;
-                            tc::mma_commit(&ctl->pfull);
-                            tc::mma_commit(&ctl->pafree);
-                            // moments VJP d_c = c (D + D^T)
-                            if (!(ok = tc::mbar_wait(&ctl->cfull, ph_cfull.next(), abort))) break;
-                            if (ndc >= 1 && !(ok = tc::mbar_wait(&ctl->dcfree, ph_dcfree.next(), abort))) break;
-                            tc::tc_fence_after();
-#pragma unroll
-                            for (int ks = 0; ks < 8; ++ks) {
-                                const uint32_t koff = (ks >> 2) * 16384u + 32u * (ks & 3);
-                                tc::mma_bf16(tbase + TM_DC, tc::sdesc_sw128(s_c + koff, 16, 1024),
-                                             tc::sdesc_sw128(s_ds + koff, 16, 1024), idDC, ks > 0);
-                            }
-                            ++ndc;
-                            tc::mma_commit(&ctl->dcfull);
-                            tc::mma_commit(&ctl->cfree);
-                            // d_xhat / d_bhat of the token
-                            if (!(ok = issue_dx(s_sx + o * 4096u, s_sb + o * 4096u, true, true))) break;
+                            ok = issue_dx(s_sx + o * 4096u, s_sb + o * 4096u, true, true);
+                            if (ok && o >= 1) ok = issue_dc();
+                            if (ok && o >= 2) ok = issue_prefix(o - 2);
                         }
                         if (ok) tc::mma_commit(&ctl->spanfree);
                     }
@@ -397,15 +454,15 @@ __global__ void __launch_bounds__(NTHR, 1)
         const int ch = m >> 6, pp = m & 63;
         const int ctid = tid;                    // 0..255
         int G[4];
-        col_groups(A.layoutB, half, G);
+        col_groups(LAYB, half, G);
         const uint32_t lane_addr = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        float* acum = reinterpret_cast<float*>(sm + OFF_ACUM);   // [2][64] inclusive cumsum of da
+        float* acum = reinterpret_cast<float*>(sm + OFF_ACUM);            // [2][64] inclusive cumsum of da
         const float* ida = reinterpret_cast<const float*>(sm + OFF_IDA);  // [2][64][4]
-        float* m1s = reinterpret_cast<float*>(sm + OFF_M1);
-        float* red = reinterpret_cast<float*>(sm + OFF_RED);     // [2 bufs][2 ch][128]
-        float* rda = reinterpret_cast<float*>(sm + OFF_RDA);     // [2 bufs][2 ch]
-        float* om = reinterpret_cast<float*>(sm + OFF_OM);       // [2 ch][64]
-        float* base = reinterpret_cast<float*>(sm + OFF_BASE);   // [2 ch]
+        const float* m1s = reinterpret_cast<const float*>(sm + OFF_M1);
+        float* coefs = reinterpret_cast<float*>(sm + OFF_COEF);           // [8][2][128]
+        float* Lt = reinterpret_cast<float*>(sm + OFF_LT);                // [2][8][8]
+        float* om = reinterpret_cast<float*>(sm + OFF_OM);                // [2][64]
+        float* misc = reinterpret_cast<float*>(sm + OFF_MISC);            // [2] dots, [2] bases
         float* myanchors = B.anchors + (int64_t)blockIdx.x * NANCHOR * 128 * 128;
         Phase ph_itemfull, ph_full[NS], ph_wfull[2], ph_spanfull, ph_pfull, ph_pafree, ph_cfree, ph_dcfull, ph_gfree,
             ph_dxfull;
@@ -420,8 +477,8 @@ __global__ void __launch_bounds__(NTHR, 1)
             // ---- item set-up: cumulative da of both chunks; D + D^T and d_m1 when (b,h) changes
             if (warp < 2) {
                 const int c2 = warp;
-                float v0 = ida[(c2 * 64 + 2 * lane) * 4 + (I.hh & 3)];
-                float v1 = ida[(c2 * 64 + 2 * lane + 1) * 4 + (I.hh & 3)];
+                const float v0 = ida[(c2 * 64 + 2 * lane) * 4 + (I.hh & 3)];
+                const float v1 = ida[(c2 * 64 + 2 * lane + 1) * 4 + (I.hh & 3)];
                 float s = v0 + v1;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -443,8 +500,9 @@ __global__ void __launch_bounds__(NTHR, 1)
                     }
                     *reinterpret_cast<uint32_t*>(ds + tc::sw128_offset(128, r2, r1)) = tc::pack_bf16x2(a0, a1);
                 }
+                float* m1w = reinterpret_cast<float*>(sm + OFF_M1);
                 for (int i = ctid; i < 128; i += NCW * 32)
-                    m1s[i] = i < R ? B.dm1[((int64_t)I.bb * P.h + I.hh) * R + i] : 0.f;
+                    m1w[i] = i < R ? B.dm1[((int64_t)I.bb * P.h + I.hh) * R + i] : 0.f;
                 tc::fence_proxy_async_smem();
             }
             named_barrier_sync(1, NCW * 32);
@@ -457,56 +515,63 @@ __global__ void __launch_bounds__(NTHR, 1)
 
             if (MODE == LOCAL) {
                 // ================================ phase A: forward sweep, anchors
-                float S[4][16];
-                if (Tch > 0) {
-                    const float* src = A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
+                {
+                    float S[4][16];
+                    if (Tch > 0) {
+                        const float* src = A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
 #pragma unroll
-                    for (int g = 0; g < 4; ++g)
+                        for (int g = 0; g < 4; ++g)
 #pragma unroll
-                        for (int e = 0; e < 16; e += 4) {
-                            const int col = 16 * G[g] + e;
-                            const float4 v = col < R ? *reinterpret_cast<const float4*>(src + col)
-                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-                            S[g][e] = v.x; S[g][e + 1] = v.y; S[g][e + 2] = v.z; S[g][e + 3] = v.w;
+                            for (int e = 0; e < 16; e += 4) {
+                                const int col = 16 * G[g] + e;
+                                const float4 v = col < R ? *reinterpret_cast<const float4*>(src + col)
+                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                                S[g][e] = v.x; S[g][e + 1] = v.y; S[g][e + 2] = v.z; S[g][e + 3] = v.w;
+                            }
+                    } else {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) S[g][e] = 0.f;
+                    }
+                    for (int t = 0; t < I.T[0]; ++t, ++q) {
+                        const uint32_t s = q % NS, wb = nw & 1;
+                        ok &= tc::mbar_wait(&ctl->full[s], ph_full[s].next(), abort);
+                        ok &= tc::mbar_wait(&ctl->wfull[wb], ph_wfull[wb].next(), abort);
+                        tc::tc_fence_after();
+                        const float et = t < Tch ? e_of(t) : 1.f;
+                        const float wt = t < Tch ? 1.f : 0.f;
+#pragma unroll
+                        for (int pass = 0; pass < 2; ++pass) {
+                            float W[2][16];
+                            tc::tmem_ld16(lane_addr + (wb ? TM_DC : TM_P) + 16 * G[2 * pass], W[0]);
+                            tc::tmem_ld16(lane_addr + (wb ? TM_DC : TM_P) + 16 * G[2 * pass + 1], W[1]);
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int g = 0; g < 2; ++g)
+#pragma unroll
+                                for (int e = 0; e < 16; ++e)
+                                    S[2 * pass + g][e] = fmaf(et, S[2 * pass + g][e], wt * W[g][e]);
                         }
-                } else {
+                        tc::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tc::mbar_arrive(&ctl->wfree[wb]);
+                            tc::mbar_arrive(&ctl->empty[s]);
+                        }
+                        ++nw;
+                        if ((t + 1) % SPAN == 0 && t + 1 < I.T[0]) {  // anchor of the span starting at t + 1
+                            float* dst = myanchors + ((int64_t)((t + 1) / SPAN - 1) * 128 + m) * 128;
 #pragma unroll
-                    for (int g = 0; g < 4; ++g)
+                            for (int g = 0; g < 4; ++g)
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) S[g][e] = 0.f;
-                }
-                for (int t = 0; t < I.T[0]; ++t, ++q) {
-                    const uint32_t s = q % NS, wb = nw & 1;
-                    ok &= tc::mbar_wait(&ctl->full[s], ph_full[s].next(), abort);
-                    ok &= tc::mbar_wait(&ctl->wfull[wb], ph_wfull[wb].next(), abort);
-                    tc::tc_fence_after();
-                    float W[4][16];
-                    tmem_ld_row(lane_addr + (wb ? TM_DC : TM_P), G, W);
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tc::mbar_arrive(&ctl->wfree[wb]);
-                        tc::mbar_arrive(&ctl->empty[s]);
-                    }
-                    ++nw;
-                    if (t < Tch) {
-                        const float et = e_of(t);
-#pragma unroll
-                        for (int g = 0; g < 4; ++g)
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) S[g][e] = fmaf(et, S[g][e], W[g][e]);
-                    }
-                    if ((t + 1) % SPAN == 0 && t + 1 < I.T[0]) {  // anchor of the span starting at t + 1
-                        float* dst = myanchors + ((int64_t)((t + 1) / SPAN - 1) * 128 + m) * 128;
-#pragma unroll
-                        for (int g = 0; g < 4; ++g)
-#pragma unroll
-                            for (int e = 0; e < 16; e += 4)
-                                *reinterpret_cast<float4*>(dst + 16 * G[g] + e) =
-                                    make_float4(S[g][e], S[g][e + 1], S[g][e + 2], S[g][e + 3]);
+                                for (int e = 0; e < 16; e += 4)
+                                    *reinterpret_cast<float4*>(dst + 16 * G[g] + e) =
+                                        make_float4(S[g][e], S[g][e + 1], S[g][e + 2], S[g][e + 3]);
+                        }
                     }
                 }
-                // ================================ phase B: spans in reverse
+                // ================================ phase B: spans in reverse, software-pipelined
                 float gr[4][16];
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
@@ -518,278 +583,298 @@ __global__ void __launch_bounds__(NTHR, 1)
                     const int s0 = sg * SPAN, len = min(SPAN, I.T[0] - s0);
                     ok &= tc::mbar_wait(&ctl->spanfull, ph_spanfull.next(), abort);
                     // anchor of the span -> TMEM (this thread's row and columns)
-                    {
-                        float av[4][16];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        float av[16];
+                        const int col0 = 16 * G[g];
                         const float* src = sg == 0 ? (A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R)
                                                    : (myanchors + ((int64_t)(sg - 1) * 128 + m) * 128);
-                        const bool have = sg == 0 ? Tch > 0 : true;
+                        const bool have = sg == 0 ? (Tch > 0 && col0 < R) : true;
 #pragma unroll
-                        for (int g = 0; g < 4; ++g)
-#pragma unroll
-                            for (int e = 0; e < 16; e += 4) {
-                                const int col = 16 * G[g] + e;
-                                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                                if (have && (sg > 0 || col < R)) v = *reinterpret_cast<const float4*>(src + col);
-                                av[g][e] = v.x; av[g][e + 1] = v.y; av[g][e + 2] = v.z; av[g][e + 3] = v.w;
-                            }
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) tc::tmem_st16(lane_addr + TM_AN + 16 * G[g], av[g]);
-                        tc::tmem_wait_st();
+                        for (int e = 0; e < 16; e += 4) {
+                            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (have) v = *reinterpret_cast<const float4*>(src + col0 + e);
+                            av[e] = v.x; av[e + 1] = v.y; av[e + 2] = v.z; av[e + 3] = v.w;
+                        }
+                        tc::tmem_st16(lane_addr + TM_AN + col0, av);
                     }
-                    // prefix B tile: rows 8 jj + 4 ch' + c  <-  span bhat tile jj, row 8 ch' + c
-                    for (int i = ctid; i < len * 2 * C * 16; i += NCW * 32) {
-                        const int j16 = i & 15, rowi = i >> 4;
-                        const int c = rowi % C, c2 = (rowi / C) & 1, jj = rowi / (2 * C);
-                        const int srow = 8 * c2 + c, drow = 8 * jj + 4 * c2 + c;
+                    tc::tmem_wait_st();
+                    // prefix B tile: rows 8 jj + 4 ch' + c  <-  span bhat tile jj, row 8 ch' + c; the
+                    // rows of absent channels and of the pad token of an odd span are zeroed (the
+                    // region held the forward sweep's staging ring)
+                    for (int i = ctid; i < ((len + 1) & ~1) * 8 * 16; i += NCW * 32) {
+                        const int j16 = i & 15, drow = i >> 4;
+                        const int jj = drow >> 3, c2 = (drow >> 2) & 1, c = drow & 3;
                         const int hv = j16 >> 3, jc = j16 & 7;
-                        const uint4 v = *reinterpret_cast<const uint4*>(sm + OFF_SB + jj * 4096 + tc::sw128_chunk(16, hv, srow, jc));
+                        uint4 v = make_uint4(0, 0, 0, 0);
+                        if (c < C && jj < len)
+                            v = *reinterpret_cast<const uint4*>(sm + OFF_SB + jj * 4096 +
+                                                                tc::sw128_chunk(16, hv, 8 * c2 + c, jc));
                         *reinterpret_cast<uint4*>(sm + OFF_PB + tc::sw128_chunk(64, hv, drow, jc)) = v;
                     }
+                    // decay matrix L[t, j] of the span, and cos / sin of its angles
+                    if (ctid < 128) {
+                        const int c2 = ctid >> 6, o = (ctid >> 3) & 7, jj = ctid & 7;
+                        const float* ac2 = acum + c2 * 64;
+                        Lt[ctid] = (o < len && jj <= o) ? __expf(ac2[s0 + o] - ac2[s0 + jj]) : 0.f;
+                    }
+                    if (ROTK == ROT_PAIRWISE || ROTK == ROT_HALF) {
+                        for (int i = ctid; i < len * 2 * P.na; i += NCW * 32) {
+                            const int o = i / (2 * P.na), rem = i - o * 2 * P.na;
+                            const int c2 = rem / P.na, a = rem - c2 * P.na;
+                            float sv, cv;
+                            sincosf(reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + c2 * 512)[a], &sv, &cv);
+                            coefs[(o * 2 + c2) * 128 + a] = cv;
+                            coefs[(o * 2 + c2) * 128 + 64 + a] = sv;
+                        }
+                    }
                     tc::fence_proxy_async_smem();
+                    named_barrier_sync(1, NCW * 32);
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(&ctl->pbready);
                     const float a_anchor = s0 > 0 ? ac[s0 - 1] : 0.f;
-                    for (int o = len - 1; o >= 0; --o) {
-                        const int t = s0 + o;
-                        const int buf = t & 1;
-                        // ---- (1) prefix A rows for token t: L[t, s0+jj] xhat, and a zero pair row
+
+                    // ---- prefix A rows for token t: L[t, s0+jj] xhat (two tokens per K step)
+                    auto build_pa = [&](int t) {
+                        const int o = t - s0;
                         if (npa >= 1) ok &= tc::mbar_wait(&ctl->pafree, ph_pafree.next(), abort);
                         ++npa;
-                        {
-                            // rows 8 jj + 4 ch' + c of the K-steps this token uses; a row holds
-                            // L[t, s0+jj] xhat[ch', s0+jj, c, :] in column half ch' and zeros elsewhere
-                            const int nrow_tok = (o % 2 == 0) ? o + 2 : o + 1;
-                            for (int i = ctid; i < nrow_tok * 8 * 16; i += NCW * 32) {
-                                const int j16 = i & 15, drow = i >> 4;
-                                const int jj = drow >> 3, c2 = (drow >> 2) & 1, c = drow & 3;
-                                const int hv = j16 >> 3, jc = j16 & 7;
-                                uint4 w = make_uint4(0, 0, 0, 0);
-                                if (hv == c2 && jj <= o && c < C) {
-                                    const float* ac2 = acum + c2 * 64;
-                                    const float L = __expf(ac2[t] - ac2[s0 + jj]);
-                                    const uint4 v = *reinterpret_cast<const uint4*>(
-                                        sm + OFF_SX + jj * 4096 + tc::sw128_chunk(16, c2, 8 * c2 + c, jc));
-                                    w.x = tc::pack_bf16x2(L * bf16lo(v.x), L * bf16hi(v.x));
-                                    w.y = tc::pack_bf16x2(L * bf16lo(v.y), L * bf16hi(v.y));
-                                    w.z = tc::pack_bf16x2(L * bf16lo(v.z), L * bf16hi(v.z));
-                                    w.w = tc::pack_bf16x2(L * bf16lo(v.w), L * bf16hi(v.w));
-                                }
-                                *reinterpret_cast<uint4*>(sm + OFF_PA + tc::sw128_chunk(64, hv, drow, jc)) = w;
+                        const int nrow_tok = (o % 2 == 0) ? o + 2 : o + 1;
+                        for (int i = ctid; i < nrow_tok * 8 * 16; i += NCW * 32) {
+                            const int j16 = i & 15, drow = i >> 4;
+                            const int jj = drow >> 3, c2 = (drow >> 2) & 1, c = drow & 3;
+                            const int hv = j16 >> 3, jc = j16 & 7;
+                            uint4 w = make_uint4(0, 0, 0, 0);
+                            if (hv == c2 && jj <= o && c < C) {
+                                const float L = Lt[(c2 * 8 + o) * 8 + jj];
+                                const uint4 v = *reinterpret_cast<const uint4*>(
+                                    sm + OFF_SX + jj * 4096 + tc::sw128_chunk(16, c2, 8 * c2 + c, jc));
+                                w.x = tc::pack_bf16x2(L * bf16lo(v.x), L * bf16hi(v.x));
+                                w.y = tc::pack_bf16x2(L * bf16lo(v.y), L * bf16hi(v.y));
+                                w.z = tc::pack_bf16x2(L * bf16lo(v.z), L * bf16hi(v.z));
+                                w.w = tc::pack_bf16x2(L * bf16lo(v.w), L * bf16hi(v.w));
                             }
+                            *reinterpret_cast<uint4*>(sm + OFF_PA + tc::sw128_chunk(64, hv, drow, jc)) = w;
                         }
                         tc::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&ctl->pafull);
-                        // cos / sin of this token's angles (both chunks), shared by all compute threads
-                        const float* rawrot = reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024);
-                        float* coef = reinterpret_cast<float*>(sm + OFF_COEF + buf * 2048);
-                        if (P.rot == ROT_PAIRWISE || P.rot == ROT_HALF) {
-                            for (int i = ctid; i < 2 * P.na; i += NCW * 32) {
-                                const int c2 = i / P.na, a = i - c2 * P.na;
-                                float sv, cv;
-                                sincosf(rawrot[c2 * 128 + a], &sv, &cv);
-                                coef[c2 * 256 + a] = cv;
-                                coef[c2 * 256 + 128 + a] = sv;
-                            }
-                        }
-                        named_barrier_sync(1, NCW * 32);
-                        // ---- (3) h_t from the prefix states and the anchor; d_da_{t+1}; c_t
+                    };
+                    // ---- h_t from the prefix states and the anchor; d_da_{t+1}; c_t -> c tile
+                    auto step_h = [&](int t) {
+                        const int o = t - s0;
                         ok &= tc::mbar_wait(&ctl->pfull, ph_pfull.next(), abort);
                         tc::tc_fence_after();
-                        float h[4][16];
-                        {
-                            float an[4][16];
-                            tmem_ld_row(lane_addr + TM_P, G, h);
-                            tmem_ld_row(lane_addr + TM_AN, G, an);
-                            tc::tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) tc::mbar_arrive(&ctl->pfree);
-                            const float dsig = __expf(ac[t] - a_anchor);
-#pragma unroll
-                            for (int g = 0; g < 4; ++g)
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) h[g][e] = fmaf(dsig, an[g][e], h[g][e]);
-                        }
-                        {
-                            float dot = 0.f;
-#pragma unroll
-                            for (int g = 0; g < 4; ++g)
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) dot = fmaf(gr[g][e], h[g][e], dot);
-                            dot = warp_sum(dot);
-                            if (lane == 0) atomicAdd(&rda[buf * 2 + ch], dot);
-                        }
+                        const float dsig = __expf(ac[t] - a_anchor);
                         const bool live = t < Tch;
-                        float c[4][16];
-                        rotate_regs<false>(P, A.layoutB, G, h, coef + ch * 256, rawrot + ch * 128, c);
+                        const float* cf = coefs + (o * 2 + ch) * 128;
+                        const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + ch * 512);
                         if (nc_ >= 1) ok &= tc::mbar_wait(&ctl->cfree, ph_cfree.next(), abort);
                         ++nc_;
-                        write_tile_row(sm + OFF_C, m, G, c, !live);
+                        float dot = 0.f;
+#pragma unroll
+                        for (int pass = 0; pass < 2; ++pass) {
+                            const int sa = slot_a<LAYB>(pass), sb = slot_b<LAYB>(pass);
+                            float ha[16], hb[16], aa[16], ab[16];
+                            tc::tmem_ld16(lane_addr + TM_P + 16 * G[sa], ha);
+                            tc::tmem_ld16(lane_addr + TM_P + 16 * G[sb], hb);
+                            tc::tmem_ld16(lane_addr + TM_AN + 16 * G[sa], aa);
+                            tc::tmem_ld16(lane_addr + TM_AN + 16 * G[sb], ab);
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                ha[e] = fmaf(dsig, aa[e], ha[e]);
+                                hb[e] = fmaf(dsig, ab[e], hb[e]);
+                                dot = fmaf(gr[sa][e], ha[e], dot);
+                                dot = fmaf(gr[sb][e], hb[e], dot);
+                            }
+                            rot_pass<ROTK, LAYB, false>(P, pass, 16 * G[sa], 16 * G[sb], ha, hb, cf, qt);
+                            write_tile16(sm + OFF_C, m, G[sa], ha, !live);
+                            write_tile16(sm + OFF_C, m, G[sb], hb, !live);
+                        }
+                        tc::tc_fence_before();
                         tc::fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&ctl->cfull);
-                        // ---- (5) d_c, d_rot, G, cotangent recurrence
+                        if (lane == 0) {
+                            tc::mbar_arrive(&ctl->pfree);
+                            tc::mbar_arrive(&ctl->cfull);
+                        }
+                        // d_da_{t+1} = e_{t+1} <g_{t+1}, h_t>  (g holds g_{t+1} here)
+                        dot = warp_sum(dot);
+                        if (lane == 0 && t + 1 < I.T[0] && chunk_ok && n < I.proc)
+                            atomicAdd(B.dda + off_da(P, I.bb, n * FL + t + 1, I.hh), e_of(t + 1) * dot);
+                    };
+                    // ---- d_c -> d_rot, G, cotangent recurrence -> g tile
+                    auto step_g = [&](int t) {
+                        const int o = t - s0;
                         ok &= tc::mbar_wait(&ctl->dcfull, ph_dcfull.next(), abort);
                         tc::tc_fence_after();
-                        float dc[4][16];
-                        tmem_ld_row(lane_addr + TM_DC, G, dc);
-                        tc::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&ctl->dcfree);
+                        const bool live = t < Tch;
+                        const float* cf = coefs + (o * 2 + ch) * 128;
+                        const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + ch * 512);
+                        const int64_t orot = off_rot(P, I.bb, n * FL + t, I.hh);
+                        const bool rot_out = P.rw > 0 && chunk_ok && n < I.proc && live;
 #pragma unroll
-                        for (int g = 0; g < 4; ++g)
+                        for (int pass = 0; pass < 2; ++pass) {
+                            const int sa = slot_a<LAYB>(pass), sb = slot_b<LAYB>(pass);
+                            float da_[16], db_[16];
+                            tc::tmem_ld16(lane_addr + TM_DC + 16 * G[sa], da_);
+                            tc::tmem_ld16(lane_addr + TM_DC + 16 * G[sb], db_);
+                            tc::tmem_wait_ld();
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) dc[g][e] = live ? dc[g][e] + m1s[16 * G[g] + e] : 0.f;
-                        // rotation-parameter gradient, reduced over the 64 rows of the chunk
-                        if (P.rw) {
-                            float cb[4][16];
-                            read_tile_row(sm + OFF_C, m, G, cb);
-                            float* rd = red + (buf * 2 + ch) * 128;
-                            if (P.rot == ROT_QUAT) {
-                                // sum_p d_c (x) conj(c) per block; d_Q = that (x) Q / |Q|^2 below
-#pragma unroll
-                                for (int part = 0; part < 2; ++part) {
-                                    float v[32];
-#pragma unroll
-                                    for (int bq = 0; bq < 8; ++bq) {
-                                        const int g = 2 * part + (bq >> 2), e = 4 * (bq & 3);
-                                        float o0, o1, o2, o3;
-                                        hamilton(dc[g][e], dc[g][e + 1], dc[g][e + 2], dc[g][e + 3], cb[g][e],
-                                                 -cb[g][e + 1], -cb[g][e + 2], -cb[g][e + 3], o0, o1, o2, o3);
-                                        v[4 * bq] = o0; v[4 * bq + 1] = o1; v[4 * bq + 2] = o2; v[4 * bq + 3] = o3;
-                                    }
-                                    transpose_reduce32(v, lane);
-                                    const int bq = lane >> 2, g = 2 * part + (bq >> 2), e = 4 * (bq & 3);
-                                    const int blk = (16 * G[g] + e) >> 2;
-                                    if (blk < P.J) atomicAdd(&rd[4 * blk + (lane & 3)], v[0]);
-                                }
-                            } else if (P.rot == ROT_PAIRWISE) {
-                                float v[32];
-#pragma unroll
-                                for (int g = 0; g < 4; ++g)
-#pragma unroll
-                                    for (int e = 0; e < 16; e += 2)
-                                        v[8 * g + e / 2] = dc[g][e] * cb[g][e + 1] - dc[g][e + 1] * cb[g][e];
-                                transpose_reduce32(v, lane);
-                                const int g = lane >> 3, e = 2 * (lane & 7);
-                                const int ang = (16 * G[g] + e) >> 1;
-                                if (ang < P.na) atomicAdd(&rd[ang], v[0]);
-                            } else {  // half-split: x columns in slots 0,1 (layout A) / slot 0 (layout B)
-                                float v[32];
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) {
-                                    const int gb0 = A.layoutB ? 1 : 2;
-                                    v[e] = dc[0][e] * cb[gb0][e] - dc[gb0][e] * cb[0][e];
-                                    v[16 + e] = A.layoutB ? 0.f : (dc[1][e] * cb[3][e] - dc[3][e] * cb[1][e]);
-                                }
-                                transpose_reduce32(v, lane);
-                                const int g = lane >> 4, e = lane & 15;
-                                const int ang = 16 * G[g] + e;
-                                if (!(A.layoutB && g == 1) && ang < P.na) atomicAdd(&rd[ang], v[0]);
+                            for (int e = 0; e < 16; e += 4) {
+                                const float4 ma = *reinterpret_cast<const float4*>(m1s + 16 * G[sa] + e);
+                                const float4 mb = *reinterpret_cast<const float4*>(m1s + 16 * G[sb] + e);
+                                da_[e] = live ? da_[e] + ma.x : 0.f; da_[e + 1] = live ? da_[e + 1] + ma.y : 0.f;
+                                da_[e + 2] = live ? da_[e + 2] + ma.z : 0.f; da_[e + 3] = live ? da_[e + 3] + ma.w : 0.f;
+                                db_[e] = live ? db_[e] + mb.x : 0.f; db_[e + 1] = live ? db_[e + 1] + mb.y : 0.f;
+                                db_[e + 2] = live ? db_[e + 2] + mb.z : 0.f; db_[e + 3] = live ? db_[e + 3] + mb.w : 0.f;
                             }
-                        }
-                        {
-                            float Gt[4][16];
-                            rotate_regs<true>(P, A.layoutB, G, dc, coef + ch * 256, rawrot + ch * 128, Gt);
+                            // rotation-parameter gradient of the pass, summed over the warp's 32 rows;
+                            // after a 16-value transpose reduction lane L (< 16) holds value L
+                            if (ROTK == ROT_PAIRWISE) {
+                                float v[16];
+                                {
+                                    float cc[16];
+                                    read_tile16(sm + OFF_C, m, G[sa], cc);
 #pragma unroll
-                            for (int g = 0; g < 4; ++g)
+                                    for (int e = 0; e < 16; e += 2) v[e / 2] = da_[e] * cc[e + 1] - da_[e + 1] * cc[e];
+                                }
+                                {
+                                    float cc[16];
+                                    read_tile16(sm + OFF_C, m, G[sb], cc);
 #pragma unroll
-                                for (int e = 0; e < 16; ++e) gr[g][e] = fmaf(e_next, gr[g][e], Gt[g][e]);
-                        }
-                        const float e_t = e_of(t);
-                        if (ng >= 1) ok &= tc::mbar_wait(&ctl->gfree, ph_gfree.next(), abort);
-                        ++ng;
-                        write_tile_row(sm + OFF_G, m, G, gr, false);
-                        tc::fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&ctl->gfull);
-                        named_barrier_sync(1, NCW * 32);
-                        // ---- outputs of the reductions: d_rot_t and d_da_{t+1}
-                        {
-                            float* rd = red + buf * 256;
-                            const int tot = 2 * 128;
-                            for (int i = ctid; i < tot; i += NCW * 32) {
-                                const int c2 = i >> 7, a = i & 127;
-                                if (a < P.rw && I.exists[c2] && (2 * I.k + c2) < I.proc) {
-                                    const int64_t o_r = off_rot(P, I.bb, (2 * I.k + c2) * FL + t, I.hh);
-                                    float val = rd[i];
-                                    if (P.rot == ROT_QUAT) {
-                                        // (sum_p d_c (x) conj(c)) (x) Q / |Q|^2, component a & 3 of block a >> 2
-                                        const float* raw = reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024) + c2 * 128;
-                                        const float* Q = raw + 4 * (a >> 2);
-                                        const float s0q = rd[(i & ~3) + 0], s1q = rd[(i & ~3) + 1], s2q = rd[(i & ~3) + 2],
-                                                    s3q = rd[(i & ~3) + 3];
+                                    for (int e = 0; e < 16; e += 2) v[8 + e / 2] = db_[e] * cc[e + 1] - db_[e + 1] * cc[e];
+                                }
+                                transpose_reduce16(v, lane);
+                                const int ang = 8 * G[(lane & 8) ? sb : sa] + (lane & 7);
+                                if (lane < 16 && ang < P.na && rot_out) atomicAdd(B.drot + orot + ang, v[0]);
+                            } else if (ROTK == ROT_HALF) {
+                                if (!(LAYB && pass == 1)) {
+                                    float v[16];
+                                    {
+                                        float cc[16];
+                                        read_tile16(sm + OFF_C, m, G[sa], cc);
+#pragma unroll
+                                        for (int e = 0; e < 16; ++e) v[e] = -db_[e] * cc[e];
+                                    }
+                                    {
+                                        float cc[16];
+                                        read_tile16(sm + OFF_C, m, G[sb], cc);
+#pragma unroll
+                                        for (int e = 0; e < 16; ++e) v[e] = fmaf(da_[e], cc[e], v[e]);
+                                    }
+                                    transpose_reduce16(v, lane);
+                                    const int ang = 16 * G[sa] + (lane & 15);
+                                    if (lane < 16 && ang < P.na && rot_out) atomicAdd(B.drot + orot + ang, v[0]);
+                                }
+                            } else if (ROTK == ROT_QUAT) {
+                                // sum_p d_c (x) conj(c) per 4-block, then (.) (x) Q / |Q|^2
+#pragma unroll
+                                for (int sl = 0; sl < 2; ++sl) {
+                                    const int gsl = sl ? sb : sa;
+                                    float v[16];
+                                    {
+                                        float cc[16];
+                                        read_tile16(sm + OFF_C, m, G[gsl], cc);
+                                        const float(&d)[16] = sl ? db_ : da_;
+#pragma unroll
+                                        for (int bq = 0; bq < 4; ++bq)
+                                            hamilton(d[4 * bq], d[4 * bq + 1], d[4 * bq + 2], d[4 * bq + 3], cc[4 * bq],
+                                                     -cc[4 * bq + 1], -cc[4 * bq + 2], -cc[4 * bq + 3], v[4 * bq],
+                                                     v[4 * bq + 1], v[4 * bq + 2], v[4 * bq + 3]);
+                                    }
+                                    transpose_reduce16(v, lane);
+                                    // lanes 4i..4i+3 (i < 4) hold the 4 components of block i
+                                    const int l0 = lane & ~3, comp = lane & 3;
+                                    const float s0q = __shfl_sync(0xffffffffu, v[0], l0);
+                                    const float s1q = __shfl_sync(0xffffffffu, v[0], l0 + 1);
+                                    const float s2q = __shfl_sync(0xffffffffu, v[0], l0 + 2);
+                                    const float s3q = __shfl_sync(0xffffffffu, v[0], l0 + 3);
+                                    const int blk = 4 * G[gsl] + ((lane >> 2) & 3);
+                                    if (lane < 16 && blk < P.J && rot_out) {
+                                        const float* Q = qt + 4 * blk;
                                         float o0, o1, o2, o3;
                                         hamilton(s0q, s1q, s2q, s3q, Q[0], Q[1], Q[2], Q[3], o0, o1, o2, o3);
                                         const float inv = 1.f / (Q[0] * Q[0] + Q[1] * Q[1] + Q[2] * Q[2] + Q[3] * Q[3]);
-                                        const int comp = a & 3;
-                                        val = inv * (comp == 0 ? o0 : comp == 1 ? o1 : comp == 2 ? o2 : o3);
+                                        const float val = comp == 0 ? o0 : comp == 1 ? o1 : comp == 2 ? o2 : o3;
+                                        atomicAdd(B.drot + orot + 4 * blk + comp, inv * val);
                                     }
-                                    B.drot[o_r + a] = val;
                                 }
                             }
-                            named_barrier_sync(1, NCW * 32);
-                            for (int i = ctid; i < tot; i += NCW * 32) rd[i] = 0.f;
-                            if (ctid < 2) {
-                                const int c2 = ctid;
-                                if (t + 1 < I.T[0] && I.exists[c2]) {
-                                    const float e1 = __expf(ida[(c2 * 64 + t + 1) * 4 + (I.hh & 3)]);
-                                    B.dda[off_da(P, I.bb, (2 * I.k + c2) * FL + t + 1, I.hh)] = e1 * rda[buf * 2 + c2];
-                                }
-                                rda[buf * 2 + c2] = 0.f;
+                            // G = derot^T(d_c); g_t = G_t + e_{t+1} g_{t+1}
+                            rot_pass<ROTK, LAYB, true>(P, pass, 16 * G[sa], 16 * G[sb], da_, db_, cf, qt);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                gr[sa][e] = fmaf(e_next, gr[sa][e], da_[e]);
+                                gr[sb][e] = fmaf(e_next, gr[sb][e], db_[e]);
                             }
                         }
-                        e_next = e_t;
-                        // ---- (7) d_xhat (lanes = rows) and d_bhat (lanes = r) of token t
+                        tc::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&ctl->dcfree);
+                        e_next = e_of(t);
+                        if (ng >= 1) ok &= tc::mbar_wait(&ctl->gfree, ph_gfree.next(), abort);
+                        ++ng;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) write_tile16(sm + OFF_G, m, G[g], gr[g], false);
+                        tc::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&ctl->gfull);
+                    };
+                    // ---- d_xhat (lanes = rows) and d_bhat (lanes = r) of token t
+                    auto step_out = [&](int t) {
                         ok &= tc::mbar_wait(&ctl->dxfull, ph_dxfull.next(), abort);
                         tc::tc_fence_after();
-                        {
-                            float v[8];
-                            tc::tmem_ld8(lane_addr + TM_DX + 8 * ch, v);
-                            float u[8];
-                            tc::tmem_ld8(lane_addr + TM_DB + 8 * half, u);
-                            tc::tmem_wait_ld();
-                            tc::tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) tc::mbar_arrive(&ctl->dxfree);
-                            if (half == 0 && chunk_ok) {
-                                const int tok = n * FL + t;
+                        float v[8], u[8];
+                        tc::tmem_ld8(lane_addr + TM_DX + 8 * ch, v);
+                        tc::tmem_ld8(lane_addr + TM_DB + 8 * half, u);
+                        tc::tmem_wait_ld();
+                        tc::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&ctl->dxfree);
+                        if (half == 0 && chunk_ok) {
+                            const int tok = n * FL + t;
 #pragma unroll
-                                for (int c = 0; c < 4; ++c)
-                                    if (c < C) B.dx[off_x(P, I.bb, tok, c, I.hh) + pp] = __float2bfloat16_rn(v[c]);
-                            }
-                            if (m < R && I.exists[half]) {
-                                const int tok = (2 * I.k + half) * FL + t;
-#pragma unroll
-                                for (int c = 0; c < 4; ++c)
-                                    if (c < C) B.db[off_b(P, I.bb, tok, c, I.hh) + m] = __float2bfloat16_rn(u[c]);
-                            }
+                            for (int c = 0; c < 4; ++c)
+                                if (c < C) B.dx[off_x(P, I.bb, tok, c, I.hh) + pp] = __float2bfloat16_rn(v[c]);
                         }
+                        if (m < R && I.exists[half]) {
+                            const int tok = (2 * I.k + half) * FL + t;
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                if (c < C) B.db[off_b(P, I.bb, tok, c, I.hh) + m] = __float2bfloat16_rn(u[c]);
+                        }
+                    };
+
+                    const int thi = s0 + len - 1;
+                    build_pa(thi);
+                    step_h(thi);
+                    if (len >= 2) build_pa(thi - 1);
+                    for (int t = thi; t >= s0; --t) {
+                        step_g(t);
+                        if (t - 1 >= s0) step_h(t - 1);
+                        if (t - 2 >= s0) build_pa(t - 2);
+                        step_out(t);
                     }
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(&ctl->spanfree);
                 }
                 // ---- chunk start: d_da_0 = e_0 <g_0, h_->, e_n = e_0 g_0 (anchor 0 = the carry)
                 {
-                    float an[4][16];
-                    tmem_ld_row(lane_addr + TM_AN, G, an);
                     float dot = 0.f;
 #pragma unroll
-                    for (int g = 0; g < 4; ++g)
+                    for (int g = 0; g < 4; ++g) {
+                        float an[16];
+                        tc::tmem_ld16(lane_addr + TM_AN + 16 * G[g], an);
+                        tc::tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) dot = fmaf(gr[g][e], an[g][e], dot);
-                    dot = warp_sum(dot);
-                    if (lane == 0) atomicAdd(&rda[ch], dot);
-                    named_barrier_sync(1, NCW * 32);
-                    if (ctid < 2) {
-                        const int c2 = ctid;
-                        if (I.T[c2] > 0)
-                            B.dda[off_da(P, I.bb, (2 * I.k + c2) * FL, I.hh)] =
-                                __expf(ida[(c2 * 64) * 4 + (I.hh & 3)]) * rda[c2];
-                        rda[c2] = 0.f;
+                        for (int e = 0; e < 16; ++e) dot = fmaf(gr[g][e], an[e], dot);
                     }
+                    dot = warp_sum(dot);
+                    if (lane == 0 && Tch > 0) atomicAdd(B.dda + off_da(P, I.bb, n * FL, I.hh), e_of(0) * dot);
                     if (Tch > 0) {
-                        const float e0 = __expf(ida[(ch * 64) * 4 + (I.hh & 3)]);
+                        const float e0 = e_of(0);
                         float* dst = B.E + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
 #pragma unroll
                         for (int g = 0; g < 4; ++g)
@@ -802,11 +887,17 @@ __global__ void __launch_bounds__(NTHR, 1)
                             }
                     }
                 }
+                // the forward-sweep ring shares memory with the prefix tiles: restore the zero
+                // padding rows the next item's W products rely on
+                named_barrier_sync(1, NCW * 32);
+                for (uint32_t i = ctid; i < 32768 / 16; i += NCW * 32)
+                    reinterpret_cast<uint4*>(sm + OFF_RING)[i] = make_uint4(0, 0, 0, 0);
+                tc::fence_proxy_async_smem();
             } else {
                 // ================================ correction by the carry cotangent dH(n+1)
                 const bool corr = chunk_ok && n + 1 < I.proc;
-                float dh[4][16];
                 {
+                    float dh[4][16];
                     const float* src = B.E + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
                     const float* hin = A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
                     float dot = 0.f;
@@ -824,24 +915,38 @@ __global__ void __launch_bounds__(NTHR, 1)
                             dot += v.x * hv.x + v.y * hv.y + v.z * hv.z + v.w * hv.w;
                         }
                     dot = warp_sum(dot);
-                    if (lane == 0) atomicAdd(&rda[ch], dot);
+                    if (lane == 0) atomicAdd(&misc[ch], dot);
                     if (ng >= 1) ok &= tc::mbar_wait(&ctl->gfree, ph_gfree.next(), abort);
                     ++ng;
-                    write_tile_row(sm + OFF_G, m, G, dh, false);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) write_tile16(sm + OFF_G, m, G[g], dh[g], false);
                     tc::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(&ctl->gfull);
                 }
                 named_barrier_sync(1, NCW * 32);
                 if (ctid < 2) {
-                    base[ctid] = __expf(acum[ctid * 64 + 63]) * rda[ctid];
-                    rda[ctid] = 0.f;
+                    misc[2 + ctid] = __expf(acum[ctid * 64 + 63]) * misc[ctid];
+                    misc[ctid] = 0.f;
                 }
                 const float alast = ac[63];
                 const bool corr_b = I.exists[half] && (2 * I.k + half) + 1 < I.proc;
                 const float alast_b = acum[half * 64 + 63];
                 for (int t = 0; t < I.T[0]; ++t, ++q) {
                     const uint32_t s = q % NS;
+                    // issue this token's read-modify-write loads before waiting for the products
+                    const int tokx = n * FL + t, tokb = (2 * I.k + half) * FL + t;
+                    float ox[4] = {0.f, 0.f, 0.f, 0.f}, ob[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (half == 0 && corr) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if (c < C) ox[c] = __bfloat162float(B.dx[off_x(P, I.bb, tokx, c, I.hh) + pp]);
+                    }
+                    if (m < R && corr_b) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if (c < C) ob[c] = __bfloat162float(B.db[off_b(P, I.bb, tokb, c, I.hh) + m]);
+                    }
                     ok &= tc::mbar_wait(&ctl->full[s], ph_full[s].next(), abort);
                     ok &= tc::mbar_wait(&ctl->dxfull, ph_dxfull.next(), abort);
                     tc::tc_fence_after();
@@ -872,23 +977,15 @@ __global__ void __launch_bounds__(NTHR, 1)
                     }
                     if (half == 0 && corr) {
                         const float sc = __expf(alast - ac[t]);
-                        const int tok = n * FL + t;
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
-                            if (c < C) {
-                                __nv_bfloat16* d = B.dx + off_x(P, I.bb, tok, c, I.hh) + pp;
-                                *d = __float2bfloat16_rn(__bfloat162float(*d) + sc * v[c]);
-                            }
+                            if (c < C) B.dx[off_x(P, I.bb, tokx, c, I.hh) + pp] = __float2bfloat16_rn(ox[c] + sc * v[c]);
                     }
                     if (m < R && corr_b) {
                         const float sc = __expf(alast_b - acum[half * 64 + t]);
-                        const int tok = (2 * I.k + half) * FL + t;
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
-                            if (c < C) {
-                                __nv_bfloat16* d = B.db + off_b(P, I.bb, tok, c, I.hh) + m;
-                                *d = __float2bfloat16_rn(__bfloat162float(*d) + sc * u[c]);
-                            }
+                            if (c < C) B.db[off_b(P, I.bb, tokb, c, I.hh) + m] = __float2bfloat16_rn(ob[c] + sc * u[c]);
                     }
                 }
                 named_barrier_sync(1, NCW * 32);
@@ -900,18 +997,11 @@ __global__ void __launch_bounds__(NTHR, 1)
                         const float* ac2 = acum + c2 * 64;
                         float pre = 0.f;
                         for (int j = 0; j < s; ++j) pre += __expf(ac2[63] - ac2[j]) * om[c2 * 64 + j];
-                        B.dda[off_da(P, I.bb, n2 * FL + s, I.hh)] += base[c2] + pre;
+                        B.dda[off_da(P, I.bb, n2 * FL + s, I.hh)] += misc[2 + c2] + pre;
                     }
                 }
                 named_barrier_sync(1, NCW * 32);
                 if (ctid < 128) om[ctid] = 0.f;
-            }
-            if (MODE == LOCAL) {
-                // the forward-sweep ring shares memory with the prefix tiles: restore the zero
-                // padding rows the next item's W products rely on
-                for (uint32_t i = ctid; i < 32768 / 16; i += NCW * 32)
-                    reinterpret_cast<uint4*>(sm + OFF_RING)[i] = make_uint4(0, 0, 0, 0);
-                tc::fence_proxy_async_smem();
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ctl->itemdone);
@@ -948,7 +1038,17 @@ cudaError_t launch_tc_bwd(int mode, const FastArgs& fa, float* E, float* anchors
     a.db = static_cast<__nv_bfloat16*>(db);
     a.dda = dda;
     a.drot = drot;
-    auto kern = mode == LOCAL ? tc_bwd_kernel<LOCAL> : tc_bwd_kernel<CORR>;
+    decltype(&tc_bwd_kernel<LOCAL, ROT_NONE, 0>) kern;
+    if (mode == CORR) {
+        kern = tc_bwd_kernel<CORR, ROT_NONE, 0>;
+    } else {
+        switch (fa.P.rot) {
+            case ROT_PAIRWISE: kern = tc_bwd_kernel<LOCAL, ROT_PAIRWISE, 0>; break;
+            case ROT_HALF: kern = fa.layoutB ? tc_bwd_kernel<LOCAL, ROT_HALF, 1> : tc_bwd_kernel<LOCAL, ROT_HALF, 0>; break;
+            case ROT_QUAT: kern = tc_bwd_kernel<LOCAL, ROT_QUAT, 0>; break;
+            default: kern = tc_bwd_kernel<LOCAL, ROT_NONE, 0>; break;
+        }
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int kid = mode == LOCAL ? KID_FAST_BWD : KID_FAST_CORRECT;
