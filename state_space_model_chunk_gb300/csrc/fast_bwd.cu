@@ -209,19 +209,35 @@ __device__ __forceinline__ void rot_pass(const MMParams& P, int pass, int ka, in
     }
 }
 
-// Parity helper: a barrier that completes once per use.
-struct Phase {
-    uint32_t n = 0;
-    __device__ uint32_t next() { return (n++) & 1; }
+// Parities of the barriers a thread waits on, one bit each, and one-bit "used before" flags,
+// all in one register.
+struct Par {
+    uint32_t b = 0;
+    __device__ __forceinline__ uint32_t next(uint32_t i) {
+        const uint32_t p = (b >> i) & 1u;
+        b ^= 1u << i;
+        return p;
+    }
+    __device__ __forceinline__ bool once(uint32_t i) {  // false the first time, true afterwards
+        const bool was = (b >> i) & 1u;
+        b |= 1u << i;
+        return was;
+    }
 };
-
+// bit positions
+enum : uint32_t {
+    B_FULL = 0,                       // NS ring stages
+    B_W = 4,                          // 2 W buffers
+    B_ITEM = 6, B_SPAN, B_PB, B_PA, B_P, B_C, B_DC, B_G, B_DX, B_ITEMDONE, B_SPANFREE,
+    U_PRE = 24, U_DC, U_DX, U_PA, U_C, U_G, U_SPAN
+};
 template <int MODE, int ROTK, int LAYB>
 __global__ void __launch_bounds__(NTHR, 1)
     tc_bwd_kernel(const __grid_constant__ BwdArgs B, const __grid_constant__ CUtensorMap tmx,
                   const __grid_constant__ CUtensorMap tmb, const __grid_constant__ CUtensorMap tmr,
                   const __grid_constant__ CUtensorMap tmd) {
     extern __shared__ unsigned char smraw[];
-    unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    unsigned char* sm = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
     Ctl* ctl = reinterpret_cast<Ctl*>(sm + OFF_CTL);
     const FastArgs& A = B.F;
     const MMParams& P = A.P;
@@ -281,12 +297,11 @@ __global__ void __launch_bounds__(NTHR, 1)
         // ====================================================================== TMA producer
         if (lane == 0) {
             uint32_t q = 0;  // ring uses
-            Phase ph_itemdone, ph_spanfree;
-            uint32_t spans_done = 0;
+            Par pr;
             bool ok = true;
             for (int it = it0; it < it1 && ok; ++it) {
                 const Item I = decode_item(A, it);
-                if (it > it0) ok &= tc::mbar_wait(&ctl->itemdone, ph_itemdone.next(), abort);
+                if (it > it0) ok &= tc::mbar_wait(&ctl->itemdone, pr.next(B_ITEMDONE), abort);
                 if (!ok) break;
                 // the item's da: 64 tokens x 4 heads per existing chunk
                 uint32_t bytes = 0;
@@ -316,7 +331,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 if (MODE == LOCAL && ok) {
                     const int nsp = (I.T[0] + SPAN - 1) / SPAN;
                     for (int sg = nsp - 1; sg >= 0 && ok; --sg) {
-                        if (spans_done >= 1) ok &= tc::mbar_wait(&ctl->spanfree, ph_spanfree.next(), abort);
+                        if (pr.once(U_SPAN)) ok &= tc::mbar_wait(&ctl->spanfree, pr.next(B_SPANFREE), abort);
                         if (!ok) break;
                         const int s0 = sg * SPAN, len = min(SPAN, I.T[0] - s0);
                         uint32_t by = 0;
@@ -336,7 +351,6 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     tc::tma_load_3d(sm + OFF_ROT + jj * 1024 + ch * 512, &tmr, 0, I.hh, row,
                                                     &ctl->spanfull);
                             }
-                        ++spans_done;
                     }
                 }
             }
@@ -354,14 +368,14 @@ __global__ void __launch_bounds__(NTHR, 1)
             const uint32_t s_g = tc::smem_u32(sm + OFF_G), s_ds = tc::smem_u32(sm + OFF_DS);
             const uint32_t s_sx = tc::smem_u32(sm + OFF_SX), s_sb = tc::smem_u32(sm + OFF_SB);
             const uint32_t s_pa = tc::smem_u32(sm + OFF_PA), s_pb = tc::smem_u32(sm + OFF_PB);
-            Phase ph_full[NS], ph_wfree[2], ph_pbready, ph_pafull, ph_pfree, ph_cfull, ph_dcfree, ph_gfull, ph_dxfree;
-            uint32_t q = 0, nw = 0, npre = 0, ndc = 0, ndx = 0;
+            Par pr;
+            uint32_t q = 0, nw = 0;
             bool ok = true;
             // d_xhat / d_bhat MMAs: A = g tile (K-major rows (ch,p) / MN-major columns r), B = one
             // token's bhat / xhat tile [16 rows (8 ch + c)][128] K-major.
             auto issue_dx = [&](uint32_t sxb, uint32_t sbb, bool wait_g, bool free_g) -> bool {
-                if (wait_g && !tc::mbar_wait(&ctl->gfull, ph_gfull.next(), abort)) return false;
-                if (ndx >= 1 && !tc::mbar_wait(&ctl->dxfree, ph_dxfree.next(), abort)) return false;
+                if (wait_g && !tc::mbar_wait(&ctl->gfull, pr.next(B_G), abort)) return false;
+                if (pr.once(U_DX) && !tc::mbar_wait(&ctl->dxfree, pr.next(B_DX), abort)) return false;
                 tc::tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -372,27 +386,25 @@ __global__ void __launch_bounds__(NTHR, 1)
                     tc::mma_bf16(tbase + TM_DB, tc::sdesc_sw128(s_g + ks * 2048u, 16384, 1024),
                                  tc::sdesc_sw128(sxb + boff, 16, 1024), idDB, ks > 0);
                 }
-                ++ndx;
                 tc::mma_commit(&ctl->dxfull);
                 if (free_g) tc::mma_commit(&ctl->gfree);
                 return true;
             };
             auto issue_prefix = [&](int o) -> bool {
-                if (!tc::mbar_wait(&ctl->pafull, ph_pafull.next(), abort)) return false;
-                if (npre >= 1 && !tc::mbar_wait(&ctl->pfree, ph_pfree.next(), abort)) return false;
+                if (!tc::mbar_wait(&ctl->pafull, pr.next(B_PA), abort)) return false;
+                if (pr.once(U_PRE) && !tc::mbar_wait(&ctl->pfree, pr.next(B_P), abort)) return false;
                 tc::tc_fence_after();
                 const int nk = o / 2 + 1;
                 for (int kq = 0; kq < nk; ++kq)
                     tc::mma_bf16(tbase + TM_P, tc::sdesc_sw128(s_pa + kq * 2048u, 8192, 1024),
                                  tc::sdesc_sw128(s_pb + kq * 2048u, 8192, 1024), idPre, kq > 0);
-                ++npre;
                 tc::mma_commit(&ctl->pfull);
                 tc::mma_commit(&ctl->pafree);
                 return true;
             };
             auto issue_dc = [&]() -> bool {
-                if (!tc::mbar_wait(&ctl->cfull, ph_cfull.next(), abort)) return false;
-                if (ndc >= 1 && !tc::mbar_wait(&ctl->dcfree, ph_dcfree.next(), abort)) return false;
+                if (!tc::mbar_wait(&ctl->cfull, pr.next(B_C), abort)) return false;
+                if (pr.once(U_DC) && !tc::mbar_wait(&ctl->dcfree, pr.next(B_DC), abort)) return false;
                 tc::tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -400,7 +412,6 @@ __global__ void __launch_bounds__(NTHR, 1)
                     tc::mma_bf16(tbase + TM_DC, tc::sdesc_sw128(s_c + koff, 16, 1024),
                                  tc::sdesc_sw128(s_ds + koff, 16, 1024), idDC, ks > 0);
                 }
-                ++ndc;
                 tc::mma_commit(&ctl->dcfull);
                 tc::mma_commit(&ctl->cfree);
                 return true;
@@ -410,10 +421,10 @@ __global__ void __launch_bounds__(NTHR, 1)
                 for (int t = 0; t < I.T[0] && ok; ++t, ++q) {
                     const uint32_t s = q % NS;
                     const uint32_t xb = s_ring + s * 8192, bb_ = xb + 4096;
-                    if (!(ok = tc::mbar_wait(&ctl->full[s], ph_full[s].next(), abort))) break;
+                    if (!(ok = tc::mbar_wait(&ctl->full[s], pr.next(B_FULL + s), abort))) break;
                     if (MODE == LOCAL) {
                         const uint32_t wb = nw & 1;
-                        if (nw >= 2 && !(ok = tc::mbar_wait(&ctl->wfree[wb], ph_wfree[wb].next(), abort))) break;
+                        if (nw >= 2 && !(ok = tc::mbar_wait(&ctl->wfree[wb], pr.next(B_W + wb), abort))) break;
                         tc::tc_fence_after();
                         tc::mma_bf16(tbase + (wb ? TM_DC : TM_P), tc::sdesc_sw128(xb, 2048, 1024),
                                      tc::sdesc_sw128(bb_, 2048, 1024), idW, 0);
@@ -429,14 +440,12 @@ __global__ void __launch_bounds__(NTHR, 1)
                     const int nsp = (I.T[0] + SPAN - 1) / SPAN;
                     for (int sg = nsp - 1; sg >= 0 && ok; --sg) {
                         const int len = min(SPAN, I.T[0] - sg * SPAN);
-                        if (!(ok = tc::mbar_wait(&ctl->pbready, ph_pbready.next(), abort))) break;
+                        if (!(ok = tc::mbar_wait(&ctl->pbready, pr.next(B_PB), abort))) break;
                         // pipelined order, matching the compute warps' signals
-                        ok = issue_prefix(len - 1) && issue_dc();
-                        if (ok && len >= 2) ok = issue_prefix(len - 2);
-                        for (int o = len - 1; o >= 0 && ok; --o) {
-                            ok = issue_dx(s_sx + o * 4096u, s_sb + o * 4096u, true, true);
-                            if (ok && o >= 1) ok = issue_dc();
-                            if (ok && o >= 2) ok = issue_prefix(o - 2);
+                        for (int u = len + 1; u >= 0 && ok; --u) {
+                            if (u <= len - 1) ok = issue_dx(s_sx + u * 4096u, s_sb + u * 4096u, true, true);
+                            if (ok && u - 1 >= 0 && u - 1 <= len - 1) ok = issue_dc();
+                            if (ok && u - 2 >= 0) ok = issue_prefix(u - 2);
                         }
                         if (ok) tc::mma_commit(&ctl->spanfree);
                     }
@@ -464,16 +473,16 @@ __global__ void __launch_bounds__(NTHR, 1)
         float* om = reinterpret_cast<float*>(sm + OFF_OM);                // [2][64]
         float* misc = reinterpret_cast<float*>(sm + OFF_MISC);            // [2] dots, [2] bases
         float* myanchors = B.anchors + (int64_t)blockIdx.x * NANCHOR * 128 * 128;
-        Phase ph_itemfull, ph_full[NS], ph_wfull[2], ph_spanfull, ph_pfull, ph_pafree, ph_cfree, ph_dcfull, ph_gfree,
-            ph_dxfull;
-        uint32_t q = 0, nw = 0, npa = 0, nc_ = 0, ng = 0;
+        Par pr;
+        uint32_t q = 0, nw = 0;
         bool ok = true;
         for (int it = it0; it < it1; ++it) {
             const Item I = decode_item(A, it);
-            const int Tch = I.T[ch];
+            const int Tch = ch ? I.T[1] : I.T[0];
             const int n = 2 * I.k + ch;
-            const bool chunk_ok = I.exists[ch];
-            ok &= tc::mbar_wait(&ctl->itemfull, ph_itemfull.next(), abort);
+            const bool chunk_ok = ch ? I.exists[1] : I.exists[0];
+            const bool half_ok = half ? I.exists[1] : I.exists[0];
+            ok &= tc::mbar_wait(&ctl->itemfull, pr.next(B_ITEM), abort);
             // ---- item set-up: cumulative da of both chunks; D + D^T and d_m1 when (b,h) changes
             if (warp < 2) {
                 const int c2 = warp;
@@ -536,8 +545,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                     }
                     for (int t = 0; t < I.T[0]; ++t, ++q) {
                         const uint32_t s = q % NS, wb = nw & 1;
-                        ok &= tc::mbar_wait(&ctl->full[s], ph_full[s].next(), abort);
-                        ok &= tc::mbar_wait(&ctl->wfull[wb], ph_wfull[wb].next(), abort);
+                        ok &= tc::mbar_wait(&ctl->full[s], pr.next(B_FULL + s), abort);
+                        ok &= tc::mbar_wait(&ctl->wfull[wb], pr.next(B_W + wb), abort);
                         tc::tc_fence_after();
                         const float et = t < Tch ? e_of(t) : 1.f;
                         const float wt = t < Tch ? 1.f : 0.f;
@@ -581,7 +590,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const int nsp = (I.T[0] + SPAN - 1) / SPAN;
                 for (int sg = nsp - 1; sg >= 0; --sg) {
                     const int s0 = sg * SPAN, len = min(SPAN, I.T[0] - s0);
-                    ok &= tc::mbar_wait(&ctl->spanfull, ph_spanfull.next(), abort);
+                    ok &= tc::mbar_wait(&ctl->spanfull, pr.next(B_SPAN), abort);
                     // anchor of the span -> TMEM (this thread's row and columns)
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
@@ -637,8 +646,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     // ---- prefix A rows for token t: L[t, s0+jj] xhat (two tokens per K step)
                     auto build_pa = [&](int t) {
                         const int o = t - s0;
-                        if (npa >= 1) ok &= tc::mbar_wait(&ctl->pafree, ph_pafree.next(), abort);
-                        ++npa;
+                        if (pr.once(U_PA)) ok &= tc::mbar_wait(&ctl->pafree, pr.next(B_PA), abort);
                         const int nrow_tok = (o % 2 == 0) ? o + 2 : o + 1;
                         for (int i = ctid; i < nrow_tok * 8 * 16; i += NCW * 32) {
                             const int j16 = i & 15, drow = i >> 4;
@@ -663,14 +671,13 @@ __global__ void __launch_bounds__(NTHR, 1)
                     // ---- h_t from the prefix states and the anchor; d_da_{t+1}; c_t -> c tile
                     auto step_h = [&](int t) {
                         const int o = t - s0;
-                        ok &= tc::mbar_wait(&ctl->pfull, ph_pfull.next(), abort);
+                        ok &= tc::mbar_wait(&ctl->pfull, pr.next(B_P), abort);
                         tc::tc_fence_after();
                         const float dsig = __expf(ac[t] - a_anchor);
                         const bool live = t < Tch;
                         const float* cf = coefs + (o * 2 + ch) * 128;
                         const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + ch * 512);
-                        if (nc_ >= 1) ok &= tc::mbar_wait(&ctl->cfree, ph_cfree.next(), abort);
-                        ++nc_;
+                        if (pr.once(U_C)) ok &= tc::mbar_wait(&ctl->cfree, pr.next(B_C), abort);
                         float dot = 0.f;
 #pragma unroll
                         for (int pass = 0; pass < 2; ++pass) {
@@ -707,7 +714,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     // ---- d_c -> d_rot, G, cotangent recurrence -> g tile
                     auto step_g = [&](int t) {
                         const int o = t - s0;
-                        ok &= tc::mbar_wait(&ctl->dcfull, ph_dcfull.next(), abort);
+                        ok &= tc::mbar_wait(&ctl->dcfull, pr.next(B_DC), abort);
                         tc::tc_fence_after();
                         const bool live = t < Tch;
                         const float* cf = coefs + (o * 2 + ch) * 128;
@@ -747,7 +754,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     for (int e = 0; e < 16; e += 2) v[8 + e / 2] = db_[e] * cc[e + 1] - db_[e + 1] * cc[e];
                                 }
                                 transpose_reduce16(v, lane);
-                                const int ang = 8 * G[(lane & 8) ? sb : sa] + (lane & 7);
+                                const int ang = 8 * ((lane & 8) ? G[sb] : G[sa]) + (lane & 7);
                                 if (lane < 16 && ang < P.na && rot_out) atomicAdd(B.drot + orot + ang, v[0]);
                             } else if (ROTK == ROT_HALF) {
                                 if (!(LAYB && pass == 1)) {
@@ -814,8 +821,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&ctl->dcfree);
                         e_next = e_of(t);
-                        if (ng >= 1) ok &= tc::mbar_wait(&ctl->gfree, ph_gfree.next(), abort);
-                        ++ng;
+                        if (pr.once(U_G)) ok &= tc::mbar_wait(&ctl->gfree, pr.next(B_G), abort);
 #pragma unroll
                         for (int g = 0; g < 4; ++g) write_tile16(sm + OFF_G, m, G[g], gr[g], false);
                         tc::fence_proxy_async_smem();
@@ -824,7 +830,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     };
                     // ---- d_xhat (lanes = rows) and d_bhat (lanes = r) of token t
                     auto step_out = [&](int t) {
-                        ok &= tc::mbar_wait(&ctl->dxfull, ph_dxfull.next(), abort);
+                        ok &= tc::mbar_wait(&ctl->dxfull, pr.next(B_DX), abort);
                         tc::tc_fence_after();
                         float v[8], u[8];
                         tc::tmem_ld8(lane_addr + TM_DX + 8 * ch, v);
@@ -839,7 +845,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                             for (int c = 0; c < 4; ++c)
                                 if (c < C) B.dx[off_x(P, I.bb, tok, c, I.hh) + pp] = __float2bfloat16_rn(v[c]);
                         }
-                        if (m < R && I.exists[half]) {
+                        if (m < R && half_ok) {
                             const int tok = (2 * I.k + half) * FL + t;
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
@@ -847,15 +853,13 @@ __global__ void __launch_bounds__(NTHR, 1)
                         }
                     };
 
+                    // u runs two tokens ahead so that every step has one call site
                     const int thi = s0 + len - 1;
-                    build_pa(thi);
-                    step_h(thi);
-                    if (len >= 2) build_pa(thi - 1);
-                    for (int t = thi; t >= s0; --t) {
-                        step_g(t);
-                        if (t - 1 >= s0) step_h(t - 1);
-                        if (t - 2 >= s0) build_pa(t - 2);
-                        step_out(t);
+                    for (int u = thi + 2; u >= s0; --u) {
+                        if (u <= thi) step_g(u);
+                        if (u - 1 >= s0 && u - 1 <= thi) step_h(u - 1);
+                        if (u - 2 >= s0) build_pa(u - 2);
+                        if (u <= thi) step_out(u);
                     }
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(&ctl->spanfree);
@@ -916,8 +920,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         }
                     dot = warp_sum(dot);
                     if (lane == 0) atomicAdd(&misc[ch], dot);
-                    if (ng >= 1) ok &= tc::mbar_wait(&ctl->gfree, ph_gfree.next(), abort);
-                    ++ng;
+                    if (pr.once(U_G)) ok &= tc::mbar_wait(&ctl->gfree, pr.next(B_G), abort);
 #pragma unroll
                     for (int g = 0; g < 4; ++g) write_tile16(sm + OFF_G, m, G[g], dh[g], false);
                     tc::fence_proxy_async_smem();
@@ -930,7 +933,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     misc[ctid] = 0.f;
                 }
                 const float alast = ac[63];
-                const bool corr_b = I.exists[half] && (2 * I.k + half) + 1 < I.proc;
+                const bool corr_b = half_ok && (2 * I.k + half) + 1 < I.proc;
                 const float alast_b = acum[half * 64 + 63];
                 for (int t = 0; t < I.T[0]; ++t, ++q) {
                     const uint32_t s = q % NS;
@@ -947,8 +950,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                         for (int c = 0; c < 4; ++c)
                             if (c < C) ob[c] = __bfloat162float(B.db[off_b(P, I.bb, tokb, c, I.hh) + m]);
                     }
-                    ok &= tc::mbar_wait(&ctl->full[s], ph_full[s].next(), abort);
-                    ok &= tc::mbar_wait(&ctl->dxfull, ph_dxfull.next(), abort);
+                    ok &= tc::mbar_wait(&ctl->full[s], pr.next(B_FULL + s), abort);
+                    ok &= tc::mbar_wait(&ctl->dxfull, pr.next(B_DX), abort);
                     tc::tc_fence_after();
                     float v[8], u[8];
                     tc::tmem_ld8(lane_addr + TM_DX + 8 * ch, v);
@@ -993,7 +996,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 if (ctid < 128) {
                     const int c2 = ctid >> 6, s = ctid & 63;
                     const int n2 = 2 * I.k + c2;
-                    if (I.exists[c2] && n2 + 1 < I.proc) {
+                    if ((c2 ? I.exists[1] : I.exists[0]) && n2 + 1 < I.proc) {
                         const float* ac2 = acum + c2 * 64;
                         float pre = 0.f;
                         for (int j = 0; j < s; ++j) pre += __expf(ac2[63] - ac2[j]) * om[c2 * 64 + j];

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                   const __grid_constant__ CUtensorMap tmb, const __grid_constant__ CUtensorMap tmr,
                   const __grid_constant__ CUtensorMap tmd) {
     extern __shared__ unsigned char smraw[];
-    unsigned char* sm = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    unsigned char* sm = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
     Ctl* ctl = reinterpret_cast<Ctl*>(sm + OFF_CTL);
     const MMParams& P = A.P;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
