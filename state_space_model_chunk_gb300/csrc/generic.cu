@@ -153,20 +153,54 @@ __global__ void __launch_bounds__(NT) k_chunk_end(MMParams P, const T* __restric
 // -------------------------------------------------------------- carry scan (K2)
 // In place: slot n holds Delta_n on entry and the carry h_-(n) on exit.
 // h_-(0) = initial, h_-(n+1) = D_n h_-(n) + Delta_n ("boundary_carries", serial part).
-__global__ void k_carry_scan(MMParams P, const float* __restrict__ initial, float* __restrict__ Hc,
-                             const float* __restrict__ Dn) {
+// Each thread owns V consecutive elements of the p x r state (V = 4: float4 when p r % 4 == 0)
+// and reads the slots of SCAN_B chunks ahead before the dependent updates, so that a thread keeps
+// SCAN_B independent loads in flight.
+constexpr int SCAN_T = 256, SCAN_B = 8;
+
+template <int V>
+struct Vec;
+template <>
+struct Vec<1> {
+    using T = float;
+    __device__ static T zero() { return 0.f; }
+    __device__ static T fma(float a, T x, T y) { return fmaf(a, x, y); }
+    __device__ static T add(T x, T y) { return x + y; }
+};
+template <>
+struct Vec<4> {
+    using T = float4;
+    __device__ static T zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+    __device__ static T fma(float a, T x, T y) {
+        return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+    }
+    __device__ static T add(T x, T y) { return make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w); }
+};
+
+template <int V>
+__global__ void __launch_bounds__(SCAN_T) k_carry_scan(MMParams P, const float* __restrict__ initial,
+                                                       float* __restrict__ Hc, const float* __restrict__ Dn) {
+    using VT = typename Vec<V>::T;
     const int hh = blockIdx.y, bb = blockIdx.z;
-    const int pr = P.p * P.r;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= pr) return;
+    const int64_t nv = (int64_t)P.p * P.r / V;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= nv) return;
     const int proc = mm_processed(P, bb);
-    float H = initial[((int64_t)bb * P.h + hh) * pr + e];
+    VT H = reinterpret_cast<const VT*>(initial + ((int64_t)bb * P.h + hh) * nv * V)[e];
     const float* D = Dn + ((int64_t)bb * P.h + hh) * P.nc;
-    for (int n = 0; n < proc; ++n) {
-        float* slot = Hc + off_carry(P, bb, hh, n) + e;
-        float delta = (n + 1 < proc) ? *slot : 0.f;
-        *slot = H;
-        H = D[n] * H + delta;
+    VT* slot0 = reinterpret_cast<VT*>(Hc + off_carry(P, bb, hh, 0)) + e;
+    for (int n0 = 0; n0 < proc; n0 += SCAN_B) {
+        VT d[SCAN_B];
+#pragma unroll
+        for (int j = 0; j < SCAN_B; ++j)
+            d[j] = (n0 + j + 1 < proc) ? slot0[(int64_t)(n0 + j) * nv] : Vec<V>::zero();
+#pragma unroll
+        for (int j = 0; j < SCAN_B; ++j) {
+            if (n0 + j < proc) {
+                slot0[(int64_t)(n0 + j) * nv] = H;
+                H = Vec<V>::fma(D[n0 + j], H, d[j]);
+            }
+        }
     }
 }
 
@@ -395,22 +429,31 @@ __global__ void __launch_bounds__(NT) k_bwd_chunk(MMParams P, const T* __restric
 // ------------------------------------------------ carry-cotangent scan (K6)
 // In place: slot n holds e_n on entry and dH(n+1), the cotangent of chunk n's end state, on
 // exit.  dH(P) = 0, dH(n) = e_n + D_n dH(n+1), d_initial = dH(0).
-__global__ void k_cot_scan(MMParams P, float* __restrict__ E, const float* __restrict__ Dn,
-                           float* __restrict__ dinit) {
+template <int V>
+__global__ void __launch_bounds__(SCAN_T) k_cot_scan(MMParams P, float* __restrict__ E, const float* __restrict__ Dn,
+                                                     float* __restrict__ dinit) {
+    using VT = typename Vec<V>::T;
     const int hh = blockIdx.y, bb = blockIdx.z;
-    const int pr = P.p * P.r;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= pr) return;
+    const int64_t nv = (int64_t)P.p * P.r / V;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= nv) return;
     const int proc = mm_processed(P, bb);
     const float* D = Dn + ((int64_t)bb * P.h + hh) * P.nc;
-    float dH = 0.f;
-    for (int n = proc - 1; n >= 0; --n) {
-        float* slot = E + off_carry(P, bb, hh, n) + e;
-        float en = *slot;
-        *slot = dH;
-        dH = en + D[n] * dH;
+    VT* slot0 = reinterpret_cast<VT*>(E + off_carry(P, bb, hh, 0)) + e;
+    VT dH = Vec<V>::zero();
+    for (int n0 = proc - 1; n0 >= 0; n0 -= SCAN_B) {
+        VT en[SCAN_B];
+#pragma unroll
+        for (int j = 0; j < SCAN_B; ++j) en[j] = (n0 - j >= 0) ? slot0[(int64_t)(n0 - j) * nv] : Vec<V>::zero();
+#pragma unroll
+        for (int j = 0; j < SCAN_B; ++j) {
+            if (n0 - j >= 0) {
+                slot0[(int64_t)(n0 - j) * nv] = dH;
+                dH = Vec<V>::fma(D[n0 - j], dH, en[j]);
+            }
+        }
     }
-    dinit[((int64_t)bb * P.h + hh) * pr + e] = dH;
+    reinterpret_cast<VT*>(dinit + ((int64_t)bb * P.h + hh) * nv * V)[e] = dH;
 }
 
 // ---------------------------------------------- boundary-cotangent correction (K7)
@@ -533,11 +576,7 @@ static cudaError_t carries(const MMParams& P, const T* x, const T* bh, const flo
     mm_prof_mark(KID_CHUNK_END, 1, st);
     k_chunk_end<T><<<gch, NT, generic_end_smem(P), st>>>(P, x, bh, da, Hc, Dn);
     mm_prof_mark(KID_CHUNK_END, 0, st);
-    dim3 gsc((P.p * P.r + 127) / 128, P.h, P.b);
-    mm_prof_mark(KID_CARRY_SCAN, 1, st);
-    k_carry_scan<<<gsc, 128, 0, st>>>(P, init, Hc, Dn);
-    mm_prof_mark(KID_CARRY_SCAN, 0, st);
-    return cudaGetLastError();
+    return generic_carry_scan(P, init, Hc, Dn, st);
 }
 
 template <typename T>
@@ -571,10 +610,7 @@ static cudaError_t bwd_impl(const MMParams& P, const GenericPtrs& A, int grid, c
                                                            (T*)A.dxhat, (T*)A.dbhat, A.dda, A.drot,
                                                            A.E, A.traj);
     mm_prof_mark(KID_BWD_CHUNK, 0, st);
-    dim3 gsc((P.p * P.r + 127) / 128, P.h, P.b);
-    mm_prof_mark(KID_COT_SCAN, 1, st);
-    k_cot_scan<<<gsc, 128, 0, st>>>(P, A.E, A.Dn, A.dinit);
-    mm_prof_mark(KID_COT_SCAN, 0, st);
+    if ((e = generic_cot_scan(P, A.E, A.Dn, A.dinit, st)) != cudaSuccess) return e;
     dim3 gch(P.nc, P.h, P.b);
     mm_prof_mark(KID_CORRECT, 1, st);
     k_correct<T><<<gch, NT, generic_correct_smem(P), st>>>(P, x, bh, A.da, A.Hc, A.E, (T*)A.dxhat,
@@ -583,19 +619,32 @@ static cudaError_t bwd_impl(const MMParams& P, const GenericPtrs& A, int grid, c
     return cudaGetLastError();
 }
 
+namespace {
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+template <int V>
+dim3 scan_grid(const MMParams& P) {
+    const int64_t nv = (int64_t)P.p * P.r / V;
+    return dim3((unsigned)((nv + SCAN_T - 1) / SCAN_T), P.h, P.b);
+}
+}  // namespace
+
 cudaError_t generic_carry_scan(const MMParams& P, const float* initial, float* Hc, const float* Dn,
                                cudaStream_t st) {
-    dim3 gsc((P.p * P.r + 127) / 128, P.h, P.b);
     mm_prof_mark(KID_CARRY_SCAN, 1, st);
-    k_carry_scan<<<gsc, 128, 0, st>>>(P, initial, Hc, Dn);
+    if ((P.p * P.r) % 4 == 0 && aligned16(initial) && aligned16(Hc))
+        k_carry_scan<4><<<scan_grid<4>(P), SCAN_T, 0, st>>>(P, initial, Hc, Dn);
+    else
+        k_carry_scan<1><<<scan_grid<1>(P), SCAN_T, 0, st>>>(P, initial, Hc, Dn);
     mm_prof_mark(KID_CARRY_SCAN, 0, st);
     return cudaGetLastError();
 }
 
 cudaError_t generic_cot_scan(const MMParams& P, float* E, const float* Dn, float* dinit, cudaStream_t st) {
-    dim3 gsc((P.p * P.r + 127) / 128, P.h, P.b);
     mm_prof_mark(KID_COT_SCAN, 1, st);
-    k_cot_scan<<<gsc, 128, 0, st>>>(P, E, Dn, dinit);
+    if ((P.p * P.r) % 4 == 0 && aligned16(E) && aligned16(dinit))
+        k_cot_scan<4><<<scan_grid<4>(P), SCAN_T, 0, st>>>(P, E, Dn, dinit);
+    else
+        k_cot_scan<1><<<scan_grid<1>(P), SCAN_T, 0, st>>>(P, E, Dn, dinit);
     mm_prof_mark(KID_COT_SCAN, 0, st);
     return cudaGetLastError();
 }
