@@ -75,12 +75,20 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
         if ((e = encode(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, xhat, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
+        box[3] = 8;  // 8 consecutive tokens: rows (token, channel)
+        if ((e = encode(&maps->x8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, xhat, dims, str, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
     }
     {   // bhat as [b*s, C, h, r/64, 64] bf16; box = one 64-wide half of the C rows
         cuuint64_t dims[5] = {64, (cuuint64_t)P.r / 64, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
         cuuint64_t str[4] = {128, (cuuint64_t)P.r * 2, (cuuint64_t)P.h * P.r * 2, (cuuint64_t)P.C * P.h * P.r * 2};
         cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)P.C, 1};
         if ((e = encode(&maps->b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bhat, dims, str, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
+        box[4] = 8;
+        if ((e = encode(&maps->b8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bhat, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
     }
@@ -144,7 +152,7 @@ cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char*, cudaStream
     cudaError_t e = encode_maps(P, A.xhat, A.bhat, A.rot, A.da, &maps);
     if (e != cudaSuccess) return e;
     const int grid = fa.items < sm_count() ? fa.items : sm_count();
-    if ((e = launch_tc_fwd(CHUNK_END, fa, maps, grid, st)) != cudaSuccess) return e;
+    if ((e = launch_tc_end(fa, maps, st)) != cudaSuccess) return e;
     if ((e = generic_carry_scan(P, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
     return launch_tc_fwd(FWD_MOMENTS, fa, maps, grid, st);
 }
@@ -183,7 +191,7 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     TensorMaps maps;
     if ((e = encode_maps(P, A.xhat, A.bhat, A.rot, A.da, &maps)) != cudaSuccess) return e;
     int grid = fa.items < sm_count() ? fa.items : sm_count();
-    if ((e = launch_tc_fwd(CHUNK_END, fa, maps, grid, st)) != cudaSuccess) return e;
+    if ((e = launch_tc_end(fa, maps, st)) != cudaSuccess) return e;
     if ((e = generic_carry_scan(P, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
     if (grid > kMaxBwdGrid) grid = kMaxBwdGrid;
     float* anchors = reinterpret_cast<float*>(scratch);
