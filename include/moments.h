@@ -30,6 +30,8 @@
  *     nothing and receive exactly zero gradient; values above s are clamped to s.
  *   - chunk_len must divide s.  It sets the granularity of the chunk-boundary carries; the
  *     result does not depend on it (the chunked recurrence is exact).
+ *   - Every tensor pointer must be 16-byte aligned (as cudaMalloc and PyTorch allocations
+ *     are); a misaligned one is rejected with MM_ERR_INVALID_ARG.
  *   - All device pointers are owned by the caller.  The library never allocates, frees or
  *     synchronises: every call only enqueues work on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream) and returns.  Outputs are overwritten, never accumulated.

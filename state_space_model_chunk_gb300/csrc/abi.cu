@@ -112,12 +112,18 @@ Layout layout(const mm_problem* P, int backward) {
 template <typename T>
 T* at(void* base, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(base) + off); }
 
+// Tensor pointers must start on a 16-byte boundary (the kernels move 16-byte vectors and tensor
+// copies); NULL passes (presence is checked separately).
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
 mm_status common_checks(const mm_problem* P, const void* xhat, const void* bhat, const float* da,
                         const float* rot, const float* initial, const int64_t* valid, void* ws,
                         size_t ws_bytes, int backward, Layout* L) {
     if (!valid_problem(P)) return MM_ERR_INVALID_ARG;
     if (!xhat || !bhat || !da || !initial || !valid) return MM_ERR_INVALID_ARG;
     if (rot_width(P) > 0 && !rot) return MM_ERR_INVALID_ARG;
+    if (misaligned(xhat) || misaligned(bhat) || misaligned(da) || misaligned(rot) || misaligned(initial))
+        return MM_ERR_INVALID_ARG;
     for (int64_t i = 0; i < P->b; ++i)
         if (valid[i] < 0) return MM_ERR_INVALID_ARG;
     if (P->b > MM_MAX_B) return MM_ERR_UNSUPPORTED;
@@ -237,7 +243,7 @@ mm_status moments_fwd(const mm_problem* prob, const void* xhat, const void* bhat
     Layout L;
     mm_status st = common_checks(prob, xhat, bhat, da, rot, initial, valid_len_host, workspace, ws_bytes, 0, &L);
     if (st != MM_OK) return st;
-    if (!m2 || !m1) return MM_ERR_INVALID_ARG;
+    if (!m2 || !m1 || misaligned(m2) || misaligned(m1)) return MM_ERR_INVALID_ARG;
     MMParams M;
     fill_params(prob, valid_len_host, &M);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -270,6 +276,9 @@ mm_status moments_bwd(const mm_problem* prob, const void* xhat, const void* bhat
     if (st != MM_OK) return st;
     if (!d_m2 || !d_m1 || !d_xhat || !d_bhat || !d_da || !d_initial) return MM_ERR_INVALID_ARG;
     if (rot_width(prob) > 0 && !d_rot) return MM_ERR_INVALID_ARG;
+    if (misaligned(d_m2) || misaligned(d_m1) || misaligned(d_xhat) || misaligned(d_bhat) || misaligned(d_da) ||
+        misaligned(d_rot) || misaligned(d_initial))
+        return MM_ERR_INVALID_ARG;
     MMParams M;
     fill_params(prob, valid_len_host, &M);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);

@@ -79,6 +79,10 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
         if ((e = encode(&maps->x8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, xhat, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
+        box[3] = 32;
+        if (P.C <= 4 && (e = encode(&maps->x32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, xhat, dims, str, box,
+                                    CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
     }
     {   // bhat as [b*s, C, h, r/64, 64] bf16; box = one 64-wide half of the C rows
         cuuint64_t dims[5] = {64, (cuuint64_t)P.r / 64, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
@@ -90,6 +94,10 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
         box[4] = 8;
         if ((e = encode(&maps->b8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bhat, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
+        box[4] = 32;
+        if (P.C <= 4 && (e = encode(&maps->b32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bhat, dims, str, box,
+                                    CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
     }
     if (P.rw > 0) {  // rot as [b*s, h, rw] fp32; box = one (token, head)
@@ -199,5 +207,5 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
         cudaSuccess)
         return e;
     if ((e = generic_cot_scan(P, A.E, A.Dn, A.dinit, st)) != cudaSuccess) return e;
-    return launch_tc_bwd(1, fa, A.E, anchors, A.dm2, A.dm1, A.dxhat, A.dbhat, A.dda, A.drot, maps, grid, st);
+    return launch_tc_corr(fa, A.da, A.E, A.dxhat, A.dbhat, A.dda, maps, st);
 }

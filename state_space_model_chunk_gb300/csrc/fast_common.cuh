@@ -27,6 +27,7 @@ struct FastArgs {
 struct TensorMaps {
     CUtensorMap x, b, rot, da, da64;  // da: 4 heads x 1 token; da64: 4 heads x 64 tokens
     CUtensorMap x8, b8;               // xhat / bhat rows of 8 consecutive tokens
+    CUtensorMap x32, b32;             // ... and of 32
 };
 
 constexpr int kMaxBwdGrid = 160;  // CTAs of the backward kernels (anchor slots in the workspace)
@@ -224,6 +225,8 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
 int sm_count();
 cudaError_t launch_tc_fwd(int mode, const FastArgs& args, const TensorMaps& maps, int grid, cudaStream_t st);
 cudaError_t launch_tc_end(const FastArgs& fa, const TensorMaps& maps, cudaStream_t st);
+cudaError_t launch_tc_corr(const FastArgs& fa, const float* da, const float* E, void* dx, void* db, float* dda,
+                           const TensorMaps& maps, cudaStream_t st);
 size_t bwd_anchor_bytes();
 cudaError_t launch_tc_bwd(int mode, const FastArgs& fa, float* E, float* anchors, const float* dm2, const float* dm1,
                           void* dx, void* db, float* dda, float* drot, const TensorMaps& maps, int grid,

@@ -1,0 +1,414 @@
+// fast_corr.cu -- boundary-cotangent correction of the recompute backward as two GEMMs per chunk.
+//
+// For every chunk n but the last processed one, with dH = dH(n+1) the cotangent of the state the
+// chunk hands on ("mamba3/moments/backward.rs", module header "Gradient math": the d_h+ terms),
+// sc_t = exp(a_last - a_t) and a_t the inclusive cumulative sum of da inside the chunk:
+//
+//   U_{t,c} = dH bhat_{t,c}   (p values)          d_xhat_{t,c} += sc_t U_{t,c}
+//   V_{t,c} = dH^T xhat_{t,c} (r values)          d_bhat_{t,c} += sc_t V_{t,c}
+//   omega_t = sum_c <xhat_{t,c}, U_{t,c}>          d_da_s += D_n <dH, h_-(n)> + sum_{j<s} sc_j omega_j
+//
+// Over the rows (t, c) of 32 tokens these are U = Bhat dH^T (M = 32 C, N = p, K = r) and
+// V = Xhat dH (M = 32 C, N = r, K = p).  One bf16 dH tile [p][r] in the 128-byte-swizzled layout
+// is the K-major B operand of the first and the MN-major B operand of the second; the xhat /
+// bhat rows come by TMA.  The epilogue (lanes = rows (t, c), two threads per row) scales, adds
+// into d_xhat / d_bhat in place, and accumulates omega.
+//
+// Warp roles: 0 TMA, 1 MMA, 2-9 dH tile + epilogue.  Every wait is bounded; a timeout sets the
+// workspace error word and the CTA winds down.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "fast.h"
+#include "fast_common.cuh"
+#include "prof.h"
+#include "tc.cuh"
+
+namespace fastcorr {
+
+using namespace fastk;
+
+constexpr int NTHR = 320;
+constexpr int NEW = 8;                     // epilogue warps
+constexpr int TPS = 32;                    // tokens per stage (rows 32 C <= 128)
+constexpr int NS = 3;                      // stages
+constexpr uint32_t SLOT = 16384;           // 128 rows x 128 B
+constexpr uint32_t STAGE = 3 * SLOT;       // xhat | bhat r 0..63 | bhat r 64..127
+constexpr uint32_t DHT = 16384;            // dH tile: 64 rows x 2 blocks x 128 B
+constexpr uint32_t OFF_DH = NS * STAGE;    // 2 dH tiles
+constexpr uint32_t OFF_SC = OFF_DH + 2 * DHT;   // sc_t, 64 fp32
+constexpr uint32_t OFF_OM = OFF_SC + 256;       // omega, 2 items x 64 fp32
+constexpr uint32_t OFF_MISC = OFF_OM + 512;     // dot (2 items), D_n
+constexpr uint32_t OFF_CTL = OFF_MISC + 64;
+constexpr uint32_t SMEM_BYTES = OFF_CTL + 256 + 1024;
+static_assert(OFF_DH % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles");
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+struct Ctl {
+    uint64_t full[NS], empty[NS];
+    uint64_t accfull[2], accfree[2];
+    uint64_t dhfull[2], dhfree[2];
+    uint64_t fin;
+    uint32_t tbase;
+    int abort;
+};
+static_assert(sizeof(Ctl) <= 256, "control block");
+
+constexpr uint32_t TM_BUF = 256;  // per accumulator buffer: U at +0 (64 columns), V at +64 (r columns)
+
+struct CItem {
+    int bb, hh, n;
+};
+
+__host__ __device__ inline int count_corr(const MMParams& P) {
+    int c = 0;
+    for (int bb = 0; bb < P.b; ++bb) {
+        const int pr = mm_processed(P, bb);
+        c += P.h * (pr > 1 ? pr - 1 : 0);
+    }
+    return c;
+}
+
+// Item -> (batch row, head, chunk) over the chunks followed by another processed chunk.
+__device__ inline CItem decode(const MMParams& P, int item) {
+    int bb = 0, base = 0;
+    for (; bb < P.b - 1; ++bb) {
+        const int pr = mm_processed(P, bb);
+        const int cnt = P.h * (pr > 1 ? pr - 1 : 0);
+        if (item < base + cnt) break;
+        base += cnt;
+    }
+    const int pr = mm_processed(P, bb);
+    const int per = pr > 1 ? pr - 1 : 1;
+    const int rem = item - base;
+    CItem I;
+    I.bb = bb;
+    I.hh = rem / per;
+    I.n = rem - I.hh * per;
+    return I;
+}
+
+__device__ __forceinline__ int range_begin(int items, int cta) { return (int)(((int64_t)cta * items) / gridDim.x); }
+
+__device__ __forceinline__ void fail(Ctl* ctl, int* err, int code) {
+    ctl->abort = 1;
+    atomicExch(err, code);
+}
+
+struct CorrArgs {
+    FastArgs F;        // problem, Hc (carries), err
+    const float* da;   // [b,s,h]
+    const float* E;    // [b,h,nc,p,r] dH(n+1) per chunk
+    __nv_bfloat16* dx;
+    __nv_bfloat16* db;
+    float* dda;
+};
+
+__global__ void __launch_bounds__(NTHR, 1)
+    tc_corr_kernel(const __grid_constant__ CorrArgs B, const __grid_constant__ CUtensorMap tmx32,
+                   const __grid_constant__ CUtensorMap tmb32) {
+    extern __shared__ unsigned char smraw[];
+    unsigned char* sm = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
+    Ctl* ctl = reinterpret_cast<Ctl*>(sm + OFF_CTL);
+    const FastArgs& A = B.F;
+    const MMParams& P = A.P;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int R = P.r, C = P.C;
+    const int items = count_corr(P);
+    const int it0 = range_begin(items, blockIdx.x), it1 = range_begin(items, blockIdx.x + 1);
+    const uint32_t rows = (uint32_t)TPS * C;
+
+    // rows past 32 C of the stage slots, the r >= 64 half (r = 64) and omega start at zero
+    for (uint32_t i = tid; i < OFF_CTL / 16; i += NTHR) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            tc::mbar_init(&ctl->full[s], 1);
+            tc::mbar_init(&ctl->empty[s], NEW);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&ctl->accfull[i], 1);
+            tc::mbar_init(&ctl->accfree[i], NEW);
+            tc::mbar_init(&ctl->dhfull[i], NEW);
+            tc::mbar_init(&ctl->dhfree[i], 1);
+        }
+        tc::mbar_init(&ctl->fin, 1);
+        ctl->abort = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&ctl->tbase, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = ctl->tbase;
+    volatile int* abort = &ctl->abort;
+
+    if (warp == 0) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            uint32_t q = 0;
+            bool ok = true;
+            for (int it = it0; it < it1 && ok; ++it) {
+                const CItem I = decode(P, it);
+                for (int st = 0; st < FL / TPS; ++st, ++q) {
+                    const uint32_t s = q % NS, u = q / NS;
+                    if (u >= 1 && !(ok = tc::mbar_wait(&ctl->empty[s], (u - 1) & 1, abort))) break;
+                    unsigned char* stg = sm + s * STAGE;
+                    tc::mbar_arrive_expect_tx(&ctl->full[s], rows * 128u * (1u + (uint32_t)R / 64u));
+                    const int row = I.bb * P.s + I.n * FL + st * TPS;
+                    tc::tma_load_4d(stg, &tmx32, 0, I.hh, 0, row, &ctl->full[s]);
+                    for (int a = 0; a < R / 64; ++a)
+                        tc::tma_load_5d(stg + (1 + a) * SLOT, &tmb32, 0, a, I.hh, 0, row, &ctl->full[s]);
+                }
+            }
+            if (!ok) fail(ctl, A.err, 41);
+            int never = 0;  // every issued copy lands before the CTA exits
+            for (uint32_t s = 0; s < NS && q > s; ++s) {
+                const uint32_t last = (q - 1 - s) / NS;
+                tc::mbar_wait(&ctl->full[s], last & 1, &never, 1u << 20);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            const uint32_t idU = tc::idesc_bf16(128, 64, 0, 0);  // U: A = bhat rows (K = r), B = dH (K-major)
+            const uint32_t idV = tc::idesc_bf16(128, R, 0, 1);   // V: A = xhat rows (K = p), B = dH (MN-major)
+            const uint32_t s0 = tc::smem_u32(sm), dh0 = tc::smem_u32(sm + OFF_DH);
+            uint32_t q = 0, li = 0;
+            bool ok = true;
+            for (int it = it0; it < it1 && ok; ++it, ++li) {
+                const uint32_t ib = li & 1;
+                const uint32_t dh = dh0 + ib * DHT;
+                if (!(ok = tc::mbar_wait(&ctl->dhfull[ib], (li >> 1) & 1, abort))) break;
+                for (int st = 0; st < FL / TPS; ++st, ++q) {
+                    const uint32_t s = q % NS, u = q / NS, ab = q & 1, ua = q >> 1;
+                    if (!(ok = tc::mbar_wait(&ctl->full[s], u & 1, abort))) break;
+                    if (ua >= 1 && !(ok = tc::mbar_wait(&ctl->accfree[ab], (ua - 1) & 1, abort))) break;
+                    tc::tc_fence_after();
+                    const uint32_t xs = s0 + s * STAGE, bs = xs + SLOT;
+                    const uint32_t tu = tbase + ab * TM_BUF, tv = tu + 64;
+                    for (int ks = 0; ks < R / 16; ++ks)
+                        tc::mma_bf16(tu, tc::sdesc_sw128(bs + (ks >> 2) * SLOT + 32u * (ks & 3), 16, 1024),
+                                     tc::sdesc_sw128(dh + (ks >> 2) * 8192u + 32u * (ks & 3), 16, 1024), idU,
+                                     ks > 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_bf16(tv, tc::sdesc_sw128(xs + 32u * ks, 16, 1024),
+                                     tc::sdesc_sw128(dh + 2048u * ks, 8192, 1024), idV, ks > 0);
+                    tc::mma_commit(&ctl->accfull[ab]);
+                }
+                if (ok) tc::mma_commit(&ctl->dhfree[ib]);
+            }
+            if (!ok) fail(ctl, A.err, 42);
+            tc::mma_commit(&ctl->fin);
+            int never = 0;  // in-flight MMAs must finish before the TMEM is released
+            tc::mbar_wait(&ctl->fin, 0, &never, 1u << 20);
+        }
+    } else {
+        // ================================================================ dH tile + epilogue
+        const int ew = warp - 2, etid = tid - 64;
+        const int hf = ew >> 2;                     // which half of the row's columns
+        const int k = ((warp & 3) << 5) + lane;     // TMEM lane = stage row (t, c)
+        const uint32_t lane_addr = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+        float* sc = reinterpret_cast<float*>(sm + OFF_SC);
+        float* misc = reinterpret_cast<float*>(sm + OFF_MISC);  // [0..1] dot per item parity, [2] D_n
+        const bool row_ok = (uint32_t)k < rows;
+        const int tl = k / C, cc = k - (k / C) * C;
+        uint32_t q = 0, li = 0;
+        bool ok = true;
+        auto check = [&](bool r) {  // the first failed wait stops the whole CTA at once
+            if (!r && ok) {
+                ok = false;
+                fail(ctl, A.err, 43);
+            }
+        };
+        for (int it = it0; it < it1; ++it, ++li) {
+            const CItem I = decode(P, it);
+            const uint32_t ib = li & 1;
+            float* om = reinterpret_cast<float*>(sm + OFF_OM) + ib * 64;
+            // ---- decay weights sc_t of the chunk (all 64 of its tokens are valid) and D_n
+            if (ew == 0) {
+                const int t0 = 2 * lane, t1 = t0 + 1;
+                const float v0 = B.da[off_da(P, I.bb, I.n * FL + t0, I.hh)];
+                const float v1 = B.da[off_da(P, I.bb, I.n * FL + t1, I.hh)];
+                float sum = v0 + v1;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, sum, off);
+                    if (lane >= off) sum += o;
+                }
+                const float alast = __shfl_sync(0xffffffffu, sum, 31);
+                sc[t1] = __expf(alast - sum);
+                sc[t0] = __expf(alast - (sum - v1));
+                if (lane == 0) misc[2] = __expf(alast);
+            }
+            // ---- dH tile (bf16, [p][r] swizzled) and <dH, h_-(n)>
+            if (li >= 2) check(tc::mbar_wait(&ctl->dhfree[ib], ((li - 2) >> 1) & 1, abort));
+            {
+                unsigned char* dht = sm + OFF_DH + ib * DHT;
+                const float* src = B.E + off_carry(P, I.bb, I.hh, I.n);
+                const float* hin = A.Hc + off_carry(P, I.bb, I.hh, I.n);
+                float dot = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int id = i * (NEW * 32) + etid;
+                    const int pp = id >> 4, j16 = id & 15, blk = j16 >> 3, j = j16 & 7;
+                    const int col = 64 * blk + 8 * j;
+                    uint4 w = make_uint4(0, 0, 0, 0);
+                    if (col < R) {
+                        const float4 e0 = *reinterpret_cast<const float4*>(src + pp * R + col);
+                        const float4 e1 = *reinterpret_cast<const float4*>(src + pp * R + col + 4);
+                        const float4 h0 = *reinterpret_cast<const float4*>(hin + pp * R + col);
+                        const float4 h1 = *reinterpret_cast<const float4*>(hin + pp * R + col + 4);
+                        dot += e0.x * h0.x + e0.y * h0.y + e0.z * h0.z + e0.w * h0.w;
+                        dot += e1.x * h1.x + e1.y * h1.y + e1.z * h1.z + e1.w * h1.w;
+                        w.x = tc::pack_bf16x2(e0.x, e0.y);
+                        w.y = tc::pack_bf16x2(e0.z, e0.w);
+                        w.z = tc::pack_bf16x2(e1.x, e1.y);
+                        w.w = tc::pack_bf16x2(e1.z, e1.w);
+                    }
+                    *reinterpret_cast<uint4*>(dht + tc::sw128_chunk(64, blk, pp, j)) = w;
+                }
+                dot = warp_sum(dot);
+                if (lane == 0) atomicAdd(&misc[ib], dot);
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ctl->dhfull[ib]);
+            }
+            named_barrier_sync(1, NEW * 32);  // sc, D_n and the dot are complete
+            // ---- the two 32-token stages
+            for (int st = 0; st < FL / TPS; ++st, ++q) {
+                const uint32_t s = q % NS, ab = q & 1;
+                const int t = st * TPS + tl;
+                const int tok = I.n * FL + t;
+                // this thread's part of the row: U columns [32 hf, 32 hf + 32), V columns [64 hf, 64 hf + 64)
+                const bool has_v = 64 * hf < R;
+                uint4 ox[4], ob[8];
+                __nv_bfloat16* px = B.dx + off_x(P, I.bb, tok, cc, I.hh) + 32 * hf;
+                __nv_bfloat16* pb = B.db + off_b(P, I.bb, tok, cc, I.hh) + 64 * hf;
+                if (row_ok) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) ox[i] = reinterpret_cast<const uint4*>(px)[i];
+                    if (has_v) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) ob[i] = reinterpret_cast<const uint4*>(pb)[i];
+                    }
+                }
+                check(tc::mbar_wait(&ctl->full[s], (q / NS) & 1, abort));  // the stage's xhat rows are read below
+                check(tc::mbar_wait(&ctl->accfull[ab], (q >> 1) & 1, abort));
+                tc::tc_fence_after();
+                const uint32_t tu = lane_addr + ab * TM_BUF, tv = tu + 64;
+                float u[32];
+                tc::tmem_ld16(tu + 32 * hf, *reinterpret_cast<float(*)[16]>(&u[0]));
+                tc::tmem_ld16(tu + 32 * hf + 16, *reinterpret_cast<float(*)[16]>(&u[16]));
+                tc::tmem_wait_ld();
+                // omega partial: <xhat row, U row> over this half (xhat row from the stage tile)
+                float w = 0.f;
+                {
+                    const unsigned char* xr = sm + s * STAGE + k * 128;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int j = 4 * hf + jj;
+                        const uint4 v = *reinterpret_cast<const uint4*>(xr + ((j ^ (k & 7)) << 4));
+                        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            w = fmaf(__uint_as_float(wd[e] << 16), u[8 * jj + 2 * e], w);
+                            w = fmaf(__uint_as_float(wd[e] & 0xFFFF0000u), u[8 * jj + 2 * e + 1], w);
+                        }
+                    }
+                }
+                if (row_ok) atomicAdd(&om[t], w);
+                const float scv = sc[t];
+                if (row_ok) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t* wd = reinterpret_cast<uint32_t*>(&ox[i]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float lo = __uint_as_float(wd[e] << 16) + scv * u[8 * i + 2 * e];
+                            const float hi = __uint_as_float(wd[e] & 0xFFFF0000u) + scv * u[8 * i + 2 * e + 1];
+                            wd[e] = tc::pack_bf16x2(lo, hi);
+                        }
+                        reinterpret_cast<uint4*>(px)[i] = ox[i];
+                    }
+                }
+                if (has_v) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        float v[16];
+                        tc::tmem_ld16(tv + 64 * hf + 16 * g, v);
+                        tc::tmem_wait_ld();
+                        if (row_ok) {
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                uint32_t* wd = reinterpret_cast<uint32_t*>(&ob[2 * g + i]);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float lo = __uint_as_float(wd[e] << 16) + scv * v[8 * i + 2 * e];
+                                    const float hi =
+                                        __uint_as_float(wd[e] & 0xFFFF0000u) + scv * v[8 * i + 2 * e + 1];
+                                    wd[e] = tc::pack_bf16x2(lo, hi);
+                                }
+                                reinterpret_cast<uint4*>(pb)[2 * g + i] = ob[2 * g + i];
+                            }
+                        }
+                    }
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(&ctl->accfree[ab]);
+                    tc::mbar_arrive(&ctl->empty[s]);
+                }
+            }
+            named_barrier_sync(1, NEW * 32);  // omega complete
+            // ---- d_da_s += D_n <dH, h_-> + sum_{j<s} sc_j omega_j
+            if (etid < FL) {
+                const float base = misc[2] * misc[ib];
+                float pre = 0.f;
+                for (int j = 0; j < etid; ++j) pre = fmaf(sc[j], om[j], pre);
+                B.dda[off_da(P, I.bb, I.n * FL + etid, I.hh)] += base + pre;
+            }
+            named_barrier_sync(1, NEW * 32);  // sc / D_n / omega / dot read: free for the next items
+            if (etid < FL) om[etid] = 0.f;
+            if (etid == 0) misc[ib] = 0.f;
+        }
+    }
+    // ---- teardown
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tbase, 512);
+    }
+}
+
+}  // namespace fastcorr
+
+namespace fastk {
+
+cudaError_t launch_tc_corr(const FastArgs& fa, const float* da, const float* E, void* dx, void* db, float* dda,
+                           const TensorMaps& maps, cudaStream_t st) {
+    using namespace fastcorr;
+    const int items = count_corr(fa.P);
+    if (items == 0) return cudaSuccess;
+    CorrArgs a;
+    a.F = fa;
+    a.da = da;
+    a.E = E;
+    a.dx = static_cast<__nv_bfloat16*>(dx);
+    a.db = static_cast<__nv_bfloat16*>(db);
+    a.dda = dda;
+    const int grid = items < sm_count() ? items : sm_count();
+    cudaError_t e = cudaFuncSetAttribute(tc_corr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    mm_prof_mark(KID_FAST_CORRECT, 1, st);
+    tc_corr_kernel<<<grid, NTHR, SMEM_BYTES, st>>>(a, maps.x32, maps.b32);
+    mm_prof_mark(KID_FAST_CORRECT, 0, st);
+    return cudaGetLastError();
+}
+
+}  // namespace fastk

@@ -92,6 +92,10 @@ def test_fwd_rejects_before_enqueue():
     norot = list(FAKE)
     norot[3] = None                                               # rot missing but rope_dim > 0
     assert _call_fwd(spec, norot, [60, 60], ws) == 1
+    for i in (0, 1, 2, 4, 5, 6):                                  # a tensor off a 16-byte boundary
+        odd = list(FAKE)
+        odd[i] = ctypes.c_void_p(0x1000 * (i + 1) + 8)
+        assert _call_fwd(spec, odd, [60, 60], ws) == 1
     big = Spec(**{**spec.__dict__, "b": 600})                      # beyond the parameter block
     assert _call_fwd(big, FAKE, [1] * 600, binding.workspace_bytes(big, False)) == 2
 
@@ -108,6 +112,11 @@ def test_bwd_rejects_before_enqueue():
     rc = lib.moments_bwd(ctypes.byref(Spec(**{**spec.__dict__, "rope_dim": 3}).problem()),
                          *[ctypes.c_void_p(0x1000)] * 5, v, *[ctypes.c_void_p(0x1000)] * 7,
                          ctypes.c_void_p(0x100000), ws, None)
+    assert rc == 1
+    args = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(14)]
+    args[7] = ctypes.c_void_p(0x1000 * 8 + 4)  # d_xhat off a 16-byte boundary
+    rc = lib.moments_bwd(ctypes.byref(spec.problem()), *args[:5], v, *args[5:12], ctypes.c_void_p(0x100000),
+                         ws, None)
     assert rc == 1
 
 
