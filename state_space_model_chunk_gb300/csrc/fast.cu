@@ -162,7 +162,7 @@ cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char*, cudaStream
     const int grid = fa.items < sm_count() ? fa.items : sm_count();
     if ((e = launch_tc_end(fa, maps, st)) != cudaSuccess) return e;
     if ((e = generic_carry_scan(P, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
-    return launch_tc_fwd(FWD_MOMENTS, fa, maps, grid, st);
+    return launch_tc_fwd(fa, maps, grid, st);
 }
 
 cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cudaStream_t st) {
@@ -203,7 +203,7 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     if ((e = generic_carry_scan(P, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
     if (grid > kMaxBwdGrid) grid = kMaxBwdGrid;
     float* anchors = reinterpret_cast<float*>(scratch);
-    if ((e = launch_tc_bwd(0, fa, A.E, anchors, A.dm2, A.dm1, A.dxhat, A.dbhat, A.dda, A.drot, maps, grid, st)) !=
+    if ((e = launch_tc_bwd(fa, A.E, anchors, A.dm2, A.dm1, A.dxhat, A.dbhat, A.dda, A.drot, maps, grid, st)) !=
         cudaSuccess)
         return e;
     if ((e = generic_cot_scan(P, A.E, A.Dn, A.dinit, st)) != cudaSuccess) return e;

@@ -2,10 +2,9 @@
 // p = 64, r in {64, 128}, C <= 4).
 //
 // Work item = a pair of 64-token chunks of one (batch row, head); the two chunks share the 128
-// TMEM lanes (row m = (chunk, p)) as in the forward.  Two modes:
-//
-// LOCAL  -- the chunk's own backward with zero incoming carry cotangent ("backward.rs", module
-//   header "Gradient math", with the d_h+ term split off):
+// TMEM lanes (row m = (chunk, p)) as in the forward.  This kernel is the chunk's own backward with
+// zero incoming carry cotangent ("backward.rs", module header "Gradient math", with the d_h+
+// term split off; fast_corr.cu adds it once the cotangent scan has run):
 //   phase A  forward sweep h = e^{da} h + W from the chunk carry (W by one block-diagonal MMA per
 //            token); the state after every 8th token is kept as an fp32 anchor in this CTA's
 //            workspace slot (7 anchors; the chunk carry is anchor 0).
@@ -19,9 +18,6 @@
 //            d_bhat = g^T xhat as N = 16 MMAs.  After the chunk: e_n = e_0 g_0.
 //            The span is software-pipelined: while the CUDA cores finish the cotangent work of
 //            token t, the tensor cores already run d_c of token t-1 and the prefix of t-2.
-// CORR   -- adds the carry cotangent dH = dH(n+1) of every chunk but the last processed one:
-//   d_xhat_jc += sc_j dH bhat_jc, d_bhat_jc += sc_j dH^T xhat_jc (the same N = 16 MMAs with the
-//   constant bf16 dH tile), d_da_s += D_n <dH, h_-> + sum_{j<s} sc_j <dH, W_j>, sc_j = e^{a_last-a_j}.
 //
 // Warp roles: 0-7 compute (two threads per row, 64 columns each, handled as two 32-column
 // passes whose rotation partners stay inside the pass), 8 TMA, 9 MMA.  d_rot and d_da are summed
@@ -60,8 +56,6 @@ constexpr uint32_t OFF_ACUM = 206848;            // cumulative da, 2 chunks x 64
 constexpr uint32_t OFF_COEF = 207360;            // span cos|sin: 8 tokens x 2 chunks x 128 fp32
 constexpr uint32_t OFF_LT = 215552;              // span decay matrix L: 2 chunks x 8 x 8 fp32
 constexpr uint32_t OFF_M1 = 216064;              // d_m1 [128] fp32
-constexpr uint32_t OFF_OM = 216576;              // correction: 2 chunks x 64 fp32 omega_j
-constexpr uint32_t OFF_MISC = 217088;            // correction: dot / base terms
 constexpr uint32_t OFF_CTL = 217216;
 constexpr uint32_t SMEM_BYTES = OFF_CTL + 512 + 1024;
 static_assert(OFF_SX % 1024 == 0 && OFF_SB % 1024 == 0 && OFF_PB % 1024 == 0 && OFF_PA % 1024 == 0, "tiles");
@@ -86,18 +80,16 @@ static_assert(sizeof(Ctl) <= 512, "control block");
 // tensor memory columns
 constexpr uint32_t TM_P = 0, TM_DC = 128, TM_AN = 256, TM_DX = 384, TM_DB = 400, TM_COLS = 512;
 
-enum { LOCAL = 0, CORR = 1 };
-
 struct BwdArgs {
     FastArgs F;         // problem, items, Hc (carries), Dn, err
-    float* E;           // [b,h,nc,p,r]: LOCAL writes e_n; CORR reads dH(n+1)
+    float* E;           // [b,h,nc,p,r]: e_n of every chunk
     float* anchors;     // [grid][7][128][128] fp32 anchor slots
     const float* dm2;   // [b,h,r,r]
     const float* dm1;   // [b,h,r]
     __nv_bfloat16* dx;  // d_xhat
     __nv_bfloat16* db;  // d_bhat
-    float* dda;         // d_da (zeroed by the host; LOCAL and CORR add into it)
-    float* drot;        // d_rot (zeroed by the host; LOCAL adds into it)
+    float* dda;         // d_da (zeroed by the host; added into)
+    float* drot;        // d_rot (zeroed by the host; added into)
 };
 
 __device__ __forceinline__ void fail(Ctl* ctl, int* err, int code) {
@@ -121,74 +113,45 @@ __device__ __forceinline__ void transpose_reduce16(float (&v)[16], int lane) {
     v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// 16 columns (group gcol of 16) of row m of a bf16 [128 x 128] swizzled tile, as floats / from floats.
-__device__ __forceinline__ void read_tile16(const unsigned char* tile, int m, int gcol, float (&v)[16]) {
-    const uint32_t hv = gcol >> 2, j0 = 2 * (gcol & 3);
-#pragma unroll
-    for (int hj = 0; hj < 2; ++hj) {
-        const uint4 w = *reinterpret_cast<const uint4*>(tile + tc::sw128_chunk(128, hv, m, j0 + hj));
-        v[8 * hj + 0] = bf16lo(w.x); v[8 * hj + 1] = bf16hi(w.x);
-        v[8 * hj + 2] = bf16lo(w.y); v[8 * hj + 3] = bf16hi(w.y);
-        v[8 * hj + 4] = bf16lo(w.z); v[8 * hj + 5] = bf16hi(w.z);
-        v[8 * hj + 6] = bf16lo(w.w); v[8 * hj + 7] = bf16hi(w.w);
-    }
-}
-__device__ __forceinline__ void write_tile16(unsigned char* tile, int m, int gcol, const float (&v)[16], bool zero) {
-    const uint32_t hv = gcol >> 2, j0 = 2 * (gcol & 3);
-#pragma unroll
-    for (int hj = 0; hj < 2; ++hj) {
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (!zero) {
-            w.x = tc::pack_bf16x2(v[8 * hj + 0], v[8 * hj + 1]);
-            w.y = tc::pack_bf16x2(v[8 * hj + 2], v[8 * hj + 3]);
-            w.z = tc::pack_bf16x2(v[8 * hj + 4], v[8 * hj + 5]);
-            w.w = tc::pack_bf16x2(v[8 * hj + 6], v[8 * hj + 7]);
-        }
-        *reinterpret_cast<uint4*>(tile + tc::sw128_chunk(128, hv, m, j0 + hj)) = w;
-    }
-}
-
-// Slots of a 32-column pass: rotation partners stay inside (half-split, r = 64: slots 0/1).
-template <int LAYB>
-__device__ __forceinline__ int slot_a(int pass) { return LAYB ? 2 * pass : pass; }
-template <int LAYB>
-__device__ __forceinline__ int slot_b(int pass) { return LAYB ? 2 * pass + 1 : pass + 2; }
-
 // (out_a, out_b) = rotation of the two slots of a pass: de-rotation R(-theta) / Q (x) . (TR =
 // false) or its transpose (TR = true).  cf: cos at [0,64), sin at [64,128) of this token and
 // chunk's angles; qt: its raw quaternions.  ka / kb: first column of slot a / b.
 template <int ROTK, int LAYB, bool TR>
 __device__ __forceinline__ void rot_pass(const MMParams& P, int pass, int ka, int kb, float (&a)[16], float (&b)[16],
                                          const float* cf, const float* qt) {
+    // cf holds cos / sin for all 64 angle slots; slots at or past the rotated width hold (1, 0)
     if (ROTK == ROT_PAIRWISE) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
             float(&v)[16] = s ? b : a;
-            const int k0 = s ? kb : ka;
+            const int i0 = (s ? kb : ka) >> 1;  // 8 consecutive angles
+            float cs[8], sn[8];
+            *reinterpret_cast<float4*>(&cs[0]) = *reinterpret_cast<const float4*>(cf + i0);
+            *reinterpret_cast<float4*>(&cs[4]) = *reinterpret_cast<const float4*>(cf + i0 + 4);
+            *reinterpret_cast<float4*>(&sn[0]) = *reinterpret_cast<const float4*>(cf + 64 + i0);
+            *reinterpret_cast<float4*>(&sn[4]) = *reinterpret_cast<const float4*>(cf + 64 + i0 + 4);
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
-                const int i = (k0 + e) >> 1;
-                if (i < P.na) {
-                    const float cs = cf[i], sn = TR ? -cf[64 + i] : cf[64 + i];
-                    const float x = v[e], y = v[e + 1];
-                    v[e] = cs * x + sn * y;
-                    v[e + 1] = -sn * x + cs * y;
-                }
+                const float c_ = cs[e / 2], s_ = TR ? -sn[e / 2] : sn[e / 2];
+                const float x = v[e], y = v[e + 1];
+                v[e] = fmaf(c_, x, s_ * y);
+                v[e + 1] = fmaf(c_, y, -s_ * x);
             }
         }
     } else if (ROTK == ROT_HALF) {
         if (LAYB && pass == 1) return;  // padding columns of r = 64
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int i = ka + e;
-            if (i < P.na) {
-                const float cs = cf[i], sn = TR ? -cf[64 + i] : cf[64 + i];
+        for (int e4 = 0; e4 < 16; e4 += 4) {
+            const float4 c4 = *reinterpret_cast<const float4*>(cf + ka + e4);
+            const float4 s4 = *reinterpret_cast<const float4*>(cf + 64 + ka + e4);
+            const float cs[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = e4 + j;
+                const float c_ = cs[j], s_ = TR ? -sn[j] : sn[j];
                 const float x = a[e], y = b[e];
-                a[e] = cs * x + sn * y;
-                b[e] = -sn * x + cs * y;
+                a[e] = fmaf(c_, x, s_ * y);
+                b[e] = fmaf(c_, y, -s_ * x);
             }
         }
     } else if (ROTK == ROT_QUAT) {
@@ -231,7 +194,7 @@ enum : uint32_t {
     B_ITEM = 6, B_SPAN, B_PB, B_PA, B_P, B_C, B_DC, B_G, B_DX, B_ITEMDONE, B_SPANFREE,
     U_PRE = 24, U_DC, U_DX, U_PA, U_C, U_G, U_SPAN
 };
-template <int MODE, int ROTK, int LAYB>
+template <int ROTK, int LAYB>
 __global__ void __launch_bounds__(NTHR, 1)
     tc_bwd_kernel(const __grid_constant__ BwdArgs B, const __grid_constant__ CUtensorMap tmx,
                   const __grid_constant__ CUtensorMap tmb, const __grid_constant__ CUtensorMap tmr,
@@ -311,7 +274,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     if (I.exists[ch])
                         tc::tma_load_2d(sm + OFF_IDA + ch * 1024, &tmd, I.hh & ~3, I.bb * P.s + (2 * I.k + ch) * FL,
                                         &ctl->itemfull);
-                // forward sweep (LOCAL) / correction tokens (CORR) through the ring
+                // forward sweep tokens through the ring
                 for (int t = 0; t < I.T[0] && ok; ++t, ++q) {
                     const uint32_t s = q % NS, u = q / NS;
                     if (u >= 1) ok &= tc::mbar_wait(&ctl->empty[s], (u - 1) & 1, abort);
@@ -328,7 +291,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                             tc::tma_load_5d(st + 4096 + a * 2048 + ch * 1024, &tmb, 0, a, I.hh, 0, row, &ctl->full[s]);
                     }
                 }
-                if (MODE == LOCAL && ok) {
+                if (ok) {
                     const int nsp = (I.T[0] + SPAN - 1) / SPAN;
                     for (int sg = nsp - 1; sg >= 0 && ok; --sg) {
                         if (pr.once(U_SPAN)) ok &= tc::mbar_wait(&ctl->spanfree, pr.next(B_SPANFREE), abort);
@@ -373,8 +336,8 @@ __global__ void __launch_bounds__(NTHR, 1)
             bool ok = true;
             // d_xhat / d_bhat MMAs: A = g tile (K-major rows (ch,p) / MN-major columns r), B = one
             // token's bhat / xhat tile [16 rows (8 ch + c)][128] K-major.
-            auto issue_dx = [&](uint32_t sxb, uint32_t sbb, bool wait_g, bool free_g) -> bool {
-                if (wait_g && !tc::mbar_wait(&ctl->gfull, pr.next(B_G), abort)) return false;
+            auto issue_dx = [&](uint32_t sxb, uint32_t sbb) -> bool {
+                if (!tc::mbar_wait(&ctl->gfull, pr.next(B_G), abort)) return false;
                 if (pr.once(U_DX) && !tc::mbar_wait(&ctl->dxfree, pr.next(B_DX), abort)) return false;
                 tc::tc_fence_after();
 #pragma unroll
@@ -387,7 +350,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                  tc::sdesc_sw128(sxb + boff, 16, 1024), idDB, ks > 0);
                 }
                 tc::mma_commit(&ctl->dxfull);
-                if (free_g) tc::mma_commit(&ctl->gfree);
+                tc::mma_commit(&ctl->gfree);
                 return true;
             };
             auto issue_prefix = [&](int o) -> bool {
@@ -422,28 +385,23 @@ __global__ void __launch_bounds__(NTHR, 1)
                     const uint32_t s = q % NS;
                     const uint32_t xb = s_ring + s * 8192, bb_ = xb + 4096;
                     if (!(ok = tc::mbar_wait(&ctl->full[s], pr.next(B_FULL + s), abort))) break;
-                    if (MODE == LOCAL) {
-                        const uint32_t wb = nw & 1;
-                        if (nw >= 2 && !(ok = tc::mbar_wait(&ctl->wfree[wb], pr.next(B_W + wb), abort))) break;
-                        tc::tc_fence_after();
-                        tc::mma_bf16(tbase + (wb ? TM_DC : TM_P), tc::sdesc_sw128(xb, 2048, 1024),
-                                     tc::sdesc_sw128(bb_, 2048, 1024), idW, 0);
-                        ++nw;
-                        tc::mma_commit(&ctl->wfull[wb]);
-                        tc::mma_commit(&ctl->empty[s]);
-                    } else {
-                        if (!(ok = issue_dx(xb, bb_, t == 0, t == I.T[0] - 1))) break;
-                        tc::mma_commit(&ctl->empty[s]);
-                    }
+                    const uint32_t wb = nw & 1;
+                    if (nw >= 2 && !(ok = tc::mbar_wait(&ctl->wfree[wb], pr.next(B_W + wb), abort))) break;
+                    tc::tc_fence_after();
+                    tc::mma_bf16(tbase + (wb ? TM_DC : TM_P), tc::sdesc_sw128(xb, 2048, 1024),
+                                 tc::sdesc_sw128(bb_, 2048, 1024), idW, 0);
+                    ++nw;
+                    tc::mma_commit(&ctl->wfull[wb]);
+                    tc::mma_commit(&ctl->empty[s]);
                 }
-                if (MODE == LOCAL && ok) {
+                if (ok) {
                     const int nsp = (I.T[0] + SPAN - 1) / SPAN;
                     for (int sg = nsp - 1; sg >= 0 && ok; --sg) {
                         const int len = min(SPAN, I.T[0] - sg * SPAN);
                         if (!(ok = tc::mbar_wait(&ctl->pbready, pr.next(B_PB), abort))) break;
                         // pipelined order, matching the compute warps' signals
                         for (int u = len + 1; u >= 0 && ok; --u) {
-                            if (u <= len - 1) ok = issue_dx(s_sx + u * 4096u, s_sb + u * 4096u, true, true);
+                            if (u <= len - 1) ok = issue_dx(s_sx + u * 4096u, s_sb + u * 4096u);
                             if (ok && u - 1 >= 0 && u - 1 <= len - 1) ok = issue_dc();
                             if (ok && u - 2 >= 0) ok = issue_prefix(u - 2);
                         }
@@ -470,8 +428,6 @@ __global__ void __launch_bounds__(NTHR, 1)
         const float* m1s = reinterpret_cast<const float*>(sm + OFF_M1);
         float* coefs = reinterpret_cast<float*>(sm + OFF_COEF);           // [8][2][128]
         float* Lt = reinterpret_cast<float*>(sm + OFF_LT);                // [2][8][8]
-        float* om = reinterpret_cast<float*>(sm + OFF_OM);                // [2][64]
-        float* misc = reinterpret_cast<float*>(sm + OFF_MISC);            // [2] dots, [2] bases
         float* myanchors = B.anchors + (int64_t)blockIdx.x * NANCHOR * 128 * 128;
         Par pr;
         uint32_t q = 0, nw = 0;
@@ -497,7 +453,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 acum[c2 * 64 + 2 * lane + 1] = s;
                 acum[c2 * 64 + 2 * lane] = s - v1;
             }
-            if (MODE == LOCAL && (ctl->loaded_b != I.bb || ctl->loaded_h != I.hh)) {
+            if (ctl->loaded_b != I.bb || ctl->loaded_h != I.hh) {
                 const float* D = B.dm2 + ((int64_t)I.bb * P.h + I.hh) * R * R;
                 unsigned char* ds = sm + OFF_DS;
                 for (int i = ctid; i < 128 * 128 / 2; i += NCW * 32) {
@@ -515,14 +471,14 @@ __global__ void __launch_bounds__(NTHR, 1)
                 tc::fence_proxy_async_smem();
             }
             named_barrier_sync(1, NCW * 32);
-            if (MODE == LOCAL && ctid == 0) {
+            if (ctid == 0) {
                 ctl->loaded_b = I.bb;
                 ctl->loaded_h = I.hh;
             }
             const float* ac = acum + ch * 64;
             auto e_of = [&](int t) -> float { return __expf(ida[(ch * 64 + t) * 4 + (I.hh & 3)]); };
 
-            if (MODE == LOCAL) {
+            {
                 // ================================ phase A: forward sweep, anchors
                 {
                     float S[4][16];
@@ -628,11 +584,11 @@ __global__ void __launch_bounds__(NTHR, 1)
                         Lt[ctid] = (o < len && jj <= o) ? __expf(ac2[s0 + o] - ac2[s0 + jj]) : 0.f;
                     }
                     if (ROTK == ROT_PAIRWISE || ROTK == ROT_HALF) {
-                        for (int i = ctid; i < len * 2 * P.na; i += NCW * 32) {
-                            const int o = i / (2 * P.na), rem = i - o * 2 * P.na;
-                            const int c2 = rem / P.na, a = rem - c2 * P.na;
-                            float sv, cv;
-                            sincosf(reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + c2 * 512)[a], &sv, &cv);
+                        for (int i = ctid; i < len * 2 * 64; i += NCW * 32) {
+                            const int o = i >> 7, c2 = (i >> 6) & 1, a = i & 63;
+                            float sv = 0.f, cv = 1.f;
+                            if (a < P.na)
+                                sincosf(reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + c2 * 512)[a], &sv, &cv);
                             coefs[(o * 2 + c2) * 128 + a] = cv;
                             coefs[(o * 2 + c2) * 128 + 64 + a] = sv;
                         }
@@ -678,7 +634,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         const float* cf = coefs + (o * 2 + ch) * 128;
                         const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + ch * 512);
                         if (pr.once(U_C)) ok &= tc::mbar_wait(&ctl->cfree, pr.next(B_C), abort);
-                        float dot = 0.f;
+                        float dotv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                         for (int pass = 0; pass < 2; ++pass) {
                             const int sa = slot_a<LAYB>(pass), sb = slot_b<LAYB>(pass);
@@ -692,8 +648,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                             for (int e = 0; e < 16; ++e) {
                                 ha[e] = fmaf(dsig, aa[e], ha[e]);
                                 hb[e] = fmaf(dsig, ab[e], hb[e]);
-                                dot = fmaf(gr[sa][e], ha[e], dot);
-                                dot = fmaf(gr[sb][e], hb[e], dot);
+                                dotv[e & 1] = fmaf(gr[sa][e], ha[e], dotv[e & 1]);
+                                dotv[2 + (e & 1)] = fmaf(gr[sb][e], hb[e], dotv[2 + (e & 1)]);
                             }
                             rot_pass<ROTK, LAYB, false>(P, pass, 16 * G[sa], 16 * G[sb], ha, hb, cf, qt);
                             write_tile16(sm + OFF_C, m, G[sa], ha, !live);
@@ -707,7 +663,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                             tc::mbar_arrive(&ctl->cfull);
                         }
                         // d_da_{t+1} = e_{t+1} <g_{t+1}, h_t>  (g holds g_{t+1} here)
-                        dot = warp_sum(dot);
+                        const float dot = warp_sum((dotv[0] + dotv[1]) + (dotv[2] + dotv[3]));
                         if (lane == 0 && t + 1 < I.T[0] && chunk_ok && n < I.proc)
                             atomicAdd(B.dda + off_da(P, I.bb, n * FL + t + 1, I.hh), e_of(t + 1) * dot);
                     };
@@ -897,114 +853,6 @@ __global__ void __launch_bounds__(NTHR, 1)
                 for (uint32_t i = ctid; i < 32768 / 16; i += NCW * 32)
                     reinterpret_cast<uint4*>(sm + OFF_RING)[i] = make_uint4(0, 0, 0, 0);
                 tc::fence_proxy_async_smem();
-            } else {
-                // ================================ correction by the carry cotangent dH(n+1)
-                const bool corr = chunk_ok && n + 1 < I.proc;
-                {
-                    float dh[4][16];
-                    const float* src = B.E + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
-                    const float* hin = A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
-                    float dot = 0.f;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g)
-#pragma unroll
-                        for (int e = 0; e < 16; e += 4) {
-                            const int col = 16 * G[g] + e;
-                            float4 v = make_float4(0.f, 0.f, 0.f, 0.f), hv = v;
-                            if (corr && col < R) {
-                                v = *reinterpret_cast<const float4*>(src + col);
-                                hv = *reinterpret_cast<const float4*>(hin + col);
-                            }
-                            dh[g][e] = v.x; dh[g][e + 1] = v.y; dh[g][e + 2] = v.z; dh[g][e + 3] = v.w;
-                            dot += v.x * hv.x + v.y * hv.y + v.z * hv.z + v.w * hv.w;
-                        }
-                    dot = warp_sum(dot);
-                    if (lane == 0) atomicAdd(&misc[ch], dot);
-                    if (pr.once(U_G)) ok &= tc::mbar_wait(&ctl->gfree, pr.next(B_G), abort);
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) write_tile16(sm + OFF_G, m, G[g], dh[g], false);
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&ctl->gfull);
-                }
-                named_barrier_sync(1, NCW * 32);
-                if (ctid < 2) {
-                    misc[2 + ctid] = __expf(acum[ctid * 64 + 63]) * misc[ctid];
-                    misc[ctid] = 0.f;
-                }
-                const float alast = ac[63];
-                const bool corr_b = half_ok && (2 * I.k + half) + 1 < I.proc;
-                const float alast_b = acum[half * 64 + 63];
-                for (int t = 0; t < I.T[0]; ++t, ++q) {
-                    const uint32_t s = q % NS;
-                    // issue this token's read-modify-write loads before waiting for the products
-                    const int tokx = n * FL + t, tokb = (2 * I.k + half) * FL + t;
-                    float ox[4] = {0.f, 0.f, 0.f, 0.f}, ob[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (half == 0 && corr) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if (c < C) ox[c] = __bfloat162float(B.dx[off_x(P, I.bb, tokx, c, I.hh) + pp]);
-                    }
-                    if (m < R && corr_b) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if (c < C) ob[c] = __bfloat162float(B.db[off_b(P, I.bb, tokb, c, I.hh) + m]);
-                    }
-                    ok &= tc::mbar_wait(&ctl->full[s], pr.next(B_FULL + s), abort);
-                    ok &= tc::mbar_wait(&ctl->dxfull, pr.next(B_DX), abort);
-                    tc::tc_fence_after();
-                    float v[8], u[8];
-                    tc::tmem_ld8(lane_addr + TM_DX + 8 * ch, v);
-                    tc::tmem_ld8(lane_addr + TM_DB + 8 * half, u);
-                    tc::tmem_wait_ld();
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&ctl->dxfree);
-                    // omega_t = sum_c <xhat_tc, U_tc> over this chunk's rows (U = dH bhat^T)
-                    float w = 0.f;
-                    if (half == 0) {
-                        const unsigned char* xt = sm + OFF_RING + s * 8192;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if (c < C) {
-                                const uint32_t off = tc::sw128_offset(16, 8 * ch + c, 64 * ch + pp);
-                                const float xv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xt + off));
-                                w = fmaf(xv, v[c], w);
-                            }
-                    }
-                    w = warp_sum(w);
-                    __syncwarp();
-                    if (lane == 0) {
-                        tc::mbar_arrive(&ctl->empty[s]);
-                        if (half == 0) atomicAdd(&om[ch * 64 + t], w);
-                    }
-                    if (half == 0 && corr) {
-                        const float sc = __expf(alast - ac[t]);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if (c < C) B.dx[off_x(P, I.bb, tokx, c, I.hh) + pp] = __float2bfloat16_rn(ox[c] + sc * v[c]);
-                    }
-                    if (m < R && corr_b) {
-                        const float sc = __expf(alast_b - acum[half * 64 + t]);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if (c < C) B.db[off_b(P, I.bb, tokb, c, I.hh) + m] = __float2bfloat16_rn(ob[c] + sc * u[c]);
-                    }
-                }
-                named_barrier_sync(1, NCW * 32);
-                // d_da_s += D_n <dH, h_-> + sum_{j<s} sc_j omega_j
-                if (ctid < 128) {
-                    const int c2 = ctid >> 6, s = ctid & 63;
-                    const int n2 = 2 * I.k + c2;
-                    if ((c2 ? I.exists[1] : I.exists[0]) && n2 + 1 < I.proc) {
-                        const float* ac2 = acum + c2 * 64;
-                        float pre = 0.f;
-                        for (int j = 0; j < s; ++j) pre += __expf(ac2[63] - ac2[j]) * om[c2 * 64 + j];
-                        B.dda[off_da(P, I.bb, n2 * FL + s, I.hh)] += misc[2 + c2] + pre;
-                    }
-                }
-                named_barrier_sync(1, NCW * 32);
-                if (ctid < 128) om[ctid] = 0.f;
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ctl->itemdone);
@@ -1027,9 +875,8 @@ namespace fastk {
 
 size_t bwd_anchor_bytes() { return (size_t)kMaxBwdGrid * fastbwd::NANCHOR * 128 * 128 * sizeof(float); }
 
-cudaError_t launch_tc_bwd(int mode, const FastArgs& fa, float* E, float* anchors, const float* dm2, const float* dm1,
-                          void* dx, void* db, float* dda, float* drot, const TensorMaps& maps, int grid,
-                          cudaStream_t st) {
+cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, const float* dm2, const float* dm1, void* dx,
+                          void* db, float* dda, float* drot, const TensorMaps& maps, int grid, cudaStream_t st) {
     using namespace fastbwd;
     BwdArgs a;
     a.F = fa;
@@ -1041,23 +888,18 @@ cudaError_t launch_tc_bwd(int mode, const FastArgs& fa, float* E, float* anchors
     a.db = static_cast<__nv_bfloat16*>(db);
     a.dda = dda;
     a.drot = drot;
-    decltype(&tc_bwd_kernel<LOCAL, ROT_NONE, 0>) kern;
-    if (mode == CORR) {
-        kern = tc_bwd_kernel<CORR, ROT_NONE, 0>;
-    } else {
-        switch (fa.P.rot) {
-            case ROT_PAIRWISE: kern = tc_bwd_kernel<LOCAL, ROT_PAIRWISE, 0>; break;
-            case ROT_HALF: kern = fa.layoutB ? tc_bwd_kernel<LOCAL, ROT_HALF, 1> : tc_bwd_kernel<LOCAL, ROT_HALF, 0>; break;
-            case ROT_QUAT: kern = tc_bwd_kernel<LOCAL, ROT_QUAT, 0>; break;
-            default: kern = tc_bwd_kernel<LOCAL, ROT_NONE, 0>; break;
-        }
+    decltype(&tc_bwd_kernel<ROT_NONE, 0>) kern;
+    switch (fa.P.rot) {
+        case ROT_PAIRWISE: kern = tc_bwd_kernel<ROT_PAIRWISE, 0>; break;
+        case ROT_HALF: kern = fa.layoutB ? tc_bwd_kernel<ROT_HALF, 1> : tc_bwd_kernel<ROT_HALF, 0>; break;
+        case ROT_QUAT: kern = tc_bwd_kernel<ROT_QUAT, 0>; break;
+        default: kern = tc_bwd_kernel<ROT_NONE, 0>; break;
     }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int kid = mode == LOCAL ? KID_FAST_BWD : KID_FAST_CORRECT;
-    mm_prof_mark(kid, 1, st);
+    mm_prof_mark(KID_FAST_BWD, 1, st);
     kern<<<grid, NTHR, SMEM_BYTES, st>>>(a, maps.x, maps.b, maps.rot, maps.da64);
-    mm_prof_mark(kid, 0, st);
+    mm_prof_mark(KID_FAST_BWD, 0, st);
     return cudaGetLastError();
 }
 

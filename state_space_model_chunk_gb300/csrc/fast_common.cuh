@@ -11,7 +11,6 @@ namespace fastk {
 
 constexpr int FL = 64;   // internal chunk length of the tensor-core path
 constexpr int NCW = 8;   // compute warps (two threads per 128-column row)
-enum { FWD_MOMENTS = 0, CHUNK_END = 1 };
 
 struct FastArgs {
     MMParams P;     // internal chunking: l = 64, nc = s / 64
@@ -151,85 +150,52 @@ __device__ __forceinline__ void hamilton(float qw, float qx, float qy, float qz,
     oz = qw * vz + qx * vy - qy * vx + qz * vw;
 }
 
-// out = R_t v on this thread's columns: the de-rotation R(-theta) / Q (x) . (TR = false) or its
-// transpose R(+theta) / conj(Q) (x) . (TR = true).  coef holds cos at [0,128) and sin at
-// [128,256) of the chunk's angles; quat the chunk's raw [J][4] quaternions.
-template <bool TR>
-__device__ __forceinline__ void rotate_regs(const MMParams& P, int layoutB, const int (&G)[4],
-                                            const float (&v)[4][16], const float* coef, const float* quat,
-                                            float (&out)[4][16]) {
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// 16 columns (group gcol of 16) of row m of a bf16 [128 x 128] swizzled tile, as floats / from floats.
+__device__ __forceinline__ void read_tile16(const unsigned char* tile, int m, int gcol, float (&v)[16]) {
+    const uint32_t hv = gcol >> 2, j0 = 2 * (gcol & 3);
 #pragma unroll
-    for (int g = 0; g < 4; ++g)
-#pragma unroll
-        for (int e = 0; e < 16; ++e) out[g][e] = v[g][e];
-    if (P.rot == ROT_PAIRWISE) {
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-                const int k = 16 * G[g] + e;
-                if (k < 2 * P.na) {
-                    const float cs = coef[k >> 1], sn = TR ? -coef[128 + (k >> 1)] : coef[128 + (k >> 1)];
-                    const float x = v[g][e], y = v[g][e + 1];
-                    out[g][e] = cs * x + sn * y;
-                    out[g][e + 1] = -sn * x + cs * y;
-                }
-            }
-    } else if (P.rot == ROT_HALF) {
-        if (!layoutB) {
-#pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-                const int ga = pr, gb = pr + 2;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int k = 16 * G[ga] + e;
-                    if (k < P.na) {
-                        const float cs = coef[k], sn = TR ? -coef[128 + k] : coef[128 + k];
-                        const float x = v[ga][e], y = v[gb][e];
-                        out[ga][e] = cs * x + sn * y;
-                        out[gb][e] = -sn * x + cs * y;
-                    }
-                }
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int k = 16 * G[0] + e;
-                if (k < P.na) {
-                    const float cs = coef[k], sn = TR ? -coef[128 + k] : coef[128 + k];
-                    const float x = v[0][e], y = v[1][e];
-                    out[0][e] = cs * x + sn * y;
-                    out[1][e] = -sn * x + cs * y;
-                }
-            }
-        }
-    } else if (P.rot == ROT_QUAT) {
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-#pragma unroll
-            for (int e = 0; e < 16; e += 4) {
-                const int blk = (16 * G[g] + e) >> 2;
-                if (blk < P.J) {
-                    const float* Q = quat + 4 * blk;
-                    const float qx = TR ? -Q[1] : Q[1], qy = TR ? -Q[2] : Q[2], qz = TR ? -Q[3] : Q[3];
-                    hamilton(Q[0], qx, qy, qz, v[g][e], v[g][e + 1], v[g][e + 2], v[g][e + 3], out[g][e],
-                             out[g][e + 1], out[g][e + 2], out[g][e + 3]);
-                }
-            }
+    for (int hj = 0; hj < 2; ++hj) {
+        const uint4 w = *reinterpret_cast<const uint4*>(tile + tc::sw128_chunk(128, hv, m, j0 + hj));
+        v[8 * hj + 0] = bf16lo(w.x); v[8 * hj + 1] = bf16hi(w.x);
+        v[8 * hj + 2] = bf16lo(w.y); v[8 * hj + 3] = bf16hi(w.y);
+        v[8 * hj + 4] = bf16lo(w.z); v[8 * hj + 5] = bf16hi(w.z);
+        v[8 * hj + 6] = bf16lo(w.w); v[8 * hj + 7] = bf16hi(w.w);
     }
 }
+__device__ __forceinline__ void write_tile16(unsigned char* tile, int m, int gcol, const float (&v)[16], bool zero) {
+    const uint32_t hv = gcol >> 2, j0 = 2 * (gcol & 3);
+#pragma unroll
+    for (int hj = 0; hj < 2; ++hj) {
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (!zero) {
+            w.x = tc::pack_bf16x2(v[8 * hj + 0], v[8 * hj + 1]);
+            w.y = tc::pack_bf16x2(v[8 * hj + 2], v[8 * hj + 3]);
+            w.z = tc::pack_bf16x2(v[8 * hj + 4], v[8 * hj + 5]);
+            w.w = tc::pack_bf16x2(v[8 * hj + 6], v[8 * hj + 7]);
+        }
+        *reinterpret_cast<uint4*>(tile + tc::sw128_chunk(128, hv, m, j0 + hj)) = w;
+    }
+}
+
+// Slots of a 32-column pass: rotation partners stay inside (half-split, r = 64: slots 0/1).
+template <int LAYB>
+__device__ __forceinline__ int slot_a(int pass) { return LAYB ? 2 * pass : pass; }
+template <int LAYB>
+__device__ __forceinline__ int slot_b(int pass) { return LAYB ? 2 * pass + 1 : pass + 2; }
 
 // host helpers
 cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, const float* rot, const float* da,
                         TensorMaps* maps);
 int sm_count();
-cudaError_t launch_tc_fwd(int mode, const FastArgs& args, const TensorMaps& maps, int grid, cudaStream_t st);
+cudaError_t launch_tc_fwd(const FastArgs& args, const TensorMaps& maps, int grid, cudaStream_t st);
 cudaError_t launch_tc_end(const FastArgs& fa, const TensorMaps& maps, cudaStream_t st);
 cudaError_t launch_tc_corr(const FastArgs& fa, const float* da, const float* E, void* dx, void* db, float* dda,
                            const TensorMaps& maps, cudaStream_t st);
 size_t bwd_anchor_bytes();
-cudaError_t launch_tc_bwd(int mode, const FastArgs& fa, float* E, float* anchors, const float* dm2, const float* dm1,
-                          void* dx, void* db, float* dda, float* drot, const TensorMaps& maps, int grid,
-                          cudaStream_t st);
+cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, const float* dm2, const float* dm1, void* dx,
+                          void* db, float* dda, float* drot, const TensorMaps& maps, int grid, cudaStream_t st);
 
 }  // namespace fastk

@@ -11,14 +11,15 @@
 //                     MMA (M = 128 rows, N = 128, K = 16 = (chunk, channel) rows), into one of
 //                     two TMEM accumulators; then the moment MMAs m2 += c^T [c | 1] over the
 //                     128 rows (8 x K=16 steps, N = 144: column 128 of the ones block gives m1).
-//   warps 0-7       : two threads per row (64 columns each).  h = e^{da} h + W in fp32
-//                     registers (the chunk recurrence h~[t] = d_t h_- + sum_j L[t,j] W_j
-//                     unrolled), de-rotation in registers, masking, bf16 c rows into the
-//                     swizzled smem tile that both moment operands read.
+//   warps 0-7       : two threads per row (64 columns each, two 32-column passes whose rotation
+//                     partners stay inside the pass).  h = e^{da} h + W in fp32 registers (the
+//                     chunk recurrence h~[t] = d_t h_- + sum_j L[t,j] W_j unrolled), de-rotation
+//                     in registers, masking, bf16 c rows into the swizzled smem tile that both
+//                     moment operands read.
 //
-// The same kernel in "chunk-end" mode starts every chunk from zero and writes the chunk-end
-// state Delta_n = sum_j exp(a_last - a_j) W_j and D_n = exp(a_last) ("backward.rs",
-// boundary_carries), which the carry scan turns into the chunk-entry carries.
+// The cos / sin of a token's angles are evaluated per warp (one angle per lane, the ones this
+// warp's columns need) into a small per-warp table, so that no block-wide barrier is needed per
+// token.  The chunk-entry carries come from the chunk-end states (fast_end.cu) and the carry scan.
 //
 // Every wait is bounded; a wait that gives up sets the workspace error word and the CTA winds
 // down (compute warps keep stepping through their loops so named barriers stay matched).
@@ -45,8 +46,8 @@ constexpr uint32_t OFF_X = 2 * C_BYTES;                // NS x 4 KB  (16 K-rows 
 constexpr uint32_t OFF_B = OFF_X + NS * 4096;          // NS x 4 KB  (16 K-rows x 128 r)
 constexpr uint32_t OFF_ROT = OFF_B + NS * 4096;        // NS x 2 chunks x 512 B raw rotation
 constexpr uint32_t OFF_DA = OFF_ROT + NS * 1024;       // NS x 2 chunks x 128 B slots (4 heads of da)
-constexpr uint32_t OFF_COEF = OFF_DA + NS * 256;       // 2 x 2 chunks x 256 floats (cos | sin)
-constexpr uint32_t OFF_CTL = OFF_COEF + 2 * 2 * 256 * 4;
+constexpr uint32_t OFF_TBL = OFF_DA + NS * 256;        // 8 warps x (32 cos | 32 sin) fp32
+constexpr uint32_t OFF_CTL = OFF_TBL + NCW * 64 * 4;
 constexpr uint32_t SMEM_BYTES = OFF_CTL + 256 + 1024;
 
 struct Ctl {
@@ -69,7 +70,7 @@ __device__ __forceinline__ void fail(Ctl* ctl, int* err, int code) {
     atomicExch(err, code);
 }
 
-template <int MODE>
+template <int ROTK, int LAYB>
 __global__ void __launch_bounds__(NTHR, 1)
     tc_fwd_kernel(const __grid_constant__ FastArgs A, const __grid_constant__ CUtensorMap tmx,
                   const __grid_constant__ CUtensorMap tmb, const __grid_constant__ CUtensorMap tmr,
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     // ---- one-time set-up: zero the staged operand tiles, the ones block, barriers, TMEM
     for (uint32_t i = tid; i < (OFF_ROT - OFF_X) / 16; i += NTHR)
         reinterpret_cast<uint4*>(sm + OFF_X)[i] = make_uint4(0, 0, 0, 0);
-    if (MODE == FWD_MOMENTS) {
+    {
         // ones block of both c tiles: column 128 (first column of the block) = 1.0, rest 0
         for (uint32_t i = tid; i < 2 * 128; i += NTHR) {
             const uint32_t buf = i >> 7, row = i & 127;
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(NTHR, 1)
             for (uint32_t q = 0; ok && q < ntok; ++q) {
                 const TokenInfo ti = walk.next();
                 if (q + 1 < ntok && !issue_w(q + 1)) { ok = false; break; }
-                if (MODE == FWD_MOMENTS) {
+                {
                     const uint32_t cb = q & 1, uc = q >> 1;
                     if (!tc::mbar_wait(&ctl->cfull[cb], uc & 1, abort)) { ok = false; break; }
                     if (ti.seg_first && seg >= 1 && !tc::mbar_wait(&ctl->segfree, (seg - 1) & 1, abort)) {
@@ -223,17 +224,33 @@ __global__ void __launch_bounds__(NTHR, 1)
         const int m = ((warp & 3) << 5) + lane;  // TMEM lane = row (chunk, p)
         const int ch = m >> 6, pp = m & 63;
         int G[4];
-        col_groups(A.layoutB, half, G);
+        col_groups(LAYB, half, G);
         const uint32_t lane_addr = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+        float* tbl = reinterpret_cast<float*>(sm + OFF_TBL) + warp * 64;  // this warp's cos | sin
+        // the angle this lane evaluates for the warp's table (table slot = lane)
+        int my_ang = 1 << 30;
+        if (ROTK == ROT_PAIRWISE) {  // slot g pair i  <->  table 8 g + i
+            const int g = lane >> 3;
+            my_ang = 8 * (g == 0 ? G[0] : g == 1 ? G[1] : g == 2 ? G[2] : G[3]) + (lane & 7);
+        } else if (ROTK == ROT_HALF) {  // pass p element e  <->  table 16 p + e
+            if (!LAYB) my_ang = 16 * (lane < 16 ? G[0] : G[1]) + (lane & 15);
+            else if (lane < 16) my_ang = 16 * G[0] + lane;
+        }
         float S[4][16];
         uint32_t q = 0, seg = 0;
         bool ok = true;
+        auto check = [&](bool r) {  // the first failed wait stops the whole CTA at once
+            if (!r && ok) {
+                ok = false;
+                fail(ctl, A.err, 13);
+            }
+        };
         for (int it = it0; it < it1; ++it) {
             const Item I = decode_item(A, it);
-            const int Tch = I.T[ch];
+            const int Tch = ch ? I.T[1] : I.T[0];
             const int n = 2 * I.k + ch;
-            // chunk-entry carry (forward) or zero (chunk-end mode)
-            if (MODE == FWD_MOMENTS && Tch > 0) {
+            // chunk-entry carry
+            if (Tch > 0) {
                 const float* src = A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
@@ -250,93 +267,110 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) S[g][e] = 0.f;
             }
-            float dsum = 0.f;
             for (int t = 0; t < I.T[0]; ++t, ++q) {
                 const uint32_t s = q % NS, u = q / NS;
-                ok &= tc::mbar_wait(&ctl->full[s], u & 1, abort);
-                const float da = reinterpret_cast<const float*>(sm + OFF_DA + s * 256 + ch * 128)[I.hh & 3];
-                const float et = __expf(da);
-                dsum += da;
-                const float* rawrot = reinterpret_cast<const float*>(sm + OFF_ROT + s * 1024);
-                float* coef = reinterpret_cast<float*>(sm + OFF_COEF + (q & 1) * 2048);
-                if (MODE == FWD_MOMENTS && (P.rot == ROT_PAIRWISE || P.rot == ROT_HALF)) {
-                    // cos / sin of both chunks' angles, shared by the 256 compute threads
-                    for (int i = tid; i < 2 * P.na; i += NCW * 32) {
-                        const int c2 = i / P.na, a = i - c2 * P.na;
-                        float sv, cv;
-                        sincosf(rawrot[c2 * 128 + a], &sv, &cv);
-                        coef[c2 * 256 + a] = cv;
-                        coef[c2 * 256 + 128 + a] = sv;
-                    }
-                    named_barrier_sync(1, NCW * 32);
-                }
-                // W_t for this row from TMEM
-                const uint32_t wb = q & 1, uw = q >> 1;
-                ok &= tc::mbar_wait(&ctl->wfull[wb], uw & 1, abort);
-                tc::tc_fence_after();
-                float W[4][16];
-#pragma unroll
-                for (int g = 0; g < 4; ++g) tc::tmem_ld16(lane_addr + TM_W + wb * 128 + 16 * G[g], W[g]);
-                tc::tmem_wait_ld();
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&ctl->wfree[wb]);
+                check(tc::mbar_wait(&ctl->full[s], u & 1, abort));
                 const bool live = t < Tch;
-                if (live) {
-#pragma unroll
-                    for (int g = 0; g < 4; ++g)
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) S[g][e] = fmaf(et, S[g][e], W[g][e]);
-                }
-                if (MODE == FWD_MOMENTS) {
-                    float c[4][16];
-                    rotate_regs<false>(P, A.layoutB, G, S, coef + ch * 256, rawrot + ch * 128, c);
+                const float et = live ? __expf(reinterpret_cast<const float*>(sm + OFF_DA + s * 256 + ch * 128)[I.hh & 3])
+                                      : 1.f;
+                const float wt = live ? 1.f : 0.f;
+                const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + s * 1024 + ch * 512);
+                if (ROTK == ROT_PAIRWISE || ROTK == ROT_HALF) {
+                    float sv = 0.f, cv = 1.f;
+                    if (my_ang < P.na) sincosf(qt[my_ang], &sv, &cv);
+                    __syncwarp();  // the previous token's table has been read
+                    tbl[lane] = cv;
+                    tbl[32 + lane] = sv;
                     __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&ctl->empty[s]);
-                    const uint32_t cb = q & 1, uc = q >> 1;
-                    if (uc >= 1) ok &= tc::mbar_wait(&ctl->cfree[cb], (uc - 1) & 1, abort);
-                    unsigned char* ct = sm + OFF_C + cb * C_BYTES;
+                }
+                const uint32_t wb = q & 1, uw = q >> 1, cb = q & 1, uc = q >> 1;
+                check(tc::mbar_wait(&ctl->wfull[wb], uw & 1, abort));
+                if (uc >= 1) check(tc::mbar_wait(&ctl->cfree[cb], (uc - 1) & 1, abort));
+                tc::tc_fence_after();
+                unsigned char* ct = sm + OFF_C + cb * C_BYTES;
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const uint32_t hv = G[g] >> 2, j0 = 2 * (G[g] & 3);
+                for (int pass = 0; pass < 2; ++pass) {
+                    const int sa = slot_a<LAYB>(pass), sb = slot_b<LAYB>(pass);
+                    float a[16], b[16];
+                    tc::tmem_ld16(lane_addr + TM_W + wb * 128 + 16 * G[sa], a);
+                    tc::tmem_ld16(lane_addr + TM_W + wb * 128 + 16 * G[sb], b);
+                    tc::tmem_wait_ld();
+                    if (pass == 1) {
+                        tc::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&ctl->wfree[wb]);
+                    }
 #pragma unroll
-                        for (int hj = 0; hj < 2; ++hj) {
-                            uint4 v = make_uint4(0, 0, 0, 0);
-                            if (live) {
-                                v.x = tc::pack_bf16x2(c[g][8 * hj + 0], c[g][8 * hj + 1]);
-                                v.y = tc::pack_bf16x2(c[g][8 * hj + 2], c[g][8 * hj + 3]);
-                                v.z = tc::pack_bf16x2(c[g][8 * hj + 4], c[g][8 * hj + 5]);
-                                v.w = tc::pack_bf16x2(c[g][8 * hj + 6], c[g][8 * hj + 7]);
+                    for (int e = 0; e < 16; ++e) {
+                        S[sa][e] = fmaf(et, S[sa][e], wt * a[e]);
+                        S[sb][e] = fmaf(et, S[sb][e], wt * b[e]);
+                        a[e] = S[sa][e];
+                        b[e] = S[sb][e];
+                    }
+                    // de-rotation c = R_t h of the pass's two slots
+                    if (ROTK == ROT_PAIRWISE) {
+#pragma unroll
+                        for (int sl = 0; sl < 2; ++sl) {
+                            float(&v)[16] = sl ? b : a;
+                            const int ti = 8 * (sl ? sb : sa);
+                            float cs[8], sn[8];
+                            *reinterpret_cast<float4*>(&cs[0]) = *reinterpret_cast<const float4*>(tbl + ti);
+                            *reinterpret_cast<float4*>(&cs[4]) = *reinterpret_cast<const float4*>(tbl + ti + 4);
+                            *reinterpret_cast<float4*>(&sn[0]) = *reinterpret_cast<const float4*>(tbl + 32 + ti);
+                            *reinterpret_cast<float4*>(&sn[4]) = *reinterpret_cast<const float4*>(tbl + 36 + ti);
+#pragma unroll
+                            for (int e = 0; e < 16; e += 2) {
+                                const float x = v[e], y = v[e + 1];
+                                v[e] = fmaf(cs[e / 2], x, sn[e / 2] * y);
+                                v[e + 1] = fmaf(cs[e / 2], y, -sn[e / 2] * x);
                             }
-                            *reinterpret_cast<uint4*>(ct + tc::sw128_chunk(128, hv, m, j0 + hj)) = v;
+                        }
+                    } else if (ROTK == ROT_HALF) {
+                        if (!(LAYB && pass == 1)) {
+                            const int ti = 16 * pass;
+#pragma unroll
+                            for (int e4 = 0; e4 < 16; e4 += 4) {
+                                const float4 c4 = *reinterpret_cast<const float4*>(tbl + ti + e4);
+                                const float4 s4 = *reinterpret_cast<const float4*>(tbl + 32 + ti + e4);
+                                const float cs[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const int e = e4 + j;
+                                    const float x = a[e], y = b[e];
+                                    a[e] = fmaf(cs[j], x, sn[j] * y);
+                                    b[e] = fmaf(cs[j], y, -sn[j] * x);
+                                }
+                            }
+                        }
+                    } else if (ROTK == ROT_QUAT) {
+#pragma unroll
+                        for (int sl = 0; sl < 2; ++sl) {
+                            float(&v)[16] = sl ? b : a;
+                            const int k0 = 16 * G[sl ? sb : sa];
+#pragma unroll
+                            for (int e = 0; e < 16; e += 4) {
+                                const int blk = (k0 + e) >> 2;
+                                if (blk < P.J) {
+                                    const float* Q = qt + 4 * blk;
+                                    hamilton(Q[0], Q[1], Q[2], Q[3], v[e], v[e + 1], v[e + 2], v[e + 3], v[e], v[e + 1],
+                                             v[e + 2], v[e + 3]);
+                                }
+                            }
                         }
                     }
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&ctl->cfull[cb]);
-                } else {
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&ctl->empty[s]);
+                    write_tile16(ct, m, G[sa], a, !live);
+                    write_tile16(ct, m, G[sb], b, !live);
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(&ctl->cfull[cb]);
+                    tc::mbar_arrive(&ctl->empty[s]);
                 }
             }
-            if (MODE == CHUNK_END) {
-                if (Tch > 0 && half == 0 && pp == 0)
-                    A.Dn[((int64_t)I.bb * P.h + I.hh) * P.nc + n] = __expf(dsum);
-                if (n + 1 < I.proc) {  // the last processed chunk's end state is never consumed
-                    float* dst = A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g)
-#pragma unroll
-                        for (int e = 0; e < 16; e += 4) {
-                            const int col = 16 * G[g] + e;
-                            if (col < R)
-                                *reinterpret_cast<float4*>(dst + col) =
-                                    make_float4(S[g][e], S[g][e + 1], S[g][e + 2], S[g][e + 3]);
-                        }
-                }
-            } else if (I.seg_last) {
+            if (I.seg_last) {
                 // flush the (b,h) moment accumulator: lanes are rows r1 of m2
-                ok &= tc::mbar_wait(&ctl->segdone, seg & 1, abort);
+                check(tc::mbar_wait(&ctl->segdone, seg & 1, abort));
                 tc::tc_fence_after();
                 float* M2 = A.m2 + ((int64_t)I.bb * P.h + I.hh) * P.r * P.r;
                 float* M1 = A.m1 + ((int64_t)I.bb * P.h + I.hh) * P.r;
@@ -363,7 +397,6 @@ __global__ void __launch_bounds__(NTHR, 1)
                 ++seg;
             }
         }
-        if (!ok) fail(ctl, A.err, 13);
     }
     // ---- teardown
     tc::tc_fence_before();
@@ -379,15 +412,20 @@ __global__ void __launch_bounds__(NTHR, 1)
 // ----------------------------------------------------------------------------- host side
 namespace fastk {
 
-cudaError_t launch_tc_fwd(int mode, const FastArgs& args, const TensorMaps& maps, int grid, cudaStream_t st) {
+cudaError_t launch_tc_fwd(const FastArgs& args, const TensorMaps& maps, int grid, cudaStream_t st) {
     using namespace fastfwd;
-    auto kern = mode == FWD_MOMENTS ? tc_fwd_kernel<FWD_MOMENTS> : tc_fwd_kernel<CHUNK_END>;
+    decltype(&tc_fwd_kernel<ROT_NONE, 0>) kern;
+    switch (args.P.rot) {
+        case ROT_PAIRWISE: kern = tc_fwd_kernel<ROT_PAIRWISE, 0>; break;
+        case ROT_HALF: kern = args.layoutB ? tc_fwd_kernel<ROT_HALF, 1> : tc_fwd_kernel<ROT_HALF, 0>; break;
+        case ROT_QUAT: kern = tc_fwd_kernel<ROT_QUAT, 0>; break;
+        default: kern = tc_fwd_kernel<ROT_NONE, 0>; break;
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int kid = mode == FWD_MOMENTS ? KID_FAST_FWD : KID_FAST_END;
-    mm_prof_mark(kid, 1, st);
+    mm_prof_mark(KID_FAST_FWD, 1, st);
     kern<<<grid, NTHR, SMEM_BYTES, st>>>(args, maps.x, maps.b, maps.rot, maps.da);
-    mm_prof_mark(kid, 0, st);
+    mm_prof_mark(KID_FAST_FWD, 0, st);
     return cudaGetLastError();
 }
 
