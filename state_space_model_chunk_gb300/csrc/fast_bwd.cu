@@ -37,7 +37,6 @@ using namespace fastk;
 
 constexpr int NTHR = 320;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
-constexpr int NS = 4;          // forward-sweep / correction staging ring (in the prefix tiles' space)
 constexpr int SPAN = 8;        // tokens per anchor span
 constexpr int NANCHOR = 7;     // anchors per 64-token chunk kept in the workspace (anchor 0 = carry)
 
@@ -47,9 +46,7 @@ constexpr uint32_t OFF_G = 32768;                // g tile     (same layout)
 constexpr uint32_t OFF_DS = 65536;               // D + D^T    [128 r2][128 r1] bf16
 constexpr uint32_t OFF_SX = 98304;               // span xhat tiles, 8 x [16 rows (8ch+c)][128 (ch,p)]
 constexpr uint32_t OFF_SB = 131072;              // span bhat tiles, 8 x [16 rows (8ch+c)][128 r]
-constexpr uint32_t OFF_PB = 163840;              // prefix B   [64 rows (8jj+4ch+c)][128 r]
-constexpr uint32_t OFF_PA = 180224;              // prefix A   [64 rows][128 (ch,p)]
-constexpr uint32_t OFF_RING = OFF_PB;            // ring stage s: X at +8 KB s, B at +8 KB s + 4 KB
+constexpr uint32_t OFF_PA = 163840;              // prefix A tiles, 8 x [16 rows (8ch+c)][128 (ch,p)]
 constexpr uint32_t OFF_ROT = 196608;             // span rotation rows, 8 tokens x 2 chunks x 512 B
 constexpr uint32_t OFF_IDA = 204800;             // item da: 2 chunks x 64 tokens x 4 heads fp32
 constexpr uint32_t OFF_ACUM = 206848;            // cumulative da, 2 chunks x 64 fp32
@@ -58,15 +55,15 @@ constexpr uint32_t OFF_LT = 215552;              // span decay matrix L: 2 chunk
 constexpr uint32_t OFF_M1 = 216064;              // d_m1 [128] fp32
 constexpr uint32_t OFF_CTL = 217216;
 constexpr uint32_t SMEM_BYTES = OFF_CTL + 512 + 1024;
-static_assert(OFF_SX % 1024 == 0 && OFF_SB % 1024 == 0 && OFF_PB % 1024 == 0 && OFF_PA % 1024 == 0, "tiles");
+static_assert(OFF_SX % 1024 == 0 && OFF_SB % 1024 == 0 && OFF_PA % 1024 == 0, "tiles");
 static_assert(OFF_ROT % 128 == 0 && OFF_IDA % 128 == 0 && OFF_CTL % 8 == 0, "tensor-copy slots");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Ctl {
     uint64_t itemfull, itemdone;
-    uint64_t full[NS], empty[NS];
+    uint64_t afull[2], ascaled[2], aempty[2];  // forward-sweep span buffers
     uint64_t wfull[2], wfree[2];
-    uint64_t spanfull, spanfree, pbready;
+    uint64_t spanfull, spanfree;
     uint64_t pafull, pafree, pfull, pfree;
     uint64_t cfull, cfree, dcfull, dcfree;
     uint64_t gfull, gfree, dxfull, dxfree;
@@ -113,16 +110,43 @@ __device__ __forceinline__ void transpose_reduce16(float (&v)[16], int lane) {
     v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
+// The same for 8 values: on return v[0] of lane L holds the sum over all lanes of v[L & 7].
+__device__ __forceinline__ void transpose_reduce8(float (&v)[8], int lane) {
+#pragma unroll
+    for (int off = 4; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = upper ? v[i] : v[i + off];
+            const float keep = upper ? v[i + off] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 8);
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
+// Whether the 16-column group gcol holds rotated columns (pairs, x halves or 4-blocks whose
+// angle / quaternion index lies below the rotated width); the others rotate by the identity.
+template <int ROTK>
+__device__ __forceinline__ bool group_rotated(const MMParams& P, int gcol) {
+    if (ROTK == ROT_PAIRWISE) return 8 * gcol < P.na;
+    if (ROTK == ROT_HALF) return 16 * gcol < P.na;
+    if (ROTK == ROT_QUAT) return 4 * gcol < P.J;
+    return false;
+}
+
 // (out_a, out_b) = rotation of the two slots of a pass: de-rotation R(-theta) / Q (x) . (TR =
 // false) or its transpose (TR = true).  cf: cos at [0,64), sin at [64,128) of this token and
 // chunk's angles; qt: its raw quaternions.  ka / kb: first column of slot a / b.
 template <int ROTK, int LAYB, bool TR>
-__device__ __forceinline__ void rot_pass(const MMParams& P, int pass, int ka, int kb, float (&a)[16], float (&b)[16],
-                                         const float* cf, const float* qt) {
+__device__ __forceinline__ void rot_pass(const MMParams& P, int pass, int ka, int kb, bool act_a, bool act_b,
+                                         float (&a)[16], float (&b)[16], const float* cf, const float* qt) {
     // cf holds cos / sin for all 64 angle slots; slots at or past the rotated width hold (1, 0)
     if (ROTK == ROT_PAIRWISE) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
+            if (!(s ? act_b : act_a)) continue;
             float(&v)[16] = s ? b : a;
             const int i0 = (s ? kb : ka) >> 1;  // 8 consecutive angles
             float cs[8], sn[8];
@@ -139,7 +163,7 @@ __device__ __forceinline__ void rot_pass(const MMParams& P, int pass, int ka, in
             }
         }
     } else if (ROTK == ROT_HALF) {
-        if (LAYB && pass == 1) return;  // padding columns of r = 64
+        if ((LAYB && pass == 1) || !act_a) return;  // padding columns of r = 64 / identity
 #pragma unroll
         for (int e4 = 0; e4 < 16; e4 += 4) {
             const float4 c4 = *reinterpret_cast<const float4*>(cf + ka + e4);
@@ -157,6 +181,7 @@ __device__ __forceinline__ void rot_pass(const MMParams& P, int pass, int ka, in
     } else if (ROTK == ROT_QUAT) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
+            if (!(s ? act_b : act_a)) continue;
             float(&v)[16] = s ? b : a;
             const int k0 = s ? kb : ka;
 #pragma unroll
@@ -189,9 +214,8 @@ struct Par {
 };
 // bit positions
 enum : uint32_t {
-    B_FULL = 0,                       // NS ring stages
     B_W = 4,                          // 2 W buffers
-    B_ITEM = 6, B_SPAN, B_PB, B_PA, B_P, B_C, B_DC, B_G, B_DX, B_ITEMDONE, B_SPANFREE,
+    B_ITEM = 6, B_SPAN, B_PA, B_P, B_C, B_DC, B_G, B_DX, B_ITEMDONE, B_SPANFREE,
     U_PRE = 24, U_DC, U_DX, U_PA, U_C, U_G, U_SPAN
 };
 template <int ROTK, int LAYB>
@@ -215,17 +239,15 @@ __global__ void __launch_bounds__(NTHR, 1)
     if (tid == 0) {
         tc::mbar_init(&ctl->itemfull, 1);
         tc::mbar_init(&ctl->itemdone, NCW);
-        for (int s = 0; s < NS; ++s) {
-            tc::mbar_init(&ctl->full[s], 1);
-            tc::mbar_init(&ctl->empty[s], 1 + NCW);
-        }
         for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&ctl->afull[i], 1);
+            tc::mbar_init(&ctl->ascaled[i], NCW);
+            tc::mbar_init(&ctl->aempty[i], 1 + NCW);
             tc::mbar_init(&ctl->wfull[i], 1);
             tc::mbar_init(&ctl->wfree[i], NCW);
         }
         tc::mbar_init(&ctl->spanfull, 1);
         tc::mbar_init(&ctl->spanfree, 1 + NCW);
-        tc::mbar_init(&ctl->pbready, NCW);
         tc::mbar_init(&ctl->pafull, NCW);
         tc::mbar_init(&ctl->pafree, 1);
         tc::mbar_init(&ctl->pfull, 1);
@@ -259,7 +281,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     if (warp == WARP_TMA) {
         // ====================================================================== TMA producer
         if (lane == 0) {
-            uint32_t q = 0;  // ring uses
+            uint32_t na0 = 0, na1 = 0;  // forward-sweep uses of the two span buffers
             Par pr;
             bool ok = true;
             for (int it = it0; it < it1 && ok; ++it) {
@@ -274,23 +296,31 @@ __global__ void __launch_bounds__(NTHR, 1)
                     if (I.exists[ch])
                         tc::tma_load_2d(sm + OFF_IDA + ch * 1024, &tmd, I.hh & ~3, I.bb * P.s + (2 * I.k + ch) * FL,
                                         &ctl->itemfull);
-                // forward sweep tokens through the ring
-                for (int t = 0; t < I.T[0] && ok; ++t, ++q) {
-                    const uint32_t s = q % NS, u = q / NS;
-                    if (u >= 1) ok &= tc::mbar_wait(&ctl->empty[s], (u - 1) & 1, abort);
+                // forward sweep: spans 0 .. nsp-2 alternate between the two span buffers (the last
+                // one in buffer 1, so that buffer 0 frees up first for the reverse sweep)
+                const int nA = (I.T[0] + SPAN - 1) / SPAN - 1;
+                for (int k = 0; k < nA && ok; ++k) {
+                    const int b = ((nA - 1 - k) & 1) ^ 1;
+                    if ((b ? na1 : na0) >= 1) ok &= tc::mbar_wait(&ctl->aempty[b], ((b ? na1 : na0) - 1) & 1, abort);
                     if (!ok) break;
                     uint32_t by = 0;
-                    for (int ch = 0; ch < 2; ++ch) by += I.exists[ch] ? stage_tx : 0u;
-                    tc::mbar_arrive_expect_tx(&ctl->full[s], by);
-                    unsigned char* st = sm + OFF_RING + s * 8192;
-                    for (int ch = 0; ch < 2; ++ch) {
-                        if (!I.exists[ch]) continue;
-                        const int row = I.bb * P.s + (2 * I.k + ch) * FL + t;
-                        tc::tma_load_4d(st + ch * 3072, &tmx, 0, I.hh, 0, row, &ctl->full[s]);
-                        for (int a = 0; a < R / 64; ++a)
-                            tc::tma_load_5d(st + 4096 + a * 2048 + ch * 1024, &tmb, 0, a, I.hh, 0, row, &ctl->full[s]);
-                    }
+                    for (int ch = 0; ch < 2; ++ch) by += I.exists[ch] ? SPAN * stage_tx : 0u;
+                    tc::mbar_arrive_expect_tx(&ctl->afull[b], by);
+                    unsigned char* xb = sm + (b ? OFF_PA : OFF_SX);
+                    unsigned char* bt = sm + (b ? OFF_C : OFF_SB);
+                    for (int jj = 0; jj < SPAN; ++jj)
+                        for (int ch = 0; ch < 2; ++ch) {
+                            if (!I.exists[ch]) continue;
+                            const int row = I.bb * P.s + (2 * I.k + ch) * FL + k * SPAN + jj;
+                            tc::tma_load_4d(xb + jj * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row, &ctl->afull[b]);
+                            for (int a = 0; a < R / 64; ++a)
+                                tc::tma_load_5d(bt + jj * 4096 + a * 2048 + ch * 1024, &tmb, 0, a, I.hh, 0, row,
+                                                &ctl->afull[b]);
+                        }
+                    if (b) ++na1; else ++na0;
                 }
+                // the reverse sweep's first span goes into buffer 0 once the forward sweep is done with it
+                if (ok && na0 >= 1) ok &= tc::mbar_wait(&ctl->aempty[0], (na0 - 1) & 1, abort);
                 if (ok) {
                     const int nsp = (I.T[0] + SPAN - 1) / SPAN;
                     for (int sg = nsp - 1; sg >= 0 && ok; --sg) {
@@ -327,12 +357,12 @@ __global__ void __launch_bounds__(NTHR, 1)
             const uint32_t idDC = tc::idesc_bf16(128, 128, 0, 0);
             const uint32_t idDX = tc::idesc_bf16(128, 16, 0, 0);
             const uint32_t idDB = tc::idesc_bf16(128, 16, 1, 0);
-            const uint32_t s_ring = tc::smem_u32(sm + OFF_RING), s_c = tc::smem_u32(sm + OFF_C);
+            const uint32_t s_c = tc::smem_u32(sm + OFF_C);
             const uint32_t s_g = tc::smem_u32(sm + OFF_G), s_ds = tc::smem_u32(sm + OFF_DS);
             const uint32_t s_sx = tc::smem_u32(sm + OFF_SX), s_sb = tc::smem_u32(sm + OFF_SB);
-            const uint32_t s_pa = tc::smem_u32(sm + OFF_PA), s_pb = tc::smem_u32(sm + OFF_PB);
+            const uint32_t s_pa = tc::smem_u32(sm + OFF_PA);
             Par pr;
-            uint32_t q = 0, nw = 0;
+            uint32_t na0 = 0, na1 = 0, nw = 0;
             bool ok = true;
             // d_xhat / d_bhat MMAs: A = g tile (K-major rows (ch,p) / MN-major columns r), B = one
             // token's bhat / xhat tile [16 rows (8 ch + c)][128] K-major.
@@ -357,10 +387,11 @@ __global__ void __launch_bounds__(NTHR, 1)
                 if (!tc::mbar_wait(&ctl->pafull, pr.next(B_PA), abort)) return false;
                 if (pr.once(U_PRE) && !tc::mbar_wait(&ctl->pfree, pr.next(B_P), abort)) return false;
                 tc::tc_fence_after();
-                const int nk = o / 2 + 1;
-                for (int kq = 0; kq < nk; ++kq)
-                    tc::mma_bf16(tbase + TM_P, tc::sdesc_sw128(s_pa + kq * 2048u, 8192, 1024),
-                                 tc::sdesc_sw128(s_pb + kq * 2048u, 8192, 1024), idPre, kq > 0);
+                // one K = 16 step per span token j <= o: A = L[t,j]-scaled xhat rows (block-diagonal
+                // over the two chunks), B = the token's bhat rows
+                for (int j = 0; j <= o; ++j)
+                    tc::mma_bf16(tbase + TM_P, tc::sdesc_sw128(s_pa + j * 4096u, 2048, 1024),
+                                 tc::sdesc_sw128(s_sb + j * 4096u, 2048, 1024), idPre, j > 0);
                 tc::mma_commit(&ctl->pfull);
                 tc::mma_commit(&ctl->pafree);
                 return true;
@@ -381,24 +412,28 @@ __global__ void __launch_bounds__(NTHR, 1)
             };
             for (int it = it0; it < it1 && ok; ++it) {
                 const Item I = decode_item(A, it);
-                for (int t = 0; t < I.T[0] && ok; ++t, ++q) {
-                    const uint32_t s = q % NS;
-                    const uint32_t xb = s_ring + s * 8192, bb_ = xb + 4096;
-                    if (!(ok = tc::mbar_wait(&ctl->full[s], pr.next(B_FULL + s), abort))) break;
+                // forward sweep: per span, sum_j L[end, j] W_j as one K = 8 x 16 product
+                const int nA = (I.T[0] + SPAN - 1) / SPAN - 1;
+                for (int k = 0; k < nA && ok; ++k) {
+                    const int b = ((nA - 1 - k) & 1) ^ 1;
+                    if (!(ok = tc::mbar_wait(&ctl->ascaled[b], (b ? na1 : na0) & 1, abort))) break;
                     const uint32_t wb = nw & 1;
                     if (nw >= 2 && !(ok = tc::mbar_wait(&ctl->wfree[wb], pr.next(B_W + wb), abort))) break;
                     tc::tc_fence_after();
-                    tc::mma_bf16(tbase + (wb ? TM_DC : TM_P), tc::sdesc_sw128(xb, 2048, 1024),
-                                 tc::sdesc_sw128(bb_, 2048, 1024), idW, 0);
+                    const uint32_t xs = tc::smem_u32(sm + (b ? OFF_PA : OFF_SX));
+                    const uint32_t bs = tc::smem_u32(sm + (b ? OFF_C : OFF_SB));
+                    for (int j = 0; j < SPAN; ++j)
+                        tc::mma_bf16(tbase + (wb ? TM_DC : TM_P), tc::sdesc_sw128(xs + j * 4096u, 2048, 1024),
+                                     tc::sdesc_sw128(bs + j * 4096u, 2048, 1024), idW, j > 0);
                     ++nw;
+                    if (b) ++na1; else ++na0;
                     tc::mma_commit(&ctl->wfull[wb]);
-                    tc::mma_commit(&ctl->empty[s]);
+                    tc::mma_commit(&ctl->aempty[b]);
                 }
                 if (ok) {
                     const int nsp = (I.T[0] + SPAN - 1) / SPAN;
                     for (int sg = nsp - 1; sg >= 0 && ok; --sg) {
                         const int len = min(SPAN, I.T[0] - sg * SPAN);
-                        if (!(ok = tc::mbar_wait(&ctl->pbready, pr.next(B_PB), abort))) break;
                         // pipelined order, matching the compute warps' signals
                         for (int u = len + 1; u >= 0 && ok; --u) {
                             if (u <= len - 1) ok = issue_dx(s_sx + u * 4096u, s_sb + u * 4096u);
@@ -430,7 +465,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         float* Lt = reinterpret_cast<float*>(sm + OFF_LT);                // [2][8][8]
         float* myanchors = B.anchors + (int64_t)blockIdx.x * NANCHOR * 128 * 128;
         Par pr;
-        uint32_t q = 0, nw = 0;
+        uint32_t na0 = 0, na1 = 0, nw = 0;
         bool ok = true;
         for (int it = it0; it < it1; ++it) {
             const Item I = decode_item(A, it);
@@ -499,13 +534,41 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
                             for (int e = 0; e < 16; ++e) S[g][e] = 0.f;
                     }
-                    for (int t = 0; t < I.T[0]; ++t, ++q) {
-                        const uint32_t s = q % NS, wb = nw & 1;
-                        ok &= tc::mbar_wait(&ctl->full[s], pr.next(B_FULL + s), abort);
+                    // per span k: S <- D_k S + sum_j L[end, j] W_j over the span's live tokens; the
+                    // tensor core forms the sum from xhat rows scaled in place by L = exp(a_end - a_j);
+                    // the state after the span is anchor k
+                    const int nA = (I.T[0] + SPAN - 1) / SPAN - 1;
+                    for (int k = 0; k < nA; ++k) {
+                        const int b = ((nA - 1 - k) & 1) ^ 1;
+                        ok &= tc::mbar_wait(&ctl->afull[b], (b ? na1 : na0) & 1, abort);
+                        unsigned char* xb = sm + (b ? OFF_PA : OFF_SX);
+                        for (int i = ctid; i < SPAN * 64; i += NCW * 32) {
+                            const int jc = i & 7, c = (i >> 3) & 3, c2 = (i >> 5) & 1, j = i >> 6;
+                            if (c >= C) continue;
+                            const int Tc = c2 ? I.T[1] : I.T[0];
+                            const int t = k * SPAN + j, tend = min(k * SPAN + SPAN - 1, Tc - 1);
+                            const float L = t < Tc ? __expf(acum[c2 * 64 + tend] - acum[c2 * 64 + t]) : 0.f;
+                            uint4* px = reinterpret_cast<uint4*>(xb + j * 4096 + tc::sw128_chunk(16, c2, 8 * c2 + c, jc));
+                            const uint4 v = *px;
+                            uint4 w;
+                            w.x = tc::pack_bf16x2(L * bf16lo(v.x), L * bf16hi(v.x));
+                            w.y = tc::pack_bf16x2(L * bf16lo(v.y), L * bf16hi(v.y));
+                            w.z = tc::pack_bf16x2(L * bf16lo(v.z), L * bf16hi(v.z));
+                            w.w = tc::pack_bf16x2(L * bf16lo(v.w), L * bf16hi(v.w));
+                            *px = w;
+                        }
+                        tc::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tc::mbar_arrive(&ctl->ascaled[b]);
+                            tc::mbar_arrive(&ctl->aempty[b]);
+                        }
+                        if (b) ++na1; else ++na0;
+                        const uint32_t wb = nw & 1;
                         ok &= tc::mbar_wait(&ctl->wfull[wb], pr.next(B_W + wb), abort);
                         tc::tc_fence_after();
-                        const float et = t < Tch ? e_of(t) : 1.f;
-                        const float wt = t < Tch ? 1.f : 0.f;
+                        const int tend = min(k * SPAN + SPAN - 1, Tch - 1);
+                        const float Dk = k * SPAN < Tch ? __expf(ac[tend] - (k > 0 ? ac[k * SPAN - 1] : 0.f)) : 1.f;
 #pragma unroll
                         for (int pass = 0; pass < 2; ++pass) {
                             float W[2][16];
@@ -516,24 +579,19 @@ __global__ void __launch_bounds__(NTHR, 1)
                             for (int g = 0; g < 2; ++g)
 #pragma unroll
                                 for (int e = 0; e < 16; ++e)
-                                    S[2 * pass + g][e] = fmaf(et, S[2 * pass + g][e], wt * W[g][e]);
+                                    S[2 * pass + g][e] = fmaf(Dk, S[2 * pass + g][e], W[g][e]);
                         }
                         tc::tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) {
-                            tc::mbar_arrive(&ctl->wfree[wb]);
-                            tc::mbar_arrive(&ctl->empty[s]);
-                        }
+                        if (lane == 0) tc::mbar_arrive(&ctl->wfree[wb]);
                         ++nw;
-                        if ((t + 1) % SPAN == 0 && t + 1 < I.T[0]) {  // anchor of the span starting at t + 1
-                            float* dst = myanchors + ((int64_t)((t + 1) / SPAN - 1) * 128 + m) * 128;
+                        float* dst = myanchors + ((int64_t)k * 128 + m) * 128;
 #pragma unroll
-                            for (int g = 0; g < 4; ++g)
+                        for (int g = 0; g < 4; ++g)
 #pragma unroll
-                                for (int e = 0; e < 16; e += 4)
-                                    *reinterpret_cast<float4*>(dst + 16 * G[g] + e) =
-                                        make_float4(S[g][e], S[g][e + 1], S[g][e + 2], S[g][e + 3]);
-                        }
+                            for (int e = 0; e < 16; e += 4)
+                                *reinterpret_cast<float4*>(dst + 16 * G[g] + e) =
+                                    make_float4(S[g][e], S[g][e + 1], S[g][e + 2], S[g][e + 3]);
                     }
                 }
                 // ================================ phase B: spans in reverse, software-pipelined
@@ -564,19 +622,6 @@ __global__ void __launch_bounds__(NTHR, 1)
                         tc::tmem_st16(lane_addr + TM_AN + col0, av);
                     }
                     tc::tmem_wait_st();
-                    // prefix B tile: rows 8 jj + 4 ch' + c  <-  span bhat tile jj, row 8 ch' + c; the
-                    // rows of absent channels and of the pad token of an odd span are zeroed (the
-                    // region held the forward sweep's staging ring)
-                    for (int i = ctid; i < ((len + 1) & ~1) * 8 * 16; i += NCW * 32) {
-                        const int j16 = i & 15, drow = i >> 4;
-                        const int jj = drow >> 3, c2 = (drow >> 2) & 1, c = drow & 3;
-                        const int hv = j16 >> 3, jc = j16 & 7;
-                        uint4 v = make_uint4(0, 0, 0, 0);
-                        if (c < C && jj < len)
-                            v = *reinterpret_cast<const uint4*>(sm + OFF_SB + jj * 4096 +
-                                                                tc::sw128_chunk(16, hv, 8 * c2 + c, jc));
-                        *reinterpret_cast<uint4*>(sm + OFF_PB + tc::sw128_chunk(64, hv, drow, jc)) = v;
-                    }
                     // decay matrix L[t, j] of the span, and cos / sin of its angles
                     if (ctid < 128) {
                         const int c2 = ctid >> 6, o = (ctid >> 3) & 7, jj = ctid & 7;
@@ -595,30 +640,28 @@ __global__ void __launch_bounds__(NTHR, 1)
                     }
                     tc::fence_proxy_async_smem();
                     named_barrier_sync(1, NCW * 32);
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&ctl->pbready);
                     const float a_anchor = s0 > 0 ? ac[s0 - 1] : 0.f;
 
-                    // ---- prefix A rows for token t: L[t, s0+jj] xhat (two tokens per K step)
+                    // ---- prefix A tiles for token t: PA_j = L[t, s0+j] xhat_j for j <= t - s0, in the
+                    // layout of the staged xhat tiles (rows 8 ch + c in column block ch); only those
+                    // rows are written, the rest of the region stays zero
                     auto build_pa = [&](int t) {
                         const int o = t - s0;
                         if (pr.once(U_PA)) ok &= tc::mbar_wait(&ctl->pafree, pr.next(B_PA), abort);
-                        const int nrow_tok = (o % 2 == 0) ? o + 2 : o + 1;
-                        for (int i = ctid; i < nrow_tok * 8 * 16; i += NCW * 32) {
-                            const int j16 = i & 15, drow = i >> 4;
-                            const int jj = drow >> 3, c2 = (drow >> 2) & 1, c = drow & 3;
-                            const int hv = j16 >> 3, jc = j16 & 7;
+                        for (int i = ctid; i < (o + 1) * 64; i += NCW * 32) {
+                            const int jc = i & 7, c = (i >> 3) & 3, c2 = (i >> 5) & 1, j = i >> 6;
+                            if (c >= C) continue;
+                            const uint32_t off = j * 4096u + tc::sw128_chunk(16, c2, 8 * c2 + c, jc);
                             uint4 w = make_uint4(0, 0, 0, 0);
-                            if (hv == c2 && jj <= o && c < C) {
-                                const float L = Lt[(c2 * 8 + o) * 8 + jj];
-                                const uint4 v = *reinterpret_cast<const uint4*>(
-                                    sm + OFF_SX + jj * 4096 + tc::sw128_chunk(16, c2, 8 * c2 + c, jc));
+                            if (c2 ? I.exists[1] : I.exists[0]) {
+                                const float L = Lt[(c2 * 8 + o) * 8 + j];
+                                const uint4 v = *reinterpret_cast<const uint4*>(sm + OFF_SX + off);
                                 w.x = tc::pack_bf16x2(L * bf16lo(v.x), L * bf16hi(v.x));
                                 w.y = tc::pack_bf16x2(L * bf16lo(v.y), L * bf16hi(v.y));
                                 w.z = tc::pack_bf16x2(L * bf16lo(v.z), L * bf16hi(v.z));
                                 w.w = tc::pack_bf16x2(L * bf16lo(v.w), L * bf16hi(v.w));
                             }
-                            *reinterpret_cast<uint4*>(sm + OFF_PA + tc::sw128_chunk(64, hv, drow, jc)) = w;
+                            *reinterpret_cast<uint4*>(sm + OFF_PA + off) = w;
                         }
                         tc::fence_proxy_async_smem();
                         __syncwarp();
@@ -651,7 +694,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                                 dotv[e & 1] = fmaf(gr[sa][e], ha[e], dotv[e & 1]);
                                 dotv[2 + (e & 1)] = fmaf(gr[sb][e], hb[e], dotv[2 + (e & 1)]);
                             }
-                            rot_pass<ROTK, LAYB, false>(P, pass, 16 * G[sa], 16 * G[sb], ha, hb, cf, qt);
+                            rot_pass<ROTK, LAYB, false>(P, pass, 16 * G[sa], 16 * G[sb], group_rotated<ROTK>(P, G[sa]),
+                                                        group_rotated<ROTK>(P, G[sb]), ha, hb, cf, qt);
                             write_tile16(sm + OFF_C, m, G[sa], ha, !live);
                             write_tile16(sm + OFF_C, m, G[sb], hb, !live);
                         }
@@ -676,10 +720,20 @@ __global__ void __launch_bounds__(NTHR, 1)
                         const float* cf = coefs + (o * 2 + ch) * 128;
                         const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + ch * 512);
                         const int64_t orot = off_rot(P, I.bb, n * FL + t, I.hh);
-                        const bool rot_out = P.rw > 0 && chunk_ok && n < I.proc && live;
+                        const bool rot_out = P.rw > 0 && chunk_ok && n < I.proc;
+                        if (!live) {  // past valid_len: d_c = 0, so g_t = e_{t+1} g_{t+1}
+                            tc::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) tc::mbar_arrive(&ctl->dcfree);
+#pragma unroll
+                            for (int g = 0; g < 4; ++g)
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) gr[g][e] *= e_next;
+                        } else {
 #pragma unroll
                         for (int pass = 0; pass < 2; ++pass) {
                             const int sa = slot_a<LAYB>(pass), sb = slot_b<LAYB>(pass);
+                            const bool act_a = group_rotated<ROTK>(P, G[sa]), act_b = group_rotated<ROTK>(P, G[sb]);
                             float da_[16], db_[16];
                             tc::tmem_ld16(lane_addr + TM_DC + 16 * G[sa], da_);
                             tc::tmem_ld16(lane_addr + TM_DC + 16 * G[sb], db_);
@@ -688,32 +742,44 @@ __global__ void __launch_bounds__(NTHR, 1)
                             for (int e = 0; e < 16; e += 4) {
                                 const float4 ma = *reinterpret_cast<const float4*>(m1s + 16 * G[sa] + e);
                                 const float4 mb = *reinterpret_cast<const float4*>(m1s + 16 * G[sb] + e);
-                                da_[e] = live ? da_[e] + ma.x : 0.f; da_[e + 1] = live ? da_[e + 1] + ma.y : 0.f;
-                                da_[e + 2] = live ? da_[e + 2] + ma.z : 0.f; da_[e + 3] = live ? da_[e + 3] + ma.w : 0.f;
-                                db_[e] = live ? db_[e] + mb.x : 0.f; db_[e + 1] = live ? db_[e + 1] + mb.y : 0.f;
-                                db_[e + 2] = live ? db_[e + 2] + mb.z : 0.f; db_[e + 3] = live ? db_[e + 3] + mb.w : 0.f;
+                                da_[e] += ma.x; da_[e + 1] += ma.y; da_[e + 2] += ma.z; da_[e + 3] += ma.w;
+                                db_[e] += mb.x; db_[e + 1] += mb.y; db_[e + 2] += mb.z; db_[e + 3] += mb.w;
                             }
-                            // rotation-parameter gradient of the pass, summed over the warp's 32 rows;
-                            // after a 16-value transpose reduction lane L (< 16) holds value L
+                            // rotation-parameter gradient of the pass, summed over the warp's 32 rows
+                            // by a transpose reduction (lane L then holds value L)
                             if (ROTK == ROT_PAIRWISE) {
-                                float v[16];
-                                {
-                                    float cc[16];
-                                    read_tile16(sm + OFF_C, m, G[sa], cc);
+                                if (act_b) {  // both slots hold rotated pairs
+                                    float v[16];
+                                    {
+                                        float cc[16];
+                                        read_tile16(sm + OFF_C, m, G[sa], cc);
 #pragma unroll
-                                    for (int e = 0; e < 16; e += 2) v[e / 2] = da_[e] * cc[e + 1] - da_[e + 1] * cc[e];
-                                }
-                                {
-                                    float cc[16];
-                                    read_tile16(sm + OFF_C, m, G[sb], cc);
+                                        for (int e = 0; e < 16; e += 2) v[e / 2] = da_[e] * cc[e + 1] - da_[e + 1] * cc[e];
+                                    }
+                                    {
+                                        float cc[16];
+                                        read_tile16(sm + OFF_C, m, G[sb], cc);
 #pragma unroll
-                                    for (int e = 0; e < 16; e += 2) v[8 + e / 2] = db_[e] * cc[e + 1] - db_[e + 1] * cc[e];
+                                        for (int e = 0; e < 16; e += 2)
+                                            v[8 + e / 2] = db_[e] * cc[e + 1] - db_[e + 1] * cc[e];
+                                    }
+                                    transpose_reduce16(v, lane);
+                                    const int ang = 8 * ((lane & 8) ? G[sb] : G[sa]) + (lane & 7);
+                                    if (lane < 16 && ang < P.na && rot_out) atomicAdd(B.drot + orot + ang, v[0]);
+                                } else if (act_a) {
+                                    float v[8];
+                                    {
+                                        float cc[16];
+                                        read_tile16(sm + OFF_C, m, G[sa], cc);
+#pragma unroll
+                                        for (int e = 0; e < 16; e += 2) v[e / 2] = da_[e] * cc[e + 1] - da_[e + 1] * cc[e];
+                                    }
+                                    transpose_reduce8(v, lane);
+                                    const int ang = 8 * G[sa] + (lane & 7);
+                                    if (lane < 8 && ang < P.na && rot_out) atomicAdd(B.drot + orot + ang, v[0]);
                                 }
-                                transpose_reduce16(v, lane);
-                                const int ang = 8 * ((lane & 8) ? G[sb] : G[sa]) + (lane & 7);
-                                if (lane < 16 && ang < P.na && rot_out) atomicAdd(B.drot + orot + ang, v[0]);
                             } else if (ROTK == ROT_HALF) {
-                                if (!(LAYB && pass == 1)) {
+                                if (!(LAYB && pass == 1) && act_a) {
                                     float v[16];
                                     {
                                         float cc[16];
@@ -735,6 +801,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                 // sum_p d_c (x) conj(c) per 4-block, then (.) (x) Q / |Q|^2
 #pragma unroll
                                 for (int sl = 0; sl < 2; ++sl) {
+                                    if (!(sl ? act_b : act_a)) continue;
                                     const int gsl = sl ? sb : sa;
                                     float v[16];
                                     {
@@ -766,7 +833,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                 }
                             }
                             // G = derot^T(d_c); g_t = G_t + e_{t+1} g_{t+1}
-                            rot_pass<ROTK, LAYB, true>(P, pass, 16 * G[sa], 16 * G[sb], da_, db_, cf, qt);
+                            rot_pass<ROTK, LAYB, true>(P, pass, 16 * G[sa], 16 * G[sb], act_a, act_b, da_, db_, cf, qt);
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 gr[sa][e] = fmaf(e_next, gr[sa][e], da_[e]);
@@ -776,6 +843,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         tc::tc_fence_before();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&ctl->dcfree);
+                        }
                         e_next = e_of(t);
                         if (pr.once(U_G)) ok &= tc::mbar_wait(&ctl->gfree, pr.next(B_G), abort);
 #pragma unroll
@@ -847,12 +915,6 @@ __global__ void __launch_bounds__(NTHR, 1)
                             }
                     }
                 }
-                // the forward-sweep ring shares memory with the prefix tiles: restore the zero
-                // padding rows the next item's W products rely on
-                named_barrier_sync(1, NCW * 32);
-                for (uint32_t i = ctid; i < 32768 / 16; i += NCW * 32)
-                    reinterpret_cast<uint4*>(sm + OFF_RING)[i] = make_uint4(0, 0, 0, 0);
-                tc::fence_proxy_async_smem();
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ctl->itemdone);
