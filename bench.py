@@ -93,6 +93,14 @@ def kernel_bytes_per_token_head(name, w):
     return 0
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per processed token-head of the
+# dominant kernels, from one ncu capture of the current kernels on large_s4096 cut to b = 2; the
+# work per chunk pair does not depend on b, so a full launch moves these bytes times its
+# token-heads.
+MEASURED_DRAM_BYTES_PER_TOKEN_HEAD = {"tc_bwd_chunk": 2.9397e9 / (2 * 4096 * 32),
+                                      "tc_fwd_chunk": 0.67248e9 / (2 * 4096 * 32)}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -357,12 +365,14 @@ def run_ours(args):
         per_launch_ms = tms / nl
         fl = kernel_flops_per_token_head(name, w) * token_heads
         by = kernel_bytes_per_token_head(name, w) * token_heads
+        tr = MEASURED_DRAM_BYTES_PER_TOKEN_HEAD.get(name) if w.name == "large_s4096" else None
+        traffic = tr * token_heads if tr else None
         sm_mhz = clk.get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
         if name.startswith("tc_") and fl:
             achieved = fl / (per_launch_ms / 1e3) / 1e12
             pk = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
             roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
-                    "traffic": None, "kernel": name,
+                    "traffic": traffic, "kernel": name,
                     "peak_source": f"{peak_src} cuBLAS bf16 dense, sustained (kernel timed inside a step)",
                     "flops_per_launch": fl, "ms_per_launch": per_launch_ms}
         elif fl:
