@@ -63,17 +63,28 @@ def tokens_of(inp, s):
 
 # ----------------------------------------------------------------- algorithmic counts
 def kernel_flops_per_token_head(name, w):
-    """Dense-contraction + recurrence flops one kernel must do per processed token-head."""
+    """Algorithmic flops per processed token-head of one kernel: the split over kernels of the
+    fwd+bwd figure F = 4pr^2 + 3(l+1)pr + 10Cpr + 10pr (the m2 and d_c Grams, the causal half of
+    the state contractions for the forward states, the recomputed states and d_W, the writes and
+    their VJPs, the carries), l = the internal chunk length of the tensor-core path (64)."""
     p, r, C = w.p, w.r, w.C
+    l = 64 if name.startswith("tc_") else w.chunk_len
     if name in ("fwd_chunk", "tc_fwd_chunk"):
-        return 2 * p * r * r + 2 * C * p * r + 2 * p * r          # Gram m2, writes, decay step
+        return 2 * p * r * r + (l + 1) * p * r + 2 * C * p * r + 2 * p * r      # m2, states, W, decay
     if name in ("bwd_chunk", "tc_bwd_chunk"):
-        return 2 * p * r * r + 6 * C * p * r + 4 * p * r          # d_c, writes + d_xhat + d_bhat, 2 recurrences
+        return 2 * p * r * r + 2 * (l + 1) * p * r + 6 * C * p * r + 6 * p * r  # d_c, states + d_W, W + d_x/d_b, scal/e_n
     if name in ("chunk_end", "tc_chunk_end"):
         return 2 * C * p * r + 2 * p * r
     if name in ("correct", "tc_correct"):
         return 6 * C * p * r
     return 0
+
+
+def step_flops_per_token_head(w):
+    """F = 4pr^2 + 3(l+1)pr + 10Cpr + 10pr, the whole fwd+bwd step's algorithmic flops."""
+    p, r, C = w.p, w.r, w.C
+    l = w.chunk_len
+    return 4 * p * r * r + 3 * (l + 1) * p * r + 10 * C * p * r + 10 * p * r
 
 
 def kernel_bytes_per_token_head(name, w):
@@ -412,6 +423,14 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, inp)
 
+    # whole-step algorithmic rate (F per token-head, fwd+bwd) against the sustained bf16 peak
+    step_tflops = None
+    if ms_max > 0:
+        th = sum(min(int(v), w.s) for v in vl) * w.h * world
+        pk_ = measured_peaks()[0].get("bf16_tflops_sustained")
+        ach = step_flops_per_token_head(w) * th / (ms_max / 1e3) / 1e12
+        step_tflops = {"achieved": ach, "peak": pk_, "frac": ach / pk_ if pk_ else None,
+                       "flops_per_token_head": step_flops_per_token_head(w)}
     if rank == 0:
         line = {
             "metric": "moments fwd+bwd tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -427,6 +446,7 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (operands 1.7 GB), no flush"},
             "e2e": e2e, "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu, "clocks": clk,
             "kernels_ms_per_step": {k: v[0] / args.steps for k, v in kernels.items()},
+            "step_tflops": step_tflops,
             "device_status": dev_status,
         }
         print(json.dumps(line), flush=True)

@@ -126,16 +126,6 @@ __device__ __forceinline__ void transpose_reduce8(float (&v)[8], int lane) {
     v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
-// Whether the 16-column group gcol holds rotated columns (pairs, x halves or 4-blocks whose
-// angle / quaternion index lies below the rotated width); the others rotate by the identity.
-template <int ROTK>
-__device__ __forceinline__ bool group_rotated(const MMParams& P, int gcol) {
-    if (ROTK == ROT_PAIRWISE) return 8 * gcol < P.na;
-    if (ROTK == ROT_HALF) return 16 * gcol < P.na;
-    if (ROTK == ROT_QUAT) return 4 * gcol < P.J;
-    return false;
-}
-
 // (out_a, out_b) = rotation of the two slots of a pass: de-rotation R(-theta) / Q (x) . (TR =
 // false) or its transpose (TR = true).  cf: cos at [0,64), sin at [64,128) of this token and
 // chunk's angles; qt: its raw quaternions.  ka / kb: first column of slot a / b.

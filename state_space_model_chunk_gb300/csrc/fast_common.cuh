@@ -186,6 +186,16 @@ __device__ __forceinline__ int slot_a(int pass) { return LAYB ? 2 * pass : pass;
 template <int LAYB>
 __device__ __forceinline__ int slot_b(int pass) { return LAYB ? 2 * pass + 1 : pass + 2; }
 
+// Whether the 16-column group gcol holds rotated columns (pairs, x halves or 4-blocks whose
+// angle / quaternion index lies below the rotated width); the others rotate by the identity.
+template <int ROTK>
+__device__ __forceinline__ bool group_rotated(const MMParams& P, int gcol) {
+    if (ROTK == ROT_PAIRWISE) return 8 * gcol < P.na;
+    if (ROTK == ROT_HALF) return 16 * gcol < P.na;
+    if (ROTK == ROT_QUAT) return 4 * gcol < P.J;
+    return false;
+}
+
 // host helpers
 cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, const float* rot, const float* da,
                         TensorMaps* maps);

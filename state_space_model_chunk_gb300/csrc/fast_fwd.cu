@@ -273,7 +273,6 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const bool live = t < Tch;
                 const float et = live ? __expf(reinterpret_cast<const float*>(sm + OFF_DA + s * 256 + ch * 128)[I.hh & 3])
                                       : 1.f;
-                const float wt = live ? 1.f : 0.f;
                 const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + s * 1024 + ch * 512);
                 if (ROTK == ROT_PAIRWISE || ROTK == ROT_HALF) {
                     float sv = 0.f, cv = 1.f;
@@ -288,22 +287,28 @@ __global__ void __launch_bounds__(NTHR, 1)
                 if (uc >= 1) check(tc::mbar_wait(&ctl->cfree[cb], (uc - 1) & 1, abort));
                 tc::tc_fence_after();
                 unsigned char* ct = sm + OFF_C + cb * C_BYTES;
+                // all four column groups of W_t in one tensor-memory round trip
+                float Wt[4][16];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) tc::tmem_ld16(lane_addr + TM_W + wb * 128 + 16 * G[g], Wt[g]);
+                tc::tmem_wait_ld();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ctl->wfree[wb]);
 #pragma unroll
                 for (int pass = 0; pass < 2; ++pass) {
                     const int sa = slot_a<LAYB>(pass), sb = slot_b<LAYB>(pass);
-                    float a[16], b[16];
-                    tc::tmem_ld16(lane_addr + TM_W + wb * 128 + 16 * G[sa], a);
-                    tc::tmem_ld16(lane_addr + TM_W + wb * 128 + 16 * G[sb], b);
-                    tc::tmem_wait_ld();
-                    if (pass == 1) {
-                        tc::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&ctl->wfree[wb]);
+                    float(&a)[16] = Wt[sa];
+                    float(&b)[16] = Wt[sb];
+                    if (live) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            S[sa][e] = fmaf(et, S[sa][e], a[e]);
+                            S[sb][e] = fmaf(et, S[sb][e], b[e]);
+                        }
                     }
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        S[sa][e] = fmaf(et, S[sa][e], wt * a[e]);
-                        S[sb][e] = fmaf(et, S[sb][e], wt * b[e]);
                         a[e] = S[sa][e];
                         b[e] = S[sb][e];
                     }
@@ -311,6 +316,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     if (ROTK == ROT_PAIRWISE) {
 #pragma unroll
                         for (int sl = 0; sl < 2; ++sl) {
+                            if (!group_rotated<ROTK>(P, G[sl ? sb : sa])) continue;  // identity
                             float(&v)[16] = sl ? b : a;
                             const int ti = 8 * (sl ? sb : sa);
                             float cs[8], sn[8];
@@ -326,7 +332,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                             }
                         }
                     } else if (ROTK == ROT_HALF) {
-                        if (!(LAYB && pass == 1)) {
+                        if (!(LAYB && pass == 1) && group_rotated<ROTK>(P, G[sa])) {
                             const int ti = 16 * pass;
 #pragma unroll
                             for (int e4 = 0; e4 < 16; e4 += 4) {
@@ -345,6 +351,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     } else if (ROTK == ROT_QUAT) {
 #pragma unroll
                         for (int sl = 0; sl < 2; ++sl) {
+                            if (!group_rotated<ROTK>(P, G[sl ? sb : sa])) continue;  // identity
                             float(&v)[16] = sl ? b : a;
                             const int k0 = 16 * G[sl ? sb : sa];
 #pragma unroll
