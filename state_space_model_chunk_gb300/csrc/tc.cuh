@@ -34,17 +34,25 @@ __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-// Bounded wait for the phase with the given parity to complete.  Gives up after `limit`
-// polls (each poll already suspends in hardware for a short time; late polls also sleep), or
-// as soon as *abort is set by another thread; returns false then.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t limit = (1u << 22)) {
+// Polling loop of mbar_wait, kept out of line: a phase that has already completed costs one
+// try_wait (about 50 cycles) instead of the loop's setup (about 190 cycles measured).
+static __device__ __noinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                   uint32_t limit) {
     for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if (i > 64) __nanosleep(i > 4096 ? 256 : 32);
     }
     return false;
+}
+
+// Bounded wait for the phase with the given parity to complete.  Gives up after `limit`
+// polls (each poll already suspends in hardware for a short time; late polls also sleep), or
+// as soon as *abort is set by another thread; returns false then.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t limit = (1u << 22)) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_poll(bar, parity, abort, limit);
 }
 
 // ----------------------------------------------------------------------- fences

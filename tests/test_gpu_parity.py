@@ -116,6 +116,23 @@ def test_parity_chunk_len_extremes(l):
     check_against_oracle(w, inp, got, w.name)
 
 
+def test_parity_steep_decay_spans():
+    """Decays far outside the usual range: two heads with per-token log-decay near -25, single
+    reset tokens (da = -70) in another, the last head unchanged, so the backward sees spans
+    whose prefix decay factors around the span midpoint would leave the safe exponent range
+    next to spans where they do not."""
+    w = WORKLOADS["large_s4096"].scaled(name="steep", b=2, s=256, h=4, C=2, valid="fixed:250")
+    inp = make_inputs(w)
+    da = inp["da"].clone()
+    da[:, :, 0:2] *= 50.0
+    da[:, 37, 2] = -70.0
+    da[:, 101, 2] = -70.0
+    da[1, 200:204, 2] = -35.0
+    inp["da"] = da.contiguous()
+    got = run_gpu(w, inp)
+    check_against_oracle(w, inp, got, w.name)
+
+
 FULL = ["quat_s2048", "large_s4096", "ragged_s16384"]
 
 
