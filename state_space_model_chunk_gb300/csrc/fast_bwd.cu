@@ -41,19 +41,18 @@ constexpr int SPAN = 8;        // tokens per anchor span
 constexpr int NANCHOR = 7;     // anchors per 64-token chunk kept in the workspace (anchor 0 = carry)
 
 // shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_C = 0;                    // c tile     [128 rows (ch,p)][128 r] bf16, 32 KB
-constexpr uint32_t OFF_G = 32768;                // g tile     (same layout)
-constexpr uint32_t OFF_DS = 65536;               // D + D^T    [128 r2][128 r1] bf16
-constexpr uint32_t OFF_SX = 98304;               // span xhat tiles, 8 x [16 rows (8ch+c)][128 (ch,p)]
-constexpr uint32_t OFF_SB = 131072;              // span bhat tiles, 8 x [16 rows (8ch+c)][128 r]
-constexpr uint32_t OFF_PA = 163840;              // prefix A tiles, 8 x [16 rows (8ch+c)][128 (ch,p)]
-constexpr uint32_t OFF_ROT = 196608;             // span rotation rows, 8 tokens x 2 chunks x 512 B
-constexpr uint32_t OFF_IDA = 204800;             // item da: 2 chunks x 64 tokens x 4 heads fp32
-constexpr uint32_t OFF_ACUM = 206848;            // cumulative da, 2 chunks x 64 fp32
-constexpr uint32_t OFF_COEF = 207360;            // span cos|sin: 8 tokens x 2 chunks x 128 fp32
-constexpr uint32_t OFF_LT = 215552;              // span decay matrix L: 2 chunks x 8 x 8 fp32
-constexpr uint32_t OFF_M1 = 216064;              // d_m1 [128] fp32
-constexpr uint32_t OFF_CTL = 217216;
+constexpr uint32_t OFF_G = 0;                    // g tile [128 rows (ch,p)][128 r] bf16, 32 KB
+constexpr uint32_t OFF_DS = 32768;               // D + D^T    [128 r2][128 r1] bf16
+constexpr uint32_t OFF_SX = 65536;               // span xhat tiles, 8 x [16 rows (8ch+c)][128 (ch,p)]
+constexpr uint32_t OFF_SB = 98304;               // span bhat tiles, 8 x [16 rows (8ch+c)][128 r]
+constexpr uint32_t OFF_PA = 131072;              // prefix A tiles, 8 x [16 rows (8ch+c)][128 (ch,p)]
+constexpr uint32_t OFF_ROT = 163840;             // span rotation rows, 8 tokens x 2 chunks x 512 B
+constexpr uint32_t OFF_IDA = 172032;             // item da: 2 chunks x 64 tokens x 4 heads fp32
+constexpr uint32_t OFF_ACUM = 174080;            // cumulative da, 2 chunks x 64 fp32
+constexpr uint32_t OFF_COEF = 174592;            // span cos|sin: 8 tokens x 2 chunks x 128 fp32
+constexpr uint32_t OFF_LT = 182784;              // span decay matrix L: 2 chunks x 8 x 8 fp32
+constexpr uint32_t OFF_M1 = 183296;              // d_m1 [128] fp32
+constexpr uint32_t OFF_CTL = 184448;
 constexpr uint32_t SMEM_BYTES = OFF_CTL + 512 + 1024;
 static_assert(OFF_SX % 1024 == 0 && OFF_SB % 1024 == 0 && OFF_PA % 1024 == 0, "tiles");
 static_assert(OFF_ROT % 128 == 0 && OFF_IDA % 128 == 0 && OFF_CTL % 8 == 0, "tensor-copy slots");
@@ -74,8 +73,27 @@ struct Ctl {
 };
 static_assert(sizeof(Ctl) <= 512, "control block");
 
-// tensor memory columns
-constexpr uint32_t TM_P = 0, TM_DC = 128, TM_AN = 256, TM_DX = 384, TM_DB = 400, TM_COLS = 512;
+// tensor memory columns; CA holds the c tile as bf16 pairs (row = lane), the A operand of the
+// d_c product, so the c tile needs no shared memory
+constexpr uint32_t TM_P = 0, TM_DC = 128, TM_AN = 256, TM_DX = 384, TM_DB = 400, TM_CA = 416, TM_COLS = 512;
+
+// c-tile row of one 16-column group in tensor memory: 16 bf16, two per 32-bit column
+__device__ __forceinline__ void ca_store16(uint32_t taddr, const float (&v)[16], bool zero) {
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = zero ? 0u : tc::pack_bf16x2(v[2 * j], v[2 * j + 1]);
+    tc::tmem_st8u(taddr, w);
+}
+__device__ __forceinline__ void ca_load16(uint32_t taddr, float (&v)[16]) {
+    uint32_t w[8];
+    tc::tmem_ld8u(taddr, w);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        v[2 * j] = bf16lo(w[j]);
+        v[2 * j + 1] = bf16hi(w[j]);
+    }
+}
 
 struct BwdArgs {
     FastArgs F;         // problem, items, Hc (carries), Dn, err
@@ -223,8 +241,8 @@ __global__ void __launch_bounds__(NTHR, 1)
     const int it0 = item_begin(A, blockIdx.x), it1 = item_begin(A, blockIdx.x + 1);
 
     // ---- set-up: zero the operand tiles whose padding rows/halves must read as zero
-    for (uint32_t i = tid; i < (OFF_ROT - OFF_C) / 16; i += NTHR)
-        reinterpret_cast<uint4*>(sm + OFF_C)[i] = make_uint4(0, 0, 0, 0);
+    for (uint32_t i = tid; i < (OFF_ROT - OFF_G) / 16; i += NTHR)
+        reinterpret_cast<uint4*>(sm + OFF_G)[i] = make_uint4(0, 0, 0, 0);
     for (uint32_t i = tid; i < (OFF_CTL - OFF_ROT) / 4; i += NTHR) reinterpret_cast<float*>(sm + OFF_ROT)[i] = 0.f;
     if (tid == 0) {
         tc::mbar_init(&ctl->itemfull, 1);
@@ -297,7 +315,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     for (int ch = 0; ch < 2; ++ch) by += I.exists[ch] ? SPAN * stage_tx : 0u;
                     tc::mbar_arrive_expect_tx(&ctl->afull[b], by);
                     unsigned char* xb = sm + (b ? OFF_PA : OFF_SX);
-                    unsigned char* bt = sm + (b ? OFF_C : OFF_SB);
+                    unsigned char* bt = sm + (b ? OFF_G : OFF_SB);
                     for (int jj = 0; jj < SPAN; ++jj)
                         for (int ch = 0; ch < 2; ++ch) {
                             if (!I.exists[ch]) continue;
@@ -347,7 +365,6 @@ __global__ void __launch_bounds__(NTHR, 1)
             const uint32_t idDC = tc::idesc_bf16(128, 128, 0, 0);
             const uint32_t idDX = tc::idesc_bf16(128, 16, 0, 0);
             const uint32_t idDB = tc::idesc_bf16(128, 16, 1, 0);
-            const uint32_t s_c = tc::smem_u32(sm + OFF_C);
             const uint32_t s_g = tc::smem_u32(sm + OFF_G), s_ds = tc::smem_u32(sm + OFF_DS);
             const uint32_t s_sx = tc::smem_u32(sm + OFF_SX), s_sb = tc::smem_u32(sm + OFF_SB);
             const uint32_t s_pa = tc::smem_u32(sm + OFF_PA);
@@ -393,8 +410,8 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t koff = (ks >> 2) * 16384u + 32u * (ks & 3);
-                    tc::mma_bf16(tbase + TM_DC, tc::sdesc_sw128(s_c + koff, 16, 1024),
-                                 tc::sdesc_sw128(s_ds + koff, 16, 1024), idDC, ks > 0);
+                    tc::mma_bf16_ta(tbase + TM_DC, tbase + TM_CA + 8u * ks, tc::sdesc_sw128(s_ds + koff, 16, 1024), idDC,
+                                    ks > 0);
                 }
                 tc::mma_commit(&ctl->dcfull);
                 tc::mma_commit(&ctl->cfree);
@@ -411,7 +428,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     if (nw >= 2 && !(ok = tc::mbar_wait(&ctl->wfree[wb], pr.next(B_W + wb), abort))) break;
                     tc::tc_fence_after();
                     const uint32_t xs = tc::smem_u32(sm + (b ? OFF_PA : OFF_SX));
-                    const uint32_t bs = tc::smem_u32(sm + (b ? OFF_C : OFF_SB));
+                    const uint32_t bs = tc::smem_u32(sm + (b ? OFF_G : OFF_SB));
                     for (int j = 0; j < SPAN; ++j)
                         tc::mma_bf16(tbase + (wb ? TM_DC : TM_P), tc::sdesc_sw128(xs + j * 4096u, 2048, 1024),
                                      tc::sdesc_sw128(bs + j * 4096u, 2048, 1024), idW, j > 0);
@@ -661,12 +678,12 @@ __global__ void __launch_bounds__(NTHR, 1)
                     auto step_h = [&](int t) {
                         const int o = t - s0;
                         ok &= tc::mbar_wait(&ctl->pfull, pr.next(B_P), abort);
+                        if (pr.once(U_C)) ok &= tc::mbar_wait(&ctl->cfree, pr.next(B_C), abort);  // CA reusable
                         tc::tc_fence_after();
                         const float dsig = __expf(ac[t] - a_anchor);
                         const bool live = t < Tch;
                         const float* cf = coefs + (o * 2 + ch) * 128;
                         const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + ch * 512);
-                        if (pr.once(U_C)) ok &= tc::mbar_wait(&ctl->cfree, pr.next(B_C), abort);
                         float dotv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                         for (int pass = 0; pass < 2; ++pass) {
@@ -686,11 +703,11 @@ __global__ void __launch_bounds__(NTHR, 1)
                             }
                             rot_pass<ROTK, LAYB, false>(P, pass, 16 * G[sa], 16 * G[sb], group_rotated<ROTK>(P, G[sa]),
                                                         group_rotated<ROTK>(P, G[sb]), ha, hb, cf, qt);
-                            write_tile16(sm + OFF_C, m, G[sa], ha, !live);
-                            write_tile16(sm + OFF_C, m, G[sb], hb, !live);
+                            ca_store16(lane_addr + TM_CA + 8 * G[sa], ha, !live);
+                            ca_store16(lane_addr + TM_CA + 8 * G[sb], hb, !live);
                         }
+                        tc::tmem_wait_st();
                         tc::tc_fence_before();
-                        tc::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
                             tc::mbar_arrive(&ctl->pfree);
@@ -742,13 +759,13 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     float v[16];
                                     {
                                         float cc[16];
-                                        read_tile16(sm + OFF_C, m, G[sa], cc);
+                                        ca_load16(lane_addr + TM_CA + 8 * G[sa], cc);
 #pragma unroll
                                         for (int e = 0; e < 16; e += 2) v[e / 2] = da_[e] * cc[e + 1] - da_[e + 1] * cc[e];
                                     }
                                     {
                                         float cc[16];
-                                        read_tile16(sm + OFF_C, m, G[sb], cc);
+                                        ca_load16(lane_addr + TM_CA + 8 * G[sb], cc);
 #pragma unroll
                                         for (int e = 0; e < 16; e += 2)
                                             v[8 + e / 2] = db_[e] * cc[e + 1] - db_[e + 1] * cc[e];
@@ -760,7 +777,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     float v[8];
                                     {
                                         float cc[16];
-                                        read_tile16(sm + OFF_C, m, G[sa], cc);
+                                        ca_load16(lane_addr + TM_CA + 8 * G[sa], cc);
 #pragma unroll
                                         for (int e = 0; e < 16; e += 2) v[e / 2] = da_[e] * cc[e + 1] - da_[e + 1] * cc[e];
                                     }
@@ -773,13 +790,13 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     float v[16];
                                     {
                                         float cc[16];
-                                        read_tile16(sm + OFF_C, m, G[sa], cc);
+                                        ca_load16(lane_addr + TM_CA + 8 * G[sa], cc);
 #pragma unroll
                                         for (int e = 0; e < 16; ++e) v[e] = -db_[e] * cc[e];
                                     }
                                     {
                                         float cc[16];
-                                        read_tile16(sm + OFF_C, m, G[sb], cc);
+                                        ca_load16(lane_addr + TM_CA + 8 * G[sb], cc);
 #pragma unroll
                                         for (int e = 0; e < 16; ++e) v[e] = fmaf(da_[e], cc[e], v[e]);
                                     }
@@ -796,7 +813,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     float v[16];
                                     {
                                         float cc[16];
-                                        read_tile16(sm + OFF_C, m, G[gsl], cc);
+                                        ca_load16(lane_addr + TM_CA + 8 * G[gsl], cc);
                                         const float(&d)[16] = sl ? db_ : da_;
 #pragma unroll
                                         for (int bq = 0; bq < 4; ++bq)
