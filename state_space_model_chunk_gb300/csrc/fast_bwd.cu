@@ -62,7 +62,8 @@ struct Ctl {
     uint64_t itemfull, itemdone;
     uint64_t afull[2], ascaled[2], aempty[2];  // forward-sweep span buffers
     uint64_t wfull[2], wfree[2];
-    uint64_t spanfull, spanfree;
+    uint64_t spanfull;
+    uint64_t slotfree[8];  // span slot j (xhat, bhat, rotation rows of one token) read for the last time
     uint64_t pafull, pafree, pfull, pfree;
     uint64_t cfull, cfree, dcfull, dcfree;
     uint64_t gfull, gfree, dxfull, dxfree;
@@ -76,6 +77,11 @@ static_assert(sizeof(Ctl) <= 512, "control block");
 // tensor memory columns; CA holds the c tile as bf16 pairs (row = lane), the A operand of the
 // d_c product, so the c tile needs no shared memory
 constexpr uint32_t TM_P = 0, TM_DC = 128, TM_AN = 256, TM_DX = 384, TM_DB = 400, TM_CA = 416, TM_COLS = 512;
+
+// Position of state element (row m, columns col .. col+3) in an anchor of the workspace: 16-byte
+// pieces ordered column-quad-major, so that the 32 rows of a warp touch 512 contiguous bytes
+// per access (each thread owns one row).
+__device__ __forceinline__ int64_t anchor_off(int m, int col) { return ((int64_t)(col >> 2) * 128 + m) * 4; }
 
 // c-tile row of one 16-column group in tensor memory: 16 bf16, two per 32-bit column
 __device__ __forceinline__ void ca_store16(uint32_t taddr, const float (&v)[16], bool zero) {
@@ -98,7 +104,7 @@ __device__ __forceinline__ void ca_load16(uint32_t taddr, float (&v)[16]) {
 struct BwdArgs {
     FastArgs F;         // problem, items, Hc (carries), Dn, err
     float* E;           // [b,h,nc,p,r]: e_n of every chunk
-    float* anchors;     // [grid][7][128][128] fp32 anchor slots
+    float* anchors;     // [grid][7] fp32 anchor slots of 128 x 128, laid out by anchor_off
     const float* dm2;   // [b,h,r,r]
     const float* dm1;   // [b,h,r]
     __nv_bfloat16* dx;  // d_xhat
@@ -223,7 +229,7 @@ struct Par {
 // bit positions
 enum : uint32_t {
     B_W = 4,                          // 2 W buffers
-    B_ITEM = 6, B_SPAN, B_PA, B_P, B_C, B_DC, B_G, B_DX, B_ITEMDONE, B_SPANFREE,
+    B_ITEM = 6, B_SPAN, B_PA, B_P, B_C, B_DC, B_G, B_DX, B_ITEMDONE,
     U_PRE = 24, U_DC, U_DX, U_PA, U_C, U_G, U_SPAN
 };
 template <int ROTK, int LAYB>
@@ -255,7 +261,7 @@ __global__ void __launch_bounds__(NTHR, 1)
             tc::mbar_init(&ctl->wfree[i], NCW);
         }
         tc::mbar_init(&ctl->spanfull, 1);
-        tc::mbar_init(&ctl->spanfree, 1 + NCW);
+        for (int j = 0; j < SPAN; ++j) tc::mbar_init(&ctl->slotfree[j], 1);
         tc::mbar_init(&ctl->pafull, NCW);
         tc::mbar_init(&ctl->pafree, 1);
         tc::mbar_init(&ctl->pfull, 1);
@@ -290,6 +296,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         // ====================================================================== TMA producer
         if (lane == 0) {
             uint32_t na0 = 0, na1 = 0;  // forward-sweep uses of the two span buffers
+            uint32_t slots = 0;         // per slot j: bit j = parity of its next release, bit 8 + j = release pending
             Par pr;
             bool ok = true;
             for (int it = it0; it < it1 && ok; ++it) {
@@ -330,16 +337,38 @@ __global__ void __launch_bounds__(NTHR, 1)
                 // the reverse sweep's first span goes into buffer 0 once the forward sweep is done with it
                 if (ok && na0 >= 1) ok &= tc::mbar_wait(&ctl->aempty[0], (na0 - 1) & 1, abort);
                 if (ok) {
+                    // Span slots refill one by one: the reverse sweep reads slot j for the last time in
+                    // the d_xhat / d_bhat product of token s0 + j, so the high slots of the next span
+                    // load while the current span still runs on the low ones.
                     const int nsp = (I.T[0] + SPAN - 1) / SPAN;
                     for (int sg = nsp - 1; sg >= 0 && ok; --sg) {
-                        if (pr.once(U_SPAN)) ok &= tc::mbar_wait(&ctl->spanfree, pr.next(B_SPANFREE), abort);
-                        if (!ok) break;
                         const int s0 = sg * SPAN, len = min(SPAN, I.T[0] - s0);
+                        auto slot_wait = [&](int jj) {
+                            if ((slots >> (8 + jj)) & 1u) {
+                                ok &= tc::mbar_wait(&ctl->slotfree[jj], (slots >> jj) & 1u, abort);
+                                slots ^= (1u << jj) | (1u << (8 + jj));
+                            }
+                        };
+                        slot_wait(len - 1);
+                        // the previous span's copies must have landed before the barrier is re-armed
+                        if (pr.once(U_SPAN)) ok &= tc::mbar_wait(&ctl->spanfull, pr.next(B_SPAN), abort);
+                        if (!ok) break;
+                        // the anchor state this span starts from, into L2 ahead of the span set-up
+                        if (sg > 0)
+                            tc::prefetch_l2(B.anchors + ((int64_t)blockIdx.x * NANCHOR + (sg - 1)) * 128 * 128,
+                                            128u * 128u * 4u);
+                        else
+                            for (int ch = 0; ch < 2; ++ch)
+                                if (I.exists[ch])
+                                    tc::prefetch_l2(A.Hc + off_carry(P, I.bb, I.hh, 2 * I.k + ch),
+                                                    (uint32_t)(P.p * P.r) * 4u);
                         uint32_t by = 0;
                         for (int ch = 0; ch < 2; ++ch)
                             if (I.exists[ch]) by += (uint32_t)len * (stage_tx + 4u * P.rw);
                         tc::mbar_arrive_expect_tx(&ctl->spanfull, by);
-                        for (int jj = 0; jj < len; ++jj)
+                        for (int jj = len - 1; jj >= 0; --jj) {
+                            slot_wait(jj);
+                            slots |= 1u << (8 + jj);
                             for (int ch = 0; ch < 2; ++ch) {
                                 if (!I.exists[ch]) continue;
                                 const int row = I.bb * P.s + (2 * I.k + ch) * FL + s0 + jj;
@@ -352,6 +381,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     tc::tma_load_3d(sm + OFF_ROT + jj * 1024 + ch * 512, &tmr, 0, I.hh, row,
                                                     &ctl->spanfull);
                             }
+                        }
                     }
                 }
             }
@@ -443,11 +473,13 @@ __global__ void __launch_bounds__(NTHR, 1)
                         const int len = min(SPAN, I.T[0] - sg * SPAN);
                         // pipelined order, matching the compute warps' signals
                         for (int u = len + 1; u >= 0 && ok; --u) {
-                            if (u <= len - 1) ok = issue_dx(s_sx + u * 4096u, s_sb + u * 4096u);
+                            if (u <= len - 1) {
+                                ok = issue_dx(s_sx + u * 4096u, s_sb + u * 4096u);
+                                tc::mma_commit(&ctl->slotfree[u]);
+                            }
                             if (ok && u - 1 >= 0 && u - 1 <= len - 1) ok = issue_dc();
                             if (ok && u - 2 >= 0) ok = issue_prefix(u - 2);
                         }
-                        if (ok) tc::mma_commit(&ctl->spanfree);
                     }
                 }
             }
@@ -592,12 +624,12 @@ __global__ void __launch_bounds__(NTHR, 1)
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&ctl->wfree[wb]);
                         ++nw;
-                        float* dst = myanchors + ((int64_t)k * 128 + m) * 128;
+                        float* dst = myanchors + (int64_t)k * 128 * 128;
 #pragma unroll
                         for (int g = 0; g < 4; ++g)
 #pragma unroll
                             for (int e = 0; e < 16; e += 4)
-                                *reinterpret_cast<float4*>(dst + 16 * G[g] + e) =
+                                *reinterpret_cast<float4*>(dst + anchor_off(m, 16 * G[g] + e)) =
                                     make_float4(S[g][e], S[g][e + 1], S[g][e + 2], S[g][e + 3]);
                     }
                 }
@@ -617,13 +649,15 @@ __global__ void __launch_bounds__(NTHR, 1)
                     for (int g = 0; g < 4; ++g) {
                         float av[16];
                         const int col0 = 16 * G[g];
-                        const float* src = sg == 0 ? (A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R)
-                                                   : (myanchors + ((int64_t)(sg - 1) * 128 + m) * 128);
+                        const float* carry = A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
+                        const float* anc = myanchors + (int64_t)(sg - 1) * 128 * 128;
                         const bool have = sg == 0 ? (Tch > 0 && col0 < R) : true;
 #pragma unroll
                         for (int e = 0; e < 16; e += 4) {
                             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (have) v = *reinterpret_cast<const float4*>(src + col0 + e);
+                            if (have)
+                                v = *reinterpret_cast<const float4*>(sg == 0 ? carry + col0 + e
+                                                                           : anc + anchor_off(m, col0 + e));
                             av[e] = v.x; av[e + 1] = v.y; av[e + 2] = v.z; av[e + 3] = v.w;
                         }
                         tc::tmem_st16(lane_addr + TM_AN + col0, av);
@@ -892,8 +926,6 @@ __global__ void __launch_bounds__(NTHR, 1)
                         if (u - 2 >= s0) build_pa(u - 2);
                         if (u <= thi) step_out(u);
                     }
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&ctl->spanfree);
                 }
                 // ---- chunk start: d_da_0 = e_0 <g_0, h_->, e_n = e_0 g_0 (anchor 0 = the carry)
                 {
