@@ -294,16 +294,23 @@ __global__ void __launch_bounds__(NTHR, 1)
 
     if (warp == WARP_TMA) {
         // ====================================================================== TMA producer
-        if (lane == 0) {
-            uint32_t na0 = 0, na1 = 0;  // forward-sweep uses of the two span buffers
-            uint32_t slots = 0;         // per slot j: bit j = parity of its next release, bit 8 + j = release pending
-            Par pr;
-            bool ok = true;
-            for (int it = it0; it < it1 && ok; ++it) {
-                const Item I = decode_item(A, it);
-                if (it > it0) ok &= tc::mbar_wait(&ctl->itemdone, pr.next(B_ITEMDONE), abort);
-                if (!ok) break;
-                // the item's da: 64 tokens x 4 heads per existing chunk
+        // The whole warp runs the loop: lane 0 arms the barriers, and the copies of a span or slot
+        // are dealt out across the lanes (one copy issue costs a thread ~100 cycles).  Wait results
+        // are made warp-uniform so that all lanes leave together.
+        uint32_t na0 = 0, na1 = 0;  // forward-sweep uses of the two span buffers
+        uint32_t slots = 0;         // per slot j: bit j = parity of its next release, bit 8 + j = release pending
+        Par pr;
+        bool ok = true;
+        const int nbx = 1 + R / 64;  // copies per token and chunk: xhat rows, bhat column blocks
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+            ok = __all_sync(0xffffffffu, ok && tc::mbar_wait(bar, parity, abort));
+        };
+        for (int it = it0; it < it1 && ok; ++it) {
+            const Item I = decode_item(A, it);
+            if (it > it0) wait_all(&ctl->itemdone, pr.next(B_ITEMDONE));
+            if (!ok) break;
+            // the item's da: 64 tokens x 4 heads per existing chunk
+            if (lane == 0) {
                 uint32_t bytes = 0;
                 for (int ch = 0; ch < 2; ++ch) bytes += I.exists[ch] ? 1024u : 0u;
                 tc::mbar_arrive_expect_tx(&ctl->itemfull, bytes);
@@ -311,48 +318,55 @@ __global__ void __launch_bounds__(NTHR, 1)
                     if (I.exists[ch])
                         tc::tma_load_2d(sm + OFF_IDA + ch * 1024, &tmd, I.hh & ~3, I.bb * P.s + (2 * I.k + ch) * FL,
                                         &ctl->itemfull);
-                // forward sweep: spans 0 .. nsp-2 alternate between the two span buffers (the last
-                // one in buffer 1, so that buffer 0 frees up first for the reverse sweep)
-                const int nA = (I.T[0] + SPAN - 1) / SPAN - 1;
-                for (int k = 0; k < nA && ok; ++k) {
-                    const int b = ((nA - 1 - k) & 1) ^ 1;
-                    if ((b ? na1 : na0) >= 1) ok &= tc::mbar_wait(&ctl->aempty[b], ((b ? na1 : na0) - 1) & 1, abort);
-                    if (!ok) break;
+            }
+            // forward sweep: spans 0 .. nsp-2 alternate between the two span buffers (the last
+            // one in buffer 1, so that buffer 0 frees up first for the reverse sweep)
+            const int nA = (I.T[0] + SPAN - 1) / SPAN - 1;
+            for (int k = 0; k < nA && ok; ++k) {
+                const int b = ((nA - 1 - k) & 1) ^ 1;
+                if ((b ? na1 : na0) >= 1) wait_all(&ctl->aempty[b], ((b ? na1 : na0) - 1) & 1);
+                if (!ok) break;
+                if (lane == 0) {
                     uint32_t by = 0;
                     for (int ch = 0; ch < 2; ++ch) by += I.exists[ch] ? SPAN * stage_tx : 0u;
                     tc::mbar_arrive_expect_tx(&ctl->afull[b], by);
-                    unsigned char* xb = sm + (b ? OFF_PA : OFF_SX);
-                    unsigned char* bt = sm + (b ? OFF_G : OFF_SB);
-                    for (int jj = 0; jj < SPAN; ++jj)
-                        for (int ch = 0; ch < 2; ++ch) {
-                            if (!I.exists[ch]) continue;
-                            const int row = I.bb * P.s + (2 * I.k + ch) * FL + k * SPAN + jj;
-                            tc::tma_load_4d(xb + jj * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row, &ctl->afull[b]);
-                            for (int a = 0; a < R / 64; ++a)
-                                tc::tma_load_5d(bt + jj * 4096 + a * 2048 + ch * 1024, &tmb, 0, a, I.hh, 0, row,
-                                                &ctl->afull[b]);
-                        }
-                    if (b) ++na1; else ++na0;
                 }
-                // the reverse sweep's first span goes into buffer 0 once the forward sweep is done with it
-                if (ok && na0 >= 1) ok &= tc::mbar_wait(&ctl->aempty[0], (na0 - 1) & 1, abort);
-                if (ok) {
-                    // Span slots refill one by one: the reverse sweep reads slot j for the last time in
-                    // the d_xhat / d_bhat product of token s0 + j, so the high slots of the next span
-                    // load while the current span still runs on the low ones.
-                    const int nsp = (I.T[0] + SPAN - 1) / SPAN;
-                    for (int sg = nsp - 1; sg >= 0 && ok; --sg) {
-                        const int s0 = sg * SPAN, len = min(SPAN, I.T[0] - s0);
-                        auto slot_wait = [&](int jj) {
-                            if ((slots >> (8 + jj)) & 1u) {
-                                ok &= tc::mbar_wait(&ctl->slotfree[jj], (slots >> jj) & 1u, abort);
-                                slots ^= (1u << jj) | (1u << (8 + jj));
-                            }
-                        };
-                        slot_wait(len - 1);
-                        // the previous span's copies must have landed before the barrier is re-armed
-                        if (pr.once(U_SPAN)) ok &= tc::mbar_wait(&ctl->spanfull, pr.next(B_SPAN), abort);
-                        if (!ok) break;
+                __syncwarp();
+                unsigned char* xb = sm + (b ? OFF_PA : OFF_SX);
+                unsigned char* bt = sm + (b ? OFF_G : OFF_SB);
+                for (int i = lane; i < SPAN * 2 * nbx; i += 32) {
+                    const int jj = i / (2 * nbx), ch = (i / nbx) & 1, kind = i % nbx;
+                    if (!I.exists[ch]) continue;
+                    const int row = I.bb * P.s + (2 * I.k + ch) * FL + k * SPAN + jj;
+                    if (kind == 0)
+                        tc::tma_load_4d(xb + jj * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row, &ctl->afull[b]);
+                    else
+                        tc::tma_load_5d(bt + jj * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 0, kind - 1, I.hh, 0,
+                                        row, &ctl->afull[b]);
+                }
+                if (b) ++na1; else ++na0;
+            }
+            // the reverse sweep's first span goes into buffer 0 once the forward sweep is done with it
+            if (ok && na0 >= 1) wait_all(&ctl->aempty[0], (na0 - 1) & 1);
+            if (ok) {
+                // Span slots refill one by one: the reverse sweep reads slot j for the last time in
+                // the d_xhat / d_bhat product of token s0 + j, so the high slots of the next span
+                // load while the current span still runs on the low ones.
+                const int nsp = (I.T[0] + SPAN - 1) / SPAN;
+                const int ncp = nbx + (P.rw ? 1 : 0);  // copies per token and chunk
+                for (int sg = nsp - 1; sg >= 0 && ok; --sg) {
+                    const int s0 = sg * SPAN, len = min(SPAN, I.T[0] - s0);
+                    auto slot_wait = [&](int jj) {
+                        if ((slots >> (8 + jj)) & 1u) {
+                            wait_all(&ctl->slotfree[jj], (slots >> jj) & 1u);
+                            slots ^= (1u << jj) | (1u << (8 + jj));
+                        }
+                    };
+                    slot_wait(len - 1);
+                    // the previous span's copies must have landed before the barrier is re-armed
+                    if (pr.once(U_SPAN)) wait_all(&ctl->spanfull, pr.next(B_SPAN));
+                    if (!ok) break;
+                    if (lane == 0) {
                         // the anchor state this span starts from, into L2 ahead of the span set-up
                         if (sg > 0)
                             tc::prefetch_l2(B.anchors + ((int64_t)blockIdx.x * NANCHOR + (sg - 1)) * 128 * 128,
@@ -366,18 +380,23 @@ __global__ void __launch_bounds__(NTHR, 1)
                         for (int ch = 0; ch < 2; ++ch)
                             if (I.exists[ch]) by += (uint32_t)len * (stage_tx + 4u * P.rw);
                         tc::mbar_arrive_expect_tx(&ctl->spanfull, by);
-                        for (int jj = len - 1; jj >= 0; --jj) {
-                            slot_wait(jj);
-                            slots |= 1u << (8 + jj);
-                            for (int ch = 0; ch < 2; ++ch) {
-                                if (!I.exists[ch]) continue;
+                    }
+                    __syncwarp();
+                    for (int jj = len - 1; jj >= 0 && ok; --jj) {
+                        slot_wait(jj);
+                        if (!ok) break;
+                        slots |= 1u << (8 + jj);
+                        if (lane < 2 * ncp) {
+                            const int ch = lane / ncp, kind = lane % ncp;
+                            if (I.exists[ch]) {
                                 const int row = I.bb * P.s + (2 * I.k + ch) * FL + s0 + jj;
-                                tc::tma_load_4d(sm + OFF_SX + jj * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row,
-                                                &ctl->spanfull);
-                                for (int a = 0; a < R / 64; ++a)
-                                    tc::tma_load_5d(sm + OFF_SB + jj * 4096 + a * 2048 + ch * 1024, &tmb, 0, a, I.hh,
-                                                    0, row, &ctl->spanfull);
-                                if (P.rw)
+                                if (kind == 0)
+                                    tc::tma_load_4d(sm + OFF_SX + jj * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row,
+                                                    &ctl->spanfull);
+                                else if (kind < nbx)
+                                    tc::tma_load_5d(sm + OFF_SB + jj * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 0,
+                                                    kind - 1, I.hh, 0, row, &ctl->spanfull);
+                                else
                                     tc::tma_load_3d(sm + OFF_ROT + jj * 1024 + ch * 512, &tmr, 0, I.hh, row,
                                                     &ctl->spanfull);
                             }
@@ -385,8 +404,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                     }
                 }
             }
-            if (!ok) fail(ctl, A.err, 21);
         }
+        if (!ok && lane == 0) fail(ctl, A.err, 21);
     } else if (warp == WARP_MMA) {
         // ====================================================================== MMA issuer
         if (lane == 0) {
