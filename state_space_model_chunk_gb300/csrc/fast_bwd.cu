@@ -52,7 +52,8 @@ constexpr uint32_t OFF_ACUM = 174080;            // cumulative da, 2 chunks x 64
 constexpr uint32_t OFF_COEF = 174592;            // span cos|sin: 8 tokens x 2 chunks x 128 fp32
 constexpr uint32_t OFF_LT = 182784;              // span decay matrix L: 2 chunks x 8 x 8 fp32
 constexpr uint32_t OFF_M1 = 183296;              // d_m1 [128] fp32
-constexpr uint32_t OFF_CTL = 184448;
+constexpr uint32_t OFF_PTR = 184448;             // per compute thread: 4 output row pointers of the item
+constexpr uint32_t OFF_CTL = 192640;
 constexpr uint32_t SMEM_BYTES = OFF_CTL + 512 + 1024;
 static_assert(OFF_SX % 1024 == 0 && OFF_SB % 1024 == 0 && OFF_PA % 1024 == 0, "tiles");
 static_assert(OFF_ROT % 128 == 0 && OFF_IDA % 128 == 0 && OFF_CTL % 8 == 0, "tensor-copy slots");
@@ -531,6 +532,18 @@ __global__ void __launch_bounds__(NTHR, 1)
             const int n = 2 * I.k + ch;
             const bool chunk_ok = ch ? I.exists[1] : I.exists[0];
             const bool half_ok = half ? I.exists[1] : I.exists[0];
+            // this thread's output rows for token 0 of the item (null where it writes none): the
+            // per-token steps only add the token stride
+            uint64_t* ptab = reinterpret_cast<uint64_t*>(sm + OFF_PTR) + ctid * 4;
+            ptab[0] = (half == 0 && chunk_ok) ? reinterpret_cast<uint64_t>(B.dx + off_x(P, I.bb, n * FL, 0, I.hh) + pp)
+                                              : 0ull;
+            ptab[1] = (m < R && half_ok)
+                          ? reinterpret_cast<uint64_t>(B.db + off_b(P, I.bb, (2 * I.k + half) * FL, 0, I.hh) + m)
+                          : 0ull;
+            ptab[2] = reinterpret_cast<uint64_t>(B.dda + off_da(P, I.bb, n * FL, I.hh));
+            ptab[3] = (P.rw > 0 && chunk_ok && n < I.proc)
+                          ? reinterpret_cast<uint64_t>(B.drot + off_rot(P, I.bb, n * FL, I.hh))
+                          : 0ull;
             ok &= tc::mbar_wait(&ctl->itemfull, pr.next(B_ITEM), abort);
             // ---- item set-up: cumulative da of both chunks; D + D^T and d_m1 when (b,h) changes
             if (warp < 2) {
@@ -769,7 +782,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         // d_da_{t+1} = e_{t+1} <g_{t+1}, h_t>  (g holds g_{t+1} here)
                         const float dot = warp_sum((dotv[0] + dotv[1]) + (dotv[2] + dotv[3]));
                         if (lane == 0 && t + 1 < I.T[0] && chunk_ok && n < I.proc)
-                            atomicAdd(B.dda + off_da(P, I.bb, n * FL + t + 1, I.hh), e_of(t + 1) * dot);
+                            atomicAdd(reinterpret_cast<float*>(ptab[2]) + (int64_t)(t + 1) * P.h, e_of(t + 1) * dot);
                     };
                     // ---- d_c -> d_rot, G, cotangent recurrence -> g tile
                     auto step_g = [&](int t) {
@@ -779,8 +792,9 @@ __global__ void __launch_bounds__(NTHR, 1)
                         const bool live = t < Tch;
                         const float* cf = coefs + (o * 2 + ch) * 128;
                         const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + ch * 512);
-                        const int64_t orot = off_rot(P, I.bb, n * FL + t, I.hh);
-                        const bool rot_out = P.rw > 0 && chunk_ok && n < I.proc;
+                        float* const drot_t = ptab[3] ? reinterpret_cast<float*>(ptab[3]) + (int64_t)t * P.h * P.rw
+                                                      : nullptr;
+                        const bool rot_out = drot_t != nullptr;
                         if (!live) {  // past valid_len: d_c = 0, so g_t = e_{t+1} g_{t+1}
                             tc::tc_fence_before();
                             __syncwarp();
@@ -825,7 +839,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     }
                                     transpose_reduce16(v, lane);
                                     const int ang = 8 * ((lane & 8) ? G[sb] : G[sa]) + (lane & 7);
-                                    if (lane < 16 && ang < P.na && rot_out) atomicAdd(B.drot + orot + ang, v[0]);
+                                    if (lane < 16 && ang < P.na && rot_out) atomicAdd(drot_t + ang, v[0]);
                                 } else if (act_a) {
                                     float v[8];
                                     {
@@ -836,7 +850,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     }
                                     transpose_reduce8(v, lane);
                                     const int ang = 8 * G[sa] + (lane & 7);
-                                    if (lane < 8 && ang < P.na && rot_out) atomicAdd(B.drot + orot + ang, v[0]);
+                                    if (lane < 8 && ang < P.na && rot_out) atomicAdd(drot_t + ang, v[0]);
                                 }
                             } else if (ROTK == ROT_HALF) {
                                 if (!(LAYB && pass == 1) && act_a) {
@@ -855,7 +869,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     }
                                     transpose_reduce16(v, lane);
                                     const int ang = 16 * G[sa] + (lane & 15);
-                                    if (lane < 16 && ang < P.na && rot_out) atomicAdd(B.drot + orot + ang, v[0]);
+                                    if (lane < 16 && ang < P.na && rot_out) atomicAdd(drot_t + ang, v[0]);
                                 }
                             } else if (ROTK == ROT_QUAT) {
                                 // sum_p d_c (x) conj(c) per 4-block, then (.) (x) Q / |Q|^2
@@ -888,7 +902,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                         hamilton(s0q, s1q, s2q, s3q, Q[0], Q[1], Q[2], Q[3], o0, o1, o2, o3);
                                         const float inv = 1.f / (Q[0] * Q[0] + Q[1] * Q[1] + Q[2] * Q[2] + Q[3] * Q[3]);
                                         const float val = comp == 0 ? o0 : comp == 1 ? o1 : comp == 2 ? o2 : o3;
-                                        atomicAdd(B.drot + orot + 4 * blk + comp, inv * val);
+                                        atomicAdd(drot_t + 4 * blk + comp, inv * val);
                                     }
                                 }
                             }
@@ -923,17 +937,18 @@ __global__ void __launch_bounds__(NTHR, 1)
                         tc::tc_fence_before();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&ctl->dxfree);
-                        if (half == 0 && chunk_ok) {
-                            const int tok = n * FL + t;
+                        const int64_t hp = (int64_t)P.h * P.p, hr = (int64_t)P.h * P.r;
+                        if (ptab[0]) {
+                            __nv_bfloat16* px = reinterpret_cast<__nv_bfloat16*>(ptab[0]) + (int64_t)t * C * hp;
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                if (c < C) B.dx[off_x(P, I.bb, tok, c, I.hh) + pp] = __float2bfloat16_rn(v[c]);
+                                if (c < C) px[c * hp] = __float2bfloat16_rn(v[c]);
                         }
-                        if (m < R && half_ok) {
-                            const int tok = (2 * I.k + half) * FL + t;
+                        if (ptab[1]) {
+                            __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(ptab[1]) + (int64_t)t * C * hr;
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                if (c < C) B.db[off_b(P, I.bb, tok, c, I.hh) + m] = __float2bfloat16_rn(u[c]);
+                                if (c < C) pb[c * hr] = __float2bfloat16_rn(u[c]);
                         }
                     };
 
