@@ -609,7 +609,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                     // tensor core forms the sum from xhat rows scaled in place by L = exp(a_end - a_j);
                     // the state after the span is anchor k
                     const int nA = (I.T[0] + SPAN - 1) / SPAN - 1;
-                    for (int k = 0; k < nA; ++k) {
+                    // scale span k's xhat rows in place and hand them to the tensor core
+                    auto scale_span = [&](int k) {
                         const int b = ((nA - 1 - k) & 1) ^ 1;
                         ok &= tc::mbar_wait(&ctl->afull[b], (b ? na1 : na0) & 1, abort);
                         unsigned char* xb = sm + (b ? OFF_PA : OFF_SX);
@@ -635,6 +636,11 @@ __global__ void __launch_bounds__(NTHR, 1)
                             tc::mbar_arrive(&ctl->aempty[b]);
                         }
                         if (b) ++na1; else ++na0;
+                    };
+                    // the next span is scaled before this span's anchor goes out, so that the
+                    // anchor stores drain while the tensor core works on the next span
+                    if (nA > 0) scale_span(0);
+                    for (int k = 0; k < nA; ++k) {
                         const uint32_t wb = nw & 1;
                         ok &= tc::mbar_wait(&ctl->wfull[wb], pr.next(B_W + wb), abort);
                         tc::tc_fence_after();
@@ -656,6 +662,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&ctl->wfree[wb]);
                         ++nw;
+                        if (k + 1 < nA) scale_span(k + 1);
                         float* dst = myanchors + (int64_t)k * 128 * 128;
 #pragma unroll
                         for (int g = 0; g < 4; ++g)
