@@ -51,11 +51,11 @@ constexpr uint32_t OFF_IDA = 172032;             // item da: 2 chunks x 64 token
 constexpr uint32_t OFF_ACUM = 174080;            // cumulative da, 2 chunks x 64 fp32
 constexpr uint32_t OFF_COEF = 174592;            // span cos|sin: 8 tokens x 2 chunks x 128 fp32
 constexpr uint32_t OFF_LT = 182784;              // span decay matrix L: 2 chunks x 8 x 8 fp32
-constexpr uint32_t OFF_M1 = 183296;              // d_m1 [128] fp32
-constexpr uint32_t OFF_PTR = 184448;             // per compute thread: 4 output row pointers of the item
-constexpr uint32_t OFF_CTL = 192640;
+constexpr uint32_t OFF_M1T = 184320;             // d_m1 as a K = 16 MMA operand: rows hi | lo (bf16) | 0
+constexpr uint32_t OFF_PTR = 188416;             // per compute thread: 4 output row pointers of the item
+constexpr uint32_t OFF_CTL = 196608;
 constexpr uint32_t SMEM_BYTES = OFF_CTL + 512 + 1024;
-static_assert(OFF_SX % 1024 == 0 && OFF_SB % 1024 == 0 && OFF_PA % 1024 == 0, "tiles");
+static_assert(OFF_SX % 1024 == 0 && OFF_SB % 1024 == 0 && OFF_PA % 1024 == 0 && OFF_M1T % 1024 == 0, "tiles");
 static_assert(OFF_ROT % 128 == 0 && OFF_IDA % 128 == 0 && OFF_CTL % 8 == 0, "tensor-copy slots");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -76,8 +76,10 @@ struct Ctl {
 static_assert(sizeof(Ctl) <= 512, "control block");
 
 // tensor memory columns; CA holds the c tile as bf16 pairs (row = lane), the A operand of the
-// d_c product, so the c tile needs no shared memory
-constexpr uint32_t TM_P = 0, TM_DC = 128, TM_AN = 256, TM_DX = 384, TM_DB = 400, TM_CA = 416, TM_COLS = 512;
+// d_c product, so the c tile needs no shared memory; ONE is a K = 16 A operand whose first two
+// columns are 1, so that one more step of that product adds d_m1 (hi + lo) to every row
+constexpr uint32_t TM_P = 0, TM_DC = 128, TM_AN = 256, TM_DX = 384, TM_DB = 400, TM_CA = 416, TM_ONE = 480,
+                   TM_COLS = 512;
 
 // Position of state element (row m, columns col .. col+3) in an anchor of the workspace: 16-byte
 // pieces ordered column-quad-major, so that the 32 rows of a warp touch 512 contiguous bytes
@@ -416,6 +418,8 @@ __global__ void __launch_bounds__(NTHR, 1)
             const uint32_t idDX = tc::idesc_bf16(128, 16, 0, 0);
             const uint32_t idDB = tc::idesc_bf16(128, 16, 1, 0);
             const uint32_t s_g = tc::smem_u32(sm + OFF_G), s_ds = tc::smem_u32(sm + OFF_DS);
+            const uint32_t s_m1t = tc::smem_u32(sm + OFF_M1T);
+            const uint32_t idM1 = tc::idesc_bf16(128, 128, 0, 1);
             const uint32_t s_sx = tc::smem_u32(sm + OFF_SX), s_sb = tc::smem_u32(sm + OFF_SB);
             const uint32_t s_pa = tc::smem_u32(sm + OFF_PA);
             Par pr;
@@ -463,6 +467,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     tc::mma_bf16_ta(tbase + TM_DC, tbase + TM_CA + 8u * ks, tc::sdesc_sw128(s_ds + koff, 16, 1024), idDC,
                                     ks > 0);
                 }
+                tc::mma_bf16_ta(tbase + TM_DC, tbase + TM_ONE, tc::sdesc_sw128(s_m1t, 2048, 1024), idM1, 1u);
                 tc::mma_commit(&ctl->dcfull);
                 tc::mma_commit(&ctl->cfree);
                 return true;
@@ -519,10 +524,14 @@ __global__ void __launch_bounds__(NTHR, 1)
         const uint32_t lane_addr = tbase + ((uint32_t)((warp & 3) * 32) << 16);
         float* acum = reinterpret_cast<float*>(sm + OFF_ACUM);            // [2][64] inclusive cumsum of da
         const float* ida = reinterpret_cast<const float*>(sm + OFF_IDA);  // [2][64][4]
-        const float* m1s = reinterpret_cast<const float*>(sm + OFF_M1);
         float* coefs = reinterpret_cast<float*>(sm + OFF_COEF);           // [8][2][128]
         float* Lt = reinterpret_cast<float*>(sm + OFF_LT);                // [2][8][8]
         float* myanchors = B.anchors + (int64_t)blockIdx.x * NANCHOR * 128 * 128;
+        if (warp < 4) {  // the constant ONE operand: elements 0 and 1 of each row are 1
+            uint32_t one[8] = {tc::pack_bf16x2(1.f, 1.f), 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            tc::tmem_st8u(lane_addr + TM_ONE, one);
+            tc::tmem_wait_st();
+        }
         Par pr;
         uint32_t na0 = 0, na1 = 0, nw = 0;
         bool ok = true;
@@ -571,9 +580,20 @@ __global__ void __launch_bounds__(NTHR, 1)
                     }
                     *reinterpret_cast<uint32_t*>(ds + tc::sw128_offset(128, r2, r1)) = tc::pack_bf16x2(a0, a1);
                 }
-                float* m1w = reinterpret_cast<float*>(sm + OFF_M1);
-                for (int i = ctid; i < 128; i += NCW * 32)
-                    m1w[i] = i < R ? B.dm1[((int64_t)I.bb * P.h + I.hh) * R + i] : 0.f;
+                // d_m1 split into bf16 hi + lo rows of the K = 16 operand (rows 2..15 zero)
+                const float* dm1 = B.dm1 + ((int64_t)I.bb * P.h + I.hh) * R;
+                for (int i = ctid; i < 16 * 128 / 2; i += NCW * 32) {
+                    const int k = i >> 6, nn = (i & 63) * 2;
+                    float v0 = 0.f, v1 = 0.f;
+                    if (k < 2) {
+                        const float m0 = nn < R ? dm1[nn] : 0.f, m1v = nn + 1 < R ? dm1[nn + 1] : 0.f;
+                        const float h0 = __bfloat162float(__float2bfloat16_rn(m0));
+                        const float h1 = __bfloat162float(__float2bfloat16_rn(m1v));
+                        v0 = k == 0 ? h0 : m0 - h0;
+                        v1 = k == 0 ? h1 : m1v - h1;
+                    }
+                    *reinterpret_cast<uint32_t*>(sm + OFF_M1T + tc::sw128_offset(16, k, nn)) = tc::pack_bf16x2(v0, v1);
+                }
                 tc::fence_proxy_async_smem();
             }
             named_barrier_sync(1, NCW * 32);
@@ -818,14 +838,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                             float da_[16], db_[16];
                             tc::tmem_ld16(lane_addr + TM_DC + 16 * G[sa], da_);
                             tc::tmem_ld16(lane_addr + TM_DC + 16 * G[sb], db_);
-                            tc::tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 16; e += 4) {
-                                const float4 ma = *reinterpret_cast<const float4*>(m1s + 16 * G[sa] + e);
-                                const float4 mb = *reinterpret_cast<const float4*>(m1s + 16 * G[sb] + e);
-                                da_[e] += ma.x; da_[e + 1] += ma.y; da_[e + 2] += ma.z; da_[e + 3] += ma.w;
-                                db_[e] += mb.x; db_[e + 1] += mb.y; db_[e + 2] += mb.z; db_[e + 3] += mb.w;
-                            }
+                            tc::tmem_wait_ld();  // d_c = DC: the product already added d_m1
                             // rotation-parameter gradient of the pass, summed over the warp's 32 rows
                             // by a transpose reduction (lane L then holds value L)
                             if (ROTK == ROT_PAIRWISE) {
