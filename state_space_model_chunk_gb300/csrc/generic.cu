@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(NT) k_chunk_end(MMParams P, const T* __restric
 // Each thread owns V consecutive elements of the p x r state (V = 4: float4 when p r % 4 == 0)
 // and reads the slots of SCAN_B chunks ahead before the dependent updates, so that a thread keeps
 // SCAN_B independent loads in flight.
-constexpr int SCAN_T = 256, SCAN_B = 8;
+constexpr int SCAN_T = 128, SCAN_B = 16;
 
 template <int V>
 struct Vec;
