@@ -11,10 +11,10 @@
 // Over the rows (t, c) of 32 tokens these are U = Bhat dH^T (M = 32 C, N = p, K = r) and
 // V = Xhat dH (M = 32 C, N = r, K = p).  One bf16 dH tile [p][r] in the 128-byte-swizzled layout
 // is the K-major B operand of the first and the MN-major B operand of the second; the xhat /
-// bhat rows come by TMA.  The epilogue (lanes = rows (t, c), two threads per row) scales, adds
+// bhat rows come by TMA.  The epilogue (lanes = rows (t, c), four threads per row) scales, adds
 // into d_xhat / d_bhat in place, and accumulates omega.
 //
-// Warp roles: 0 TMA, 1 MMA, 2-9 dH tile + epilogue.  Every wait is bounded; a timeout sets the
+// Warp roles: 0 TMA, 1 MMA, 2-17 dH tile + epilogue.  Every wait is bounded; a timeout sets the
 // workspace error word and the CTA winds down.
 #include <cuda.h>
 
@@ -28,8 +28,8 @@ namespace fastcorr {
 
 using namespace fastk;
 
-constexpr int NTHR = 320;
-constexpr int NEW = 8;                     // epilogue warps
+constexpr int NTHR = 576;
+constexpr int NEW = 16;                    // epilogue warps: four per TMEM lane quarter
 constexpr int TPS = 32;                    // tokens per stage (rows 32 C <= 128)
 constexpr int NS = 3;                      // stages
 constexpr uint32_t SLOT = 16384;           // 128 rows x 128 B
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     } else {
         // ================================================================ dH tile + epilogue
         const int ew = warp - 2, etid = tid - 64;
-        const int hf = ew >> 2;                     // which half of the row's columns
+        const int qf = ew >> 2;                     // which quarter of the row's columns
         const int k = ((warp & 3) << 5) + lane;     // TMEM lane = stage row (t, c)
         const uint32_t lane_addr = tbase + ((uint32_t)((warp & 3) * 32) << 16);
         float* sc = reinterpret_cast<float*>(sm + OFF_SC);
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const float* hin = A.Hc + off_carry(P, I.bb, I.hh, I.n);
                 float dot = 0.f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < 64 * 16 / (NEW * 32); ++i) {
                     const int id = i * (NEW * 32) + etid;
                     const int pp = id >> 4, j16 = id & 15, blk = j16 >> 3, j = j16 & 7;
                     const int col = 64 * blk + 8 * j;
@@ -283,34 +283,33 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const uint32_t s = q % NS, ab = q & 1;
                 const int t = st * TPS + tl;
                 const int tok = I.n * FL + t;
-                // this thread's part of the row: U columns [32 hf, 32 hf + 32), V columns [64 hf, 64 hf + 64)
-                const bool has_v = 64 * hf < R;
-                uint4 ox[4], ob[8];
-                __nv_bfloat16* px = B.dx + off_x(P, I.bb, tok, cc, I.hh) + 32 * hf;
-                __nv_bfloat16* pb = B.db + off_b(P, I.bb, tok, cc, I.hh) + 64 * hf;
+                // this thread's part of the row: U columns [16 qf, 16 qf + 16), V columns [32 qf, 32 qf + 32)
+                const bool has_v = 32 * qf < R;
+                uint4 ox[2], ob[4];
+                __nv_bfloat16* px = B.dx + off_x(P, I.bb, tok, cc, I.hh) + 16 * qf;
+                __nv_bfloat16* pb = B.db + off_b(P, I.bb, tok, cc, I.hh) + 32 * qf;
                 if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) ox[i] = reinterpret_cast<const uint4*>(px)[i];
+                    for (int i = 0; i < 2; ++i) ox[i] = reinterpret_cast<const uint4*>(px)[i];
                     if (has_v) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) ob[i] = reinterpret_cast<const uint4*>(pb)[i];
+                        for (int i = 0; i < 4; ++i) ob[i] = reinterpret_cast<const uint4*>(pb)[i];
                     }
                 }
                 check(tc::mbar_wait(&ctl->full[s], (q / NS) & 1, abort));  // the stage's xhat rows are read below
                 check(tc::mbar_wait(&ctl->accfull[ab], (q >> 1) & 1, abort));
                 tc::tc_fence_after();
                 const uint32_t tu = lane_addr + ab * TM_BUF, tv = tu + 64;
-                float u[32];
-                tc::tmem_ld16(tu + 32 * hf, *reinterpret_cast<float(*)[16]>(&u[0]));
-                tc::tmem_ld16(tu + 32 * hf + 16, *reinterpret_cast<float(*)[16]>(&u[16]));
+                float u[16];
+                tc::tmem_ld16(tu + 16 * qf, u);
                 tc::tmem_wait_ld();
-                // omega partial: <xhat row, U row> over this half (xhat row from the stage tile)
+                // omega partial: <xhat row, U row> over this quarter (xhat row from the stage tile)
                 float w = 0.f;
                 {
                     const unsigned char* xr = sm + s * STAGE + k * 128;
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int j = 4 * hf + jj;
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * qf + jj;
                         const uint4 v = *reinterpret_cast<const uint4*>(xr + ((j ^ (k & 7)) << 4));
                         const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -324,7 +323,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const float scv = sc[t];
                 if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < 2; ++i) {
                         uint32_t* wd = reinterpret_cast<uint32_t*>(&ox[i]);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -337,9 +336,9 @@ __global__ void __launch_bounds__(NTHR, 1)
                 }
                 if (has_v) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
+                    for (int g = 0; g < 2; ++g) {
                         float v[16];
-                        tc::tmem_ld16(tv + 64 * hf + 16 * g, v);
+                        tc::tmem_ld16(tv + 32 * qf + 16 * g, v);
                         tc::tmem_wait_ld();
                         if (row_ok) {
 #pragma unroll
