@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size (profiling runs)")
+    ap.add_argument("--recompute-carries", action="store_true",
+                    help="backward recomputes the chunk carries instead of taking the forward's")
     return ap.parse_args()
 
 
@@ -288,12 +290,16 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     vl = inp["valid_len"]
 
+    reuse = not args.recompute_carries
+
     def step(src):
+        # as the autograd function does: the forward writes its chunk carries into the backward's
+        # workspace and the backward takes them from there (MM_FLAG_REUSE_CARRIES)
         r_ = src["rot"] if rot is not None else None
-        binding.moments_fwd(spec, src["xhat"], src["bhat"], src["da"], r_, src["initial"], vl, workspace=ws_f,
-                            out=(m2, m1))
+        binding.moments_fwd(spec, src["xhat"], src["bhat"], src["da"], r_, src["initial"], vl,
+                            workspace=ws_b if reuse else ws_f, out=(m2, m1))
         binding.moments_bwd(spec, src["xhat"], src["bhat"], src["da"], r_, src["initial"], vl, src["d_m2"],
-                            src["d_m1"], workspace=ws_b, out=grads)
+                            src["d_m1"], workspace=ws_b, out=grads, reuse_carries=reuse)
 
     warm = max(args.warmup, 3)
     for _ in range(warm):
@@ -443,7 +449,9 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "path_fwd": "tcgen05" if binding.path(spec, False) == 1 else "simt",
                        "path_bwd": "tcgen05" if binding.path(spec, True) == 1 else "simt",
-                       "l2": "inputs larger than L2 (operands 1.7 GB), no flush"},
+                       "l2": "inputs larger than L2 (operands 1.7 GB), no flush",
+                       "carries": "recomputed by the backward" if args.recompute_carries
+                       else "forward's, reused by the backward"},
             "e2e": e2e, "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu, "clocks": clk,
             "kernels_ms_per_step": {k: v[0] / args.steps for k, v in kernels.items()},
             "step_tflops": step_tflops,

@@ -75,6 +75,13 @@ typedef enum {
 
 /* Kernel-path selection (mm_problem.flags). */
 #define MM_FLAG_FORCE_GENERIC 0x1u /* use the SIMT fp32 kernels even where the tensor-core path applies */
+/* moments_bwd only: the workspace holds the chunk carries that a moments_fwd call with the same
+ * problem and the same input tensors wrote into it (the caller sized that workspace with
+ * mm_workspace_bytes(prob, 1) and passed it to both calls, and changed none of the inputs in
+ * between).  The backward then skips recomputing the chunk-end contributions and the carry scan.
+ * The flag is ignored (the carries are recomputed) when the forward and the backward of the
+ * problem take different kernel paths (mm_path differs), whose carry layouts differ. */
+#define MM_FLAG_REUSE_CARRIES 0x2u
 
 typedef struct {
     int64_t b, s, C, h, p, r; /* batch, padded sequence, channels, heads, per-head dim, state rank */
@@ -98,7 +105,9 @@ mm_status moments_fwd(const mm_problem* prob, const void* xhat, const void* bhat
                       float* m2, float* m1, void* workspace, size_t ws_bytes, void* stream);
 
 /* Backward: the five input gradients for cotangents (d_m2, d_m1), recomputing every state
- * from the leaf inputs (nothing is saved by the forward).  d_m2 need not be symmetric.
+ * from the leaf inputs (nothing is saved by the forward; with MM_FLAG_REUSE_CARRIES the chunk
+ * carries, 1/chunk of the state trajectory, come from the forward's workspace instead).
+ * d_m2 need not be symmetric.
  * Source: "backward.rs", moments_phys_bwd, MomentsGrads, module header "Gradient math". */
 mm_status moments_bwd(const mm_problem* prob, const void* xhat, const void* bhat, const float* da,
                       const float* rot, const float* initial, const int64_t* valid_len_host,

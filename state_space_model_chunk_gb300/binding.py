@@ -25,6 +25,7 @@ from . import build as _build
 MM_F32, MM_BF16 = 0, 1
 ROT = {"none": 0, "pairwise": 1, "half": 2, "quat": 3}
 MM_FLAG_FORCE_GENERIC = 0x1
+MM_FLAG_REUSE_CARRIES = 0x2
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda", 5: "nonfinite",
           6: "timeout"}
 
@@ -93,10 +94,10 @@ class Spec:
     dtype: str = "bf16"
     force_generic: bool = False
 
-    def problem(self) -> Problem:
+    def problem(self, extra_flags: int = 0) -> Problem:
         return Problem(self.b, self.s, self.C, self.h, self.p, self.r, self.chunk_len,
                        MM_BF16 if self.dtype == "bf16" else MM_F32, ROT[self.rot], self.rope_dim,
-                       self.quat_blocks, MM_FLAG_FORCE_GENERIC if self.force_generic else 0, 0)
+                       self.quat_blocks, (MM_FLAG_FORCE_GENERIC if self.force_generic else 0) | extra_flags, 0)
 
     @staticmethod
     def from_tensors(xhat, bhat, chunk_len, rot="none", rope_dim=0, quat_blocks=0, force_generic=False):
@@ -160,8 +161,12 @@ def moments_fwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, *, workspac
 
 
 def moments_bwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, d_m2, d_m1, *, workspace=None,
-                stream=None, out=None):
-    """Backward call; returns dict d_xhat, d_bhat, d_da, d_rot, d_initial."""
+                stream=None, out=None, reuse_carries=False):
+    """Backward call; returns dict d_xhat, d_bhat, d_da, d_rot, d_initial.  ``reuse_carries``:
+    ``workspace`` (sized for the backward) went through :func:`moments_fwd` of the same spec and
+    unchanged inputs, whose chunk carries the backward then takes instead of recomputing them."""
+    if reuse_carries and workspace is None:
+        raise ValueError("reuse_carries needs the workspace the forward wrote")
     lib = load()
     _check_dev(xhat, bhat, da, rot, initial, d_m2, d_m1)
     dev = xhat.device
@@ -172,7 +177,8 @@ def moments_bwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, d_m2, d_m1,
     ws = workspace if workspace is not None else alloc_workspace(spec, True, dev)
     vh = _valid_host(valid_len, spec.b)
     st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
-    rc = lib.moments_bwd(ctypes.byref(spec.problem()), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot),
+    prob = spec.problem(MM_FLAG_REUSE_CARRIES if reuse_carries else 0)
+    rc = lib.moments_bwd(ctypes.byref(prob), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot),
                          _ptr(initial), ctypes.cast(vh.data_ptr(), ctypes.POINTER(ctypes.c_int64)),
                          _ptr(d_m2), _ptr(d_m1), _ptr(out["d_xhat"]), _ptr(out["d_bhat"]),
                          _ptr(out["d_da"]), _ptr(out["d_rot"]), _ptr(out["d_initial"]), _ptr(ws),
@@ -206,14 +212,17 @@ def moments_fwd_noalloc(spec: Spec, xhat, bhat, da, rot, initial, valid_len, *, 
 
 
 class Moments(torch.autograd.Function):
-    """(m2, m1) with the recompute backward: only the five leaf inputs are saved."""
+    """(m2, m1) with the recompute backward: the five leaf inputs are saved, and the forward's
+    workspace, whose chunk carries (1/chunk of the state trajectory) the backward reuses."""
 
     @staticmethod
     def forward(ctx, xhat, bhat, da, rot, initial, valid_len, spec):
-        m2, m1 = moments_fwd(spec, xhat, bhat, da, rot, initial, valid_len)
+        ws = alloc_workspace(spec, True, xhat.device)
+        m2, m1 = moments_fwd(spec, xhat, bhat, da, rot, initial, valid_len, workspace=ws)
         ctx.save_for_backward(xhat, bhat, da, rot, initial)
         ctx.valid_len = valid_len
         ctx.spec = spec
+        ctx.ws = ws
         return m2, m1
 
     @staticmethod
@@ -222,7 +231,9 @@ class Moments(torch.autograd.Function):
         sp = ctx.spec
         d_m2 = torch.zeros((sp.b, sp.h, sp.r, sp.r), device=xhat.device) if d_m2 is None else d_m2.contiguous()
         d_m1 = torch.zeros((sp.b, sp.h, sp.r), device=xhat.device) if d_m1 is None else d_m1.contiguous()
-        g = moments_bwd(ctx.spec, xhat, bhat, da, rot, initial, ctx.valid_len, d_m2, d_m1)
+        g = moments_bwd(ctx.spec, xhat, bhat, da, rot, initial, ctx.valid_len, d_m2, d_m1, workspace=ctx.ws,
+                        reuse_carries=True)
+        ctx.ws = None
         return g["d_xhat"], g["d_bhat"], g["d_da"], g["d_rot"], g["d_initial"], None, None
 
 

@@ -293,6 +293,8 @@ mm_status moments_bwd(const mm_problem* prob, const void* xhat, const void* bhat
     A.xhat = xhat; A.bhat = bhat; A.da = da; A.rot = rot; A.initial = initial;
     A.dm2 = d_m2; A.dm1 = d_m1; A.dxhat = d_xhat; A.dbhat = d_bhat; A.dda = d_da; A.drot = d_rot;
     A.dinit = d_initial;
+    // carries from the forward: only where both directions share the path (and so the layout)
+    A.reuse_carries = (prob->flags & MM_FLAG_REUSE_CARRIES) && use_fast(prob, M, 0) == fast;
     A.Hc = at<float>(workspace, L.Hc);
     A.Dn = at<float>(workspace, L.Dn);
     A.E = at<float>(workspace, L.E);

@@ -199,8 +199,10 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     TensorMaps maps;
     if ((e = encode_maps(P, A.xhat, A.bhat, A.rot, A.da, &maps)) != cudaSuccess) return e;
     int grid = fa.items < sm_count() ? fa.items : sm_count();
-    if ((e = launch_tc_end(fa, maps, st)) != cudaSuccess) return e;
-    if ((e = generic_carry_scan(P, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
+    if (!A.reuse_carries) {  // else the forward of the same problem left the carries in Hc / Dn
+        if ((e = launch_tc_end(fa, maps, st)) != cudaSuccess) return e;
+        if ((e = generic_carry_scan(P, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
+    }
     if (grid > kMaxBwdGrid) grid = kMaxBwdGrid;
     float* anchors = reinterpret_cast<float*>(scratch);
     if ((e = launch_tc_bwd(fa, A.E, anchors, A.dm2, A.dm1, A.dxhat, A.dbhat, A.dda, A.drot, maps, grid, st)) !=

@@ -599,7 +599,7 @@ static cudaError_t bwd_impl(const MMParams& P, const GenericPtrs& A, int grid, c
     if (e != cudaSuccess) return e;
     const T* x = (const T*)A.xhat;
     const T* bh = (const T*)A.bhat;
-    if ((e = carries<T>(P, x, bh, A.da, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
+    if (!A.reuse_carries && (e = carries<T>(P, x, bh, A.da, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
     int64_t nbh = (int64_t)P.b * P.h;
     int64_t tot = nbh * P.r * P.r;
     mm_prof_mark(KID_DSYM, 1, st);

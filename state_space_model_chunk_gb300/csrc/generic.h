@@ -3,6 +3,7 @@
 #include "common.cuh"
 
 struct GenericPtrs {
+    int reuse_carries;  // backward: Hc / Dn already hold this problem's carries (from its forward)
     const void* xhat;
     const void* bhat;
     const float* da;

@@ -128,3 +128,21 @@ def test_no_cpu_fallback():
     with pytest.raises(RuntimeError):
         binding.moments_fwd(base_spec(b=1, s=16), x, b, torch.zeros(1, 16, 1), torch.zeros(1, 16, 1, 4),
                             torch.zeros(1, 1, 8, 16), [16])
+
+
+def test_flag_values_match_the_header():
+    text = open(os.path.join(ROOT, "include", "moments.h")).read()
+    flags = dict(re.findall(r"#define\s+(MM_FLAG_[A-Z_]+)\s+(0x[0-9a-fA-F]+)u", text))
+    assert int(flags["MM_FLAG_FORCE_GENERIC"], 16) == binding.MM_FLAG_FORCE_GENERIC
+    assert int(flags["MM_FLAG_REUSE_CARRIES"], 16) == binding.MM_FLAG_REUSE_CARRIES
+    spec = Spec(1, 64, 1, 2, 8, 16, 16)
+    assert spec.problem(binding.MM_FLAG_REUSE_CARRIES).flags == binding.MM_FLAG_REUSE_CARRIES
+
+
+def test_reuse_carries_needs_the_forward_workspace():
+    """The binding refuses a carry-reusing backward without the workspace the forward wrote."""
+    import torch
+    spec = Spec(1, 64, 1, 2, 8, 16, 16, dtype="f32")
+    x = torch.zeros((1, 64, 1, 2, 8))
+    with pytest.raises(ValueError):
+        binding.moments_bwd(spec, x, x, x, None, x, [60], x, x, reuse_carries=True)

@@ -133,6 +133,34 @@ def test_parity_steep_decay_spans():
     check_against_oracle(w, inp, got, w.name)
 
 
+@pytest.mark.parametrize("w", [SMALL[3], SMALL[0],
+                               WORKLOADS["large_s4096"].scaled(name="mixed_paths", b=1, s=128, h=4, C=6)],
+                         ids=["tensor_core", "simt", "mixed_paths"])
+def test_backward_reusing_forward_carries(w):
+    """MM_FLAG_REUSE_CARRIES: forward then backward on one workspace gives the gradients of a
+    backward that recomputes the carries (on the tensor-core path, the SIMT path, and a problem
+    whose forward and backward take different paths, where the flag is ignored)."""
+    inp = make_inputs(w)
+    d = {k: v.to(DEV) for k, v in inp.items() if k != "valid_len"}
+    spec = spec_of(w)
+    rot = d["rot"] if d["rot"].numel() else None
+    args = (spec, d["xhat"], d["bhat"], d["da"], rot, d["initial"], inp["valid_len"])
+    ref = binding.moments_bwd(*args, d["d_m2"], d["d_m1"])
+    ws = binding.alloc_workspace(spec, True, torch.device(DEV))
+    m2, m1 = binding.moments_fwd(*args, workspace=ws)
+    got = binding.moments_bwd(*args, d["d_m2"], d["d_m1"], workspace=ws, reuse_carries=True)
+    torch.cuda.synchronize()
+    for k in GRADS:
+        if ref[k] is None:
+            continue
+        a_, b_ = got[k].float().cpu(), ref[k].float().cpu()
+        assert torch.allclose(a_, b_, rtol=1e-5, atol=1e-6 * max(1.0, float(b_.abs().max()))), k
+    out = dict(m2=m2.cpu(), m1=m1.cpu())
+    for k in GRADS:
+        out[k] = got[k].cpu() if got[k] is not None else torch.zeros(0)
+    check_against_oracle(w, inp, out, w.name + "/reuse")
+
+
 FULL = ["quat_s2048", "large_s4096", "ragged_s16384"]
 
 
