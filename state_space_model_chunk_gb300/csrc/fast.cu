@@ -64,6 +64,28 @@ int sm_count() {
     return n;
 }
 
+cudaError_t encode_grad_maps(const MMParams& P, const void* dx, const void* db, TensorMaps* maps) {
+    const cuuint64_t bs = (cuuint64_t)P.b * P.s;
+    cudaError_t e;
+    {   // as x32, over d_xhat
+        cuuint64_t dims[4] = {(cuuint64_t)P.p, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
+        cuuint64_t str[3] = {(cuuint64_t)P.p * 2, (cuuint64_t)P.h * P.p * 2, (cuuint64_t)P.C * P.h * P.p * 2};
+        cuuint32_t box[4] = {64, 1, (cuuint32_t)P.C, 32};
+        if ((e = encode(&maps->dx32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, dx, dims, str, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
+    }
+    {   // as b32, over d_bhat
+        cuuint64_t dims[5] = {64, (cuuint64_t)P.r / 64, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
+        cuuint64_t str[4] = {128, (cuuint64_t)P.r * 2, (cuuint64_t)P.h * P.r * 2, (cuuint64_t)P.C * P.h * P.r * 2};
+        cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)P.C, 32};
+        if ((e = encode(&maps->db32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, db, dims, str, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, const float* rot, const float* da,
                         TensorMaps* maps) {
     const cuuint64_t bs = (cuuint64_t)P.b * P.s;
@@ -209,5 +231,6 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
         cudaSuccess)
         return e;
     if ((e = generic_cot_scan(P, A.E, A.Dn, A.dinit, st)) != cudaSuccess) return e;
+    if ((e = encode_grad_maps(P, A.dxhat, A.dbhat, &maps)) != cudaSuccess) return e;
     return launch_tc_corr(fa, A.da, A.E, A.dxhat, A.dbhat, A.dda, maps, st);
 }

@@ -27,6 +27,7 @@ struct TensorMaps {
     CUtensorMap x, b, rot, da, da64;  // da: 4 heads x 1 token; da64: 4 heads x 64 tokens
     CUtensorMap x8, b8;               // xhat / bhat rows of 8 consecutive tokens
     CUtensorMap x32, b32;             // ... and of 32
+    CUtensorMap dx32, db32;           // d_xhat / d_bhat rows of 32 tokens (backward only)
 };
 
 constexpr int kMaxBwdGrid = 160;  // CTAs of the backward kernels (anchor slots in the workspace)
@@ -202,6 +203,8 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
 int sm_count();
 cudaError_t launch_tc_fwd(const FastArgs& args, const TensorMaps& maps, int grid, cudaStream_t st);
 cudaError_t launch_tc_end(const FastArgs& fa, const TensorMaps& maps, cudaStream_t st);
+// Tensor maps over the d_xhat / d_bhat outputs, same geometry as x32 / b32 (C <= 4).
+cudaError_t encode_grad_maps(const MMParams& P, const void* dx, const void* db, TensorMaps* maps);
 cudaError_t launch_tc_corr(const FastArgs& fa, const float* da, const float* E, void* dx, void* db, float* dda,
                            const TensorMaps& maps, cudaStream_t st);
 size_t bwd_anchor_bytes();

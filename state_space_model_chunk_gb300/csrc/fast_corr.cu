@@ -31,9 +31,12 @@ using namespace fastk;
 constexpr int NTHR = 576;
 constexpr int NEW = 16;                    // epilogue warps: four per TMEM lane quarter
 constexpr int TPS = 32;                    // tokens per stage (rows 32 C <= 128)
-constexpr int NS = 3;                      // stages
+constexpr int NS = 2;                      // stages
 constexpr uint32_t SLOT = 16384;           // 128 rows x 128 B
-constexpr uint32_t STAGE = 3 * SLOT;       // xhat | bhat r 0..63 | bhat r 64..127
+// xhat | bhat r 0..63 | bhat r 64..127 | d_xhat | d_bhat r 0..63 | d_bhat r 64..127: the gradient
+// rows come in with the stage and go back out by tensor stores once the epilogue updated them
+constexpr uint32_t STAGE = 6 * SLOT;
+constexpr uint32_t SL_DX = 3, SL_DB = 4;   // slot indices of d_xhat / d_bhat
 constexpr uint32_t DHT = 16384;            // dH tile: 64 rows x 2 blocks x 128 B
 constexpr uint32_t OFF_DH = NS * STAGE;    // 2 dH tiles
 constexpr uint32_t OFF_SC = OFF_DH + 2 * DHT;   // sc_t, 64 fp32
@@ -45,7 +48,7 @@ static_assert(OFF_DH % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Ctl {
-    uint64_t full[NS], empty[NS];
+    uint64_t full[NS], upd[NS];  // upd: the epilogue has updated the stage's gradient rows
     uint64_t accfull[2], accfree[2];
     uint64_t dhfull[2], dhfree[2];
     uint64_t fin;
@@ -106,7 +109,8 @@ struct CorrArgs {
 
 __global__ void __launch_bounds__(NTHR, 1)
     tc_corr_kernel(const __grid_constant__ CorrArgs B, const __grid_constant__ CUtensorMap tmx32,
-                   const __grid_constant__ CUtensorMap tmb32) {
+                   const __grid_constant__ CUtensorMap tmb32, const __grid_constant__ CUtensorMap tmdx32,
+                   const __grid_constant__ CUtensorMap tmdb32) {
     extern __shared__ unsigned char smraw[];
     unsigned char* sm = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
     Ctl* ctl = reinterpret_cast<Ctl*>(sm + OFF_CTL);
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             tc::mbar_init(&ctl->full[s], 1);
-            tc::mbar_init(&ctl->empty[s], NEW);
+            tc::mbar_init(&ctl->upd[s], NEW);
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&ctl->accfull[i], 1);
@@ -148,23 +152,46 @@ __global__ void __launch_bounds__(NTHR, 1)
 
     if (warp == 0) {
         // ================================================================ TMA producer
+        // Per stage: the xhat / bhat rows and the d_xhat / d_bhat rows of 32 tokens in; before a
+        // slot is reused, the stage it held goes back out (the updated gradient rows) by tensor
+        // stores, whose reads of the slot complete before the new loads are issued.
         if (lane == 0) {
             uint32_t q = 0;
             bool ok = true;
+            int srow[NS] = {0, 0}, shh[NS] = {0, 0};  // global row and head of the stage each slot holds
+            auto store_back = [&](uint32_t qq) -> bool {
+                const uint32_t s = qq % NS;
+                if (!tc::mbar_wait(&ctl->upd[s], (qq / NS) & 1, abort)) return false;
+                unsigned char* stg = sm + s * STAGE;
+                tc::tma_store_4d(&tmdx32, 0, shh[s], 0, srow[s], stg + SL_DX * SLOT);
+                for (int a = 0; a < R / 64; ++a)
+                    tc::tma_store_5d(&tmdb32, 0, a, shh[s], 0, srow[s], stg + (SL_DB + a) * SLOT);
+                tc::bulk_commit();
+                tc::bulk_wait_read0();
+                return true;
+            };
             for (int it = it0; it < it1 && ok; ++it) {
                 const CItem I = decode(P, it);
                 for (int st = 0; st < FL / TPS; ++st, ++q) {
-                    const uint32_t s = q % NS, u = q / NS;
-                    if (u >= 1 && !(ok = tc::mbar_wait(&ctl->empty[s], (u - 1) & 1, abort))) break;
+                    const uint32_t s = q % NS;
+                    if (q >= NS && !(ok = store_back(q - NS))) break;
                     unsigned char* stg = sm + s * STAGE;
-                    tc::mbar_arrive_expect_tx(&ctl->full[s], rows * 128u * (1u + (uint32_t)R / 64u));
+                    tc::mbar_arrive_expect_tx(&ctl->full[s], 2u * rows * 128u * (1u + (uint32_t)R / 64u));
                     const int row = I.bb * P.s + I.n * FL + st * TPS;
                     tc::tma_load_4d(stg, &tmx32, 0, I.hh, 0, row, &ctl->full[s]);
-                    for (int a = 0; a < R / 64; ++a)
+                    tc::tma_load_4d(stg + SL_DX * SLOT, &tmdx32, 0, I.hh, 0, row, &ctl->full[s]);
+                    for (int a = 0; a < R / 64; ++a) {
                         tc::tma_load_5d(stg + (1 + a) * SLOT, &tmb32, 0, a, I.hh, 0, row, &ctl->full[s]);
+                        tc::tma_load_5d(stg + (SL_DB + a) * SLOT, &tmdb32, 0, a, I.hh, 0, row, &ctl->full[s]);
+                    }
+                    srow[s] = row;
+                    shh[s] = I.hh;
                 }
             }
+            // the last stages go out too
+            for (uint32_t qq = q >= NS ? q - NS : 0; ok && qq < q; ++qq) ok = store_back(qq);
             if (!ok) fail(ctl, A.err, 41);
+            tc::bulk_wait0();       // every store has completed
             int never = 0;  // every issued copy lands before the CTA exits
             for (uint32_t s = 0; s < NS && q > s; ++s) {
                 const uint32_t last = (q - 1 - s) / NS;
@@ -215,7 +242,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         float* sc = reinterpret_cast<float*>(sm + OFF_SC);
         float* misc = reinterpret_cast<float*>(sm + OFF_MISC);  // [0..1] dot per item parity, [2] D_n
         const bool row_ok = (uint32_t)k < rows;
-        const int tl = k / C, cc = k - (k / C) * C;
+        const int tl = k / C;  // the row's token in the stage (rows are (token, channel))
         uint32_t q = 0, li = 0;
         bool ok = true;
         auto check = [&](bool r) {  // the first failed wait stops the whole CTA at once
@@ -282,31 +309,20 @@ __global__ void __launch_bounds__(NTHR, 1)
             for (int st = 0; st < FL / TPS; ++st, ++q) {
                 const uint32_t s = q % NS, ab = q & 1;
                 const int t = st * TPS + tl;
-                const int tok = I.n * FL + t;
                 // this thread's part of the row: U columns [16 qf, 16 qf + 16), V columns [32 qf, 32 qf + 32)
                 const bool has_v = 32 * qf < R;
-                uint4 ox[2], ob[4];
-                __nv_bfloat16* px = B.dx + off_x(P, I.bb, tok, cc, I.hh) + 16 * qf;
-                __nv_bfloat16* pb = B.db + off_b(P, I.bb, tok, cc, I.hh) + 32 * qf;
-                if (row_ok) {
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) ox[i] = reinterpret_cast<const uint4*>(px)[i];
-                    if (has_v) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) ob[i] = reinterpret_cast<const uint4*>(pb)[i];
-                    }
-                }
-                check(tc::mbar_wait(&ctl->full[s], (q / NS) & 1, abort));  // the stage's xhat rows are read below
+                check(tc::mbar_wait(&ctl->full[s], (q / NS) & 1, abort));  // the stage's rows are read below
                 check(tc::mbar_wait(&ctl->accfull[ab], (q >> 1) & 1, abort));
                 tc::tc_fence_after();
                 const uint32_t tu = lane_addr + ab * TM_BUF, tv = tu + 64;
                 float u[16];
                 tc::tmem_ld16(tu + 16 * qf, u);
                 tc::tmem_wait_ld();
+                unsigned char* const stg = sm + s * STAGE;
                 // omega partial: <xhat row, U row> over this quarter (xhat row from the stage tile)
                 float w = 0.f;
                 {
-                    const unsigned char* xr = sm + s * STAGE + k * 128;
+                    const unsigned char* xr = stg + k * 128;
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
                         const int j = 2 * qf + jj;
@@ -321,20 +337,24 @@ __global__ void __launch_bounds__(NTHR, 1)
                 }
                 if (row_ok) atomicAdd(&om[t], w);
                 const float scv = sc[t];
-                if (row_ok) {
+                if (row_ok) {  // d_xhat row += sc U, in the stage's d_xhat slot (same layout as xhat)
+                    unsigned char* dr = stg + SL_DX * SLOT + k * 128;
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        uint32_t* wd = reinterpret_cast<uint32_t*>(&ox[i]);
+                    for (int jj = 0; jj < 2; ++jj) {
+                        uint4* pw = reinterpret_cast<uint4*>(dr + (((2 * qf + jj) ^ (k & 7)) << 4));
+                        uint4 o = *pw;
+                        uint32_t* wd = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float lo = __uint_as_float(wd[e] << 16) + scv * u[8 * i + 2 * e];
-                            const float hi = __uint_as_float(wd[e] & 0xFFFF0000u) + scv * u[8 * i + 2 * e + 1];
+                            const float lo = __uint_as_float(wd[e] << 16) + scv * u[8 * jj + 2 * e];
+                            const float hi = __uint_as_float(wd[e] & 0xFFFF0000u) + scv * u[8 * jj + 2 * e + 1];
                             wd[e] = tc::pack_bf16x2(lo, hi);
                         }
-                        reinterpret_cast<uint4*>(px)[i] = ox[i];
+                        *pw = o;
                     }
                 }
-                if (has_v) {
+                if (has_v) {  // d_bhat row += sc V, columns [32 qf, 32 qf + 32): slot qf / 2, chunks 4 (qf & 1) ..
+                    unsigned char* br = stg + (SL_DB + (qf >> 1)) * SLOT + k * 128;
 #pragma unroll
                     for (int g = 0; g < 2; ++g) {
                         float v[16];
@@ -343,7 +363,10 @@ __global__ void __launch_bounds__(NTHR, 1)
                         if (row_ok) {
 #pragma unroll
                             for (int i = 0; i < 2; ++i) {
-                                uint32_t* wd = reinterpret_cast<uint32_t*>(&ob[2 * g + i]);
+                                const int j = 4 * (qf & 1) + 2 * g + i;
+                                uint4* pw = reinterpret_cast<uint4*>(br + ((j ^ (k & 7)) << 4));
+                                uint4 o = *pw;
+                                uint32_t* wd = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
                                     const float lo = __uint_as_float(wd[e] << 16) + scv * v[8 * i + 2 * e];
@@ -351,16 +374,17 @@ __global__ void __launch_bounds__(NTHR, 1)
                                         __uint_as_float(wd[e] & 0xFFFF0000u) + scv * v[8 * i + 2 * e + 1];
                                     wd[e] = tc::pack_bf16x2(lo, hi);
                                 }
-                                reinterpret_cast<uint4*>(pb)[2 * g + i] = ob[2 * g + i];
+                                *pw = o;
                             }
                         }
                     }
                 }
+                tc::fence_proxy_async_smem();  // the updated rows are read by the tensor stores
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     tc::mbar_arrive(&ctl->accfree[ab]);
-                    tc::mbar_arrive(&ctl->empty[s]);
+                    tc::mbar_arrive(&ctl->upd[s]);
                 }
             }
             named_barrier_sync(1, NEW * 32);  // omega complete
@@ -405,7 +429,7 @@ cudaError_t launch_tc_corr(const FastArgs& fa, const float* da, const float* E, 
     cudaError_t e = cudaFuncSetAttribute(tc_corr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     mm_prof_mark(KID_FAST_CORRECT, 1, st);
-    tc_corr_kernel<<<grid, NTHR, SMEM_BYTES, st>>>(a, maps.x32, maps.b32);
+    tc_corr_kernel<<<grid, NTHR, SMEM_BYTES, st>>>(a, maps.x32, maps.b32, maps.dx32, maps.db32);
     mm_prof_mark(KID_FAST_CORRECT, 0, st);
     return cudaGetLastError();
 }
