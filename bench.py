@@ -260,6 +260,19 @@ def collect_kernels(lib):
     return kernels
 
 
+def max_over_ranks(x, dist, device):
+    """The largest of a per-rank value over all ranks (a job takes as long as its slowest rank)."""
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms_max):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_max / 1e3)
+
+
 def run_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -331,11 +344,8 @@ def run_ours(args):
     dev_status = [int(lib.mm_device_status(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(stream.cuda_stream)))
                   for ws in (ws_f, ws_b)]
 
-    t = torch.tensor([ms], device=dev)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = world * ntok / (ms_max / 1e3)
+    ms_max = max_over_ranks(ms, dist, dev)
+    value = job_tokens_per_s(ntok, world, ms_max)
 
     # ---- e2e: host buffers through the same C ABI, copies inside the timed region
     e2e = None
@@ -383,12 +393,10 @@ def run_ours(args):
         run_steps(e_steps, e0)
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = torch.tensor([e0.elapsed_time(e1) / e_steps], device=dev)
-        if dist:
-            dist.all_reduce(ems, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * ntok / (float(ems.item()) / 1e3), "unit": "tokens/s",
+        ems = max_over_ranks(e0.elapsed_time(e1) / e_steps, dist, dev)
+        e2e = {"value": job_tokens_per_s(ntok, world, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": float(ems.item()), "steps": e_steps,
+               "ms_per_step": ems, "steps": e_steps,
                "copies": "pinned H2D of every input each step on a second stream, overlapping the previous step's kernels"}
         del bufs
 
