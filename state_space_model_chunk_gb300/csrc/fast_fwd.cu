@@ -29,6 +29,7 @@
 #include "fast.h"
 #include "fast_common.cuh"
 #include "prof.h"
+#include "rot_sincos.cuh"
 #include "tc.cuh"
 
 namespace fastfwd {
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + s * 1024 + ch * 512);
                 if (ROTK == ROT_PAIRWISE || ROTK == ROT_HALF) {
                     float sv = 0.f, cv = 1.f;
-                    if (my_ang < P.na) sincosf(qt[my_ang], &sv, &cv);
+                    if (my_ang < P.na) rot_sincos(qt[my_ang], &sv, &cv);
                     __syncwarp();  // the previous token's table has been read
                     tbl[lane] = cv;
                     tbl[32 + lane] = sv;
