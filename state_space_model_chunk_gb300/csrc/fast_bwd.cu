@@ -5,24 +5,29 @@
 // TMEM lanes (row m = (chunk, p)) as in the forward.  This kernel is the chunk's own backward with
 // zero incoming carry cotangent ("backward.rs", module header "Gradient math", with the d_h+
 // term split off; fast_corr.cu adds it once the cotangent scan has run):
-//   phase A  forward sweep h = e^{da} h + W from the chunk carry (W by one block-diagonal MMA per
-//            token); the state after every 8th token is kept as an fp32 anchor in this CTA's
-//            workspace slot (7 anchors; the chunk carry is anchor 0).
+//   phase A  forward sweep from the chunk carry, one 8-token span at a time: S <- D_k S +
+//            sum_j L[end, j] W_j with the sum as one K = 128 tensor-core product (xhat rows scaled
+//            in place by L); the state after every 8th token is kept as an fp32 anchor in this
+//            CTA's workspace slot (7 anchors; the chunk carry is anchor 0), column-quad-major.
 //   phase B  8-token spans in reverse.  For token t of a span starting at s0 the state is
-//            rebuilt exactly as  h_t = (prod_{s0<=i<=t} e_i) A + sum_{s0<=j<=t} L[t,j] W_j : one
-//            prefix MMA whose A rows are xhat rows scaled by L[t,j] = exp(a_t - a_j) (two tokens
-//            per K=16 step), plus the anchor term read from TMEM.  Then c = derot(h) (bf16 tile),
-//            d_c = c (D + D^T) + d_m1 on tcgen05 (K = r), d_rot from (c, d_c) by warp transpose
+//            rebuilt exactly as  h_t = exp(a_t - a_anchor) A + sum_{s0<=j<=t} L[t,j] W_j : one
+//            prefix product with one K = 16 step per span token j <= t (A rows = xhat rows scaled
+//            by L[t,j] = exp(a_t - a_j)), plus the anchor term read from TMEM.  Then c = derot(h)
+//            as bf16 pairs into TMEM, d_c = c (D + D^T) + 1 d_m1^T on tcgen05 with A = that c
+//            tile (K = r, and one K = 16 step for d_m1), d_rot from (c, d_c) by warp transpose
 //            reductions over p, G = derot^T(d_c), the cotangent recurrence g_t = G_t + e_{t+1}
 //            g_{t+1} in registers, d_da_{t+1} = e_{t+1} <g_{t+1}, h_t>, and d_xhat = g bhat^T,
 //            d_bhat = g^T xhat as N = 16 MMAs.  After the chunk: e_n = e_0 g_0.
 //            The span is software-pipelined: while the CUDA cores finish the cotangent work of
-//            token t, the tensor cores already run d_c of token t-1 and the prefix of t-2.
+//            token t, the tensor cores already run d_c of token t-1 and the prefix of t-2.  The
+//            span's token slots are released one by one (token s0 + j's d_xhat / d_bhat product
+//            is the last reader of slot j), so the next span's high slots load early.
 //
 // Warp roles: 0-7 compute (two threads per row, 64 columns each, handled as two 32-column
-// passes whose rotation partners stay inside the pass), 8 TMA, 9 MMA.  d_rot and d_da are summed
-// over p with warp transpose-reductions and added to global memory (zeroed by the host).  Every
-// wait is bounded; a timeout sets the workspace error word and the CTA winds down.
+// passes whose rotation partners stay inside the pass), 8 TMA (all 32 lanes issue copies), 9 MMA.
+// d_rot and d_da are summed over p with warp transpose-reductions and added to global memory
+// (zeroed by the host).  Every wait is bounded; a timeout sets the workspace error word and the
+// CTA winds down.
 #include <cuda.h>
 
 #include "common.cuh"
