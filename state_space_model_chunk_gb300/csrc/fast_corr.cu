@@ -11,8 +11,9 @@
 // Over the rows (t, c) of 32 tokens these are U = Bhat dH^T (M = 32 C, N = p, K = r) and
 // V = Xhat dH (M = 32 C, N = r, K = p).  One bf16 dH tile [p][r] in the 128-byte-swizzled layout
 // is the K-major B operand of the first and the MN-major B operand of the second; the xhat /
-// bhat rows come by TMA.  The epilogue (lanes = rows (t, c), four threads per row) scales, adds
-// into d_xhat / d_bhat in place, and accumulates omega.
+// bhat rows and the d_xhat / d_bhat rows of the stage come by TMA.  The epilogue (lanes = rows
+// (t, c), four threads per row) adds sc_t U / sc_t V to the gradient rows in shared memory and
+// accumulates omega; the copy warp writes the updated rows back with tensor stores.
 //
 // Warp roles: 0 TMA, 1 MMA, 2-17 dH tile + epilogue.  Every wait is bounded; a timeout sets the
 // workspace error word and the CTA winds down.
