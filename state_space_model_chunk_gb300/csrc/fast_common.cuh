@@ -154,18 +154,7 @@ __device__ __forceinline__ void hamilton(float qw, float qx, float qy, float qz,
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// 16 columns (group gcol of 16) of row m of a bf16 [128 x 128] swizzled tile, as floats / from floats.
-__device__ __forceinline__ void read_tile16(const unsigned char* tile, int m, int gcol, float (&v)[16]) {
-    const uint32_t hv = gcol >> 2, j0 = 2 * (gcol & 3);
-#pragma unroll
-    for (int hj = 0; hj < 2; ++hj) {
-        const uint4 w = *reinterpret_cast<const uint4*>(tile + tc::sw128_chunk(128, hv, m, j0 + hj));
-        v[8 * hj + 0] = bf16lo(w.x); v[8 * hj + 1] = bf16hi(w.x);
-        v[8 * hj + 2] = bf16lo(w.y); v[8 * hj + 3] = bf16hi(w.y);
-        v[8 * hj + 4] = bf16lo(w.z); v[8 * hj + 5] = bf16hi(w.z);
-        v[8 * hj + 6] = bf16lo(w.w); v[8 * hj + 7] = bf16hi(w.w);
-    }
-}
+// 16 columns (group gcol of 16) of row m of a bf16 [128 x 128] swizzled tile, from floats.
 __device__ __forceinline__ void write_tile16(unsigned char* tile, int m, int gcol, const float (&v)[16], bool zero) {
     const uint32_t hv = gcol >> 2, j0 = 2 * (gcol & 3);
 #pragma unroll
