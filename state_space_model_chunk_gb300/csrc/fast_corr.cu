@@ -15,8 +15,10 @@
 // (t, c), four threads per row) adds sc_t U / sc_t V to the gradient rows in shared memory and
 // accumulates omega; the copy warp writes the updated rows back with tensor stores.
 //
-// Warp roles: 0 TMA, 1 MMA, 2-17 dH tile + epilogue.  Every wait is bounded; a timeout sets the
-// workspace error word and the CTA winds down.
+// Warp roles: 0 TMA, 1 MMA, 2-17 epilogue, 18-19 builders.  The builders prepare the next item
+// (bf16 dH tile, sc_t, D_n and <dH, h_-(n)>, double-buffered by item parity) while the epilogue
+// works on the current one, so the item boundary costs no global-load latency.  Every wait is
+// bounded; a timeout sets the workspace error word and the CTA winds down.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -29,8 +31,10 @@ namespace fastcorr {
 
 using namespace fastk;
 
-constexpr int NTHR = 576;
 constexpr int NEW = 16;                    // epilogue warps: four per TMEM lane quarter
+constexpr int NBW = 2;                     // builder warps
+constexpr int NTHR = (2 + NEW + NBW) * 32;
+static_assert(NBW == 2, "the epilogue sums two dot partials");
 constexpr int TPS = 32;                    // tokens per stage (rows 32 C <= 128)
 constexpr int NS = 2;                      // stages
 constexpr uint32_t SLOT = 16384;           // 128 rows x 128 B
@@ -40,9 +44,9 @@ constexpr uint32_t STAGE = 6 * SLOT;
 constexpr uint32_t SL_DX = 3, SL_DB = 4;   // slot indices of d_xhat / d_bhat
 constexpr uint32_t DHT = 16384;            // dH tile: 64 rows x 2 blocks x 128 B
 constexpr uint32_t OFF_DH = NS * STAGE;    // 2 dH tiles
-constexpr uint32_t OFF_SC = OFF_DH + 2 * DHT;   // sc_t, 64 fp32
-constexpr uint32_t OFF_OM = OFF_SC + 256;       // omega, 2 items x 64 fp32
-constexpr uint32_t OFF_MISC = OFF_OM + 512;     // dot (2 items), D_n
+constexpr uint32_t OFF_SC = OFF_DH + 2 * DHT;   // sc_t, 2 items x 64 fp32
+constexpr uint32_t OFF_OM = OFF_SC + 512;       // omega, 2 items x 64 fp32
+constexpr uint32_t OFF_MISC = OFF_OM + 512;     // dot partials [item][builder warp], then D_n [item]
 constexpr uint32_t OFF_CTL = OFF_MISC + 64;
 constexpr uint32_t SMEM_BYTES = OFF_CTL + 256 + 1024;
 static_assert(OFF_DH % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles");
@@ -52,6 +56,7 @@ struct Ctl {
     uint64_t full[NS], upd[NS];  // upd: the epilogue has updated the stage's gradient rows
     uint64_t accfull[2], accfree[2];
     uint64_t dhfull[2], dhfree[2];
+    uint64_t scfree[2];  // the epilogue has read the item's sc_t, D_n and dot
     uint64_t fin;
     uint32_t tbase;
     int abort;
@@ -133,8 +138,9 @@ __global__ void __launch_bounds__(NTHR, 1)
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&ctl->accfull[i], 1);
             tc::mbar_init(&ctl->accfree[i], NEW);
-            tc::mbar_init(&ctl->dhfull[i], NEW);
+            tc::mbar_init(&ctl->dhfull[i], NBW);
             tc::mbar_init(&ctl->dhfree[i], 1);
+            tc::mbar_init(&ctl->scfree[i], 1);
         }
         tc::mbar_init(&ctl->fin, 1);
         ctl->abort = 0;
@@ -234,14 +240,13 @@ __global__ void __launch_bounds__(NTHR, 1)
             int never = 0;  // in-flight MMAs must finish before the TMEM is released
             tc::mbar_wait(&ctl->fin, 0, &never, 1u << 20);
         }
-    } else {
-        // ================================================================ dH tile + epilogue
+    } else if (warp < 2 + NEW) {
+        // ================================================================ epilogue
         const int ew = warp - 2, etid = tid - 64;
         const int qf = ew >> 2;                     // which quarter of the row's columns
         const int k = ((warp & 3) << 5) + lane;     // TMEM lane = stage row (t, c)
         const uint32_t lane_addr = tbase + ((uint32_t)((warp & 3) * 32) << 16);
-        float* sc = reinterpret_cast<float*>(sm + OFF_SC);
-        float* misc = reinterpret_cast<float*>(sm + OFF_MISC);  // [0..1] dot per item parity, [2] D_n
+        const float* misc = reinterpret_cast<const float*>(sm + OFF_MISC);
         const bool row_ok = (uint32_t)k < rows;
         const int tl = k / C;  // the row's token in the stage (rows are (token, channel))
         uint32_t q = 0, li = 0;
@@ -256,56 +261,8 @@ __global__ void __launch_bounds__(NTHR, 1)
             const CItem I = decode(P, it);
             const uint32_t ib = li & 1;
             float* om = reinterpret_cast<float*>(sm + OFF_OM) + ib * 64;
-            // ---- decay weights sc_t of the chunk (all 64 of its tokens are valid) and D_n
-            if (ew == 0) {
-                const int t0 = 2 * lane, t1 = t0 + 1;
-                const float v0 = B.da[off_da(P, I.bb, I.n * FL + t0, I.hh)];
-                const float v1 = B.da[off_da(P, I.bb, I.n * FL + t1, I.hh)];
-                float sum = v0 + v1;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float o = __shfl_up_sync(0xffffffffu, sum, off);
-                    if (lane >= off) sum += o;
-                }
-                const float alast = __shfl_sync(0xffffffffu, sum, 31);
-                sc[t1] = __expf(alast - sum);
-                sc[t0] = __expf(alast - (sum - v1));
-                if (lane == 0) misc[2] = __expf(alast);
-            }
-            // ---- dH tile (bf16, [p][r] swizzled) and <dH, h_-(n)>
-            if (li >= 2) check(tc::mbar_wait(&ctl->dhfree[ib], ((li - 2) >> 1) & 1, abort));
-            {
-                unsigned char* dht = sm + OFF_DH + ib * DHT;
-                const float* src = B.E + off_carry(P, I.bb, I.hh, I.n);
-                const float* hin = A.Hc + off_carry(P, I.bb, I.hh, I.n);
-                float dot = 0.f;
-#pragma unroll
-                for (int i = 0; i < 64 * 16 / (NEW * 32); ++i) {
-                    const int id = i * (NEW * 32) + etid;
-                    const int pp = id >> 4, j16 = id & 15, blk = j16 >> 3, j = j16 & 7;
-                    const int col = 64 * blk + 8 * j;
-                    uint4 w = make_uint4(0, 0, 0, 0);
-                    if (col < R) {
-                        const float4 e0 = *reinterpret_cast<const float4*>(src + pp * R + col);
-                        const float4 e1 = *reinterpret_cast<const float4*>(src + pp * R + col + 4);
-                        const float4 h0 = *reinterpret_cast<const float4*>(hin + pp * R + col);
-                        const float4 h1 = *reinterpret_cast<const float4*>(hin + pp * R + col + 4);
-                        dot += e0.x * h0.x + e0.y * h0.y + e0.z * h0.z + e0.w * h0.w;
-                        dot += e1.x * h1.x + e1.y * h1.y + e1.z * h1.z + e1.w * h1.w;
-                        w.x = tc::pack_bf16x2(e0.x, e0.y);
-                        w.y = tc::pack_bf16x2(e0.z, e0.w);
-                        w.z = tc::pack_bf16x2(e1.x, e1.y);
-                        w.w = tc::pack_bf16x2(e1.z, e1.w);
-                    }
-                    *reinterpret_cast<uint4*>(dht + tc::sw128_chunk(64, blk, pp, j)) = w;
-                }
-                dot = warp_sum(dot);
-                if (lane == 0) atomicAdd(&misc[ib], dot);
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&ctl->dhfull[ib]);
-            }
-            named_barrier_sync(1, NEW * 32);  // sc, D_n and the dot are complete
+            const float* sc = reinterpret_cast<const float*>(sm + OFF_SC) + ib * 64;
+            check(tc::mbar_wait(&ctl->dhfull[ib], (li >> 1) & 1, abort));  // sc, D_n and the dot are ready
             // ---- the two 32-token stages
             for (int st = 0; st < FL / TPS; ++st, ++q) {
                 const uint32_t s = q % NS, ab = q & 1;
@@ -391,15 +348,89 @@ __global__ void __launch_bounds__(NTHR, 1)
             named_barrier_sync(1, NEW * 32);  // omega complete
             // ---- d_da_s += D_n <dH, h_-> + sum_{j<s} sc_j omega_j
             if (etid < FL) {
-                const float base = misc[2] * misc[ib];
+                const float base = misc[2 * NBW + ib] * (misc[NBW * ib] + misc[NBW * ib + 1]);
                 float pre = 0.f;
                 for (int j = 0; j < etid; ++j) pre = fmaf(sc[j], om[j], pre);
                 B.dda[off_da(P, I.bb, I.n * FL + etid, I.hh)] += base + pre;
             }
             named_barrier_sync(1, NEW * 32);  // sc / D_n / omega / dot read: free for the next items
             if (etid < FL) om[etid] = 0.f;
-            if (etid == 0) misc[ib] = 0.f;
+            if (etid == 0) tc::mbar_arrive(&ctl->scfree[ib]);
         }
+    } else {
+        // ================================================================ builders
+        // Item by item, into the buffers of the item's parity once the MMAs (dH tile) and the
+        // epilogue (sc_t, D_n, dot) of the item two back are done with them: the bf16 dH tile
+        // [p][r] in the 128-byte-swizzled layout, this warp's part of <dH, h_-(n)>, and (warp 0)
+        // the decay weights sc_t = exp(a_last - a_t) and D_n = exp(a_last).
+        const int bw = warp - 2 - NEW, bt = tid - (2 + NEW) * 32;
+        float* misc = reinterpret_cast<float*>(sm + OFF_MISC);
+        uint32_t li = 0;
+        bool ok = true;
+        for (int it = it0; it < it1 && ok; ++it, ++li) {
+            const CItem I = decode(P, it);
+            const uint32_t ib = li & 1;
+            if (li >= 2 && !(ok = tc::mbar_wait(&ctl->dhfree[ib], ((li - 2) >> 1) & 1, abort) &&
+                                  tc::mbar_wait(&ctl->scfree[ib], ((li - 2) >> 1) & 1, abort)))
+                break;
+            if (bw == 0) {  // all 64 tokens of the chunk are valid
+                float* sc = reinterpret_cast<float*>(sm + OFF_SC) + ib * 64;
+                const int t0 = 2 * lane, t1 = t0 + 1;
+                const float v0 = B.da[off_da(P, I.bb, I.n * FL + t0, I.hh)];
+                const float v1 = B.da[off_da(P, I.bb, I.n * FL + t1, I.hh)];
+                float sum = v0 + v1;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, sum, off);
+                    if (lane >= off) sum += o;
+                }
+                const float alast = __shfl_sync(0xffffffffu, sum, 31);
+                sc[t1] = __expf(alast - sum);
+                sc[t0] = __expf(alast - (sum - v1));
+                if (lane == 0) misc[2 * NBW + ib] = __expf(alast);
+            }
+            unsigned char* dht = sm + OFF_DH + ib * DHT;
+            const float* src = B.E + off_carry(P, I.bb, I.hh, I.n);
+            const float* hin = A.Hc + off_carry(P, I.bb, I.hh, I.n);
+            float dot = 0.f;
+            constexpr int NB = NBW * 32, PER = 64 * 16 / NB, GRP = 4;
+            for (int i0 = 0; i0 < PER; i0 += GRP) {
+                float4 e[GRP][2], h[GRP][2];
+#pragma unroll
+                for (int g = 0; g < GRP; ++g) {  // the group's loads are all in flight together
+                    const int id = (i0 + g) * NB + bt;
+                    const int pp = id >> 4, col = 64 * ((id >> 3) & 1) + 8 * (id & 7);
+                    const bool in = col < R;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        e[g][hh] = in ? *reinterpret_cast<const float4*>(src + pp * R + col + 4 * hh)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                        h[g][hh] = in ? *reinterpret_cast<const float4*>(hin + pp * R + col + 4 * hh)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < GRP; ++g) {
+                    const int id = (i0 + g) * NB + bt;
+                    const int pp = id >> 4, blk = (id >> 3) & 1, j = id & 7;
+                    const float4 e0 = e[g][0], e1 = e[g][1], h0 = h[g][0], h1 = h[g][1];
+                    dot += e0.x * h0.x + e0.y * h0.y + e0.z * h0.z + e0.w * h0.w;
+                    dot += e1.x * h1.x + e1.y * h1.y + e1.z * h1.z + e1.w * h1.w;
+                    uint4 w;
+                    w.x = tc::pack_bf16x2(e0.x, e0.y);
+                    w.y = tc::pack_bf16x2(e0.z, e0.w);
+                    w.z = tc::pack_bf16x2(e1.x, e1.y);
+                    w.w = tc::pack_bf16x2(e1.z, e1.w);
+                    *reinterpret_cast<uint4*>(dht + tc::sw128_chunk(64, blk, pp, j)) = w;
+                }
+            }
+            dot = warp_sum(dot);
+            if (lane == 0) misc[NBW * ib + bw] = dot;
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ctl->dhfull[ib]);
+        }
+        if (!ok) fail(ctl, A.err, 44);
     }
     // ---- teardown
     tc::tc_fence_before();
