@@ -6,7 +6,8 @@
 // row m = (chunk ch, per-head index p), so every per-token quantity is a 128 x r tile.
 //
 //   warp 8 (TMA)    : per token, xhat/bhat rows of both chunks (128-byte swizzle), the
-//                     token's rotation parameters and da, into a 4-stage ring.
+//                     token's rotation parameters and da, into a 4-stage ring; the copies of a
+//                     token are issued from different lanes.
 //   warp 9 (MMA)    : W_t = sum_c xhat_tc (x) bhat_tc for both chunks as ONE block-diagonal
 //                     MMA (M = 128 rows, N = 128, K = 16 = (chunk, channel) rows), into one of
 //                     two TMEM accumulators; then the moment MMAs m2 += c^T [c | 1] over the
@@ -131,33 +132,45 @@ __global__ void __launch_bounds__(NTHR, 1)
 
     if (warp == WARP_TMA) {
         // ================================================================ TMA producer
-        if (lane == 0) {
-            uint32_t q = 0;
-            for (int it = it0; it < it1 && !*abort; ++it) {
-                Item I = decode_item(A, it);
-                for (int t = 0; t < I.T[0] && !*abort; ++t, ++q) {
-                    const uint32_t s = q % NS, u = q / NS;
-                    if (u >= 1 && !tc::mbar_wait(&ctl->empty[s], (u - 1) & 1, abort)) {
-                        fail(ctl, A.err, 11);
-                        break;
-                    }
+        // The whole warp runs the loop: lane 0 arms the stage barrier and the copies of a token
+        // (xhat rows, bhat column blocks, rotation row and da of both chunks) go out from
+        // different lanes, since one copy issue costs a thread about 100 cycles.  Wait results are
+        // made warp-uniform so that all lanes leave together.
+        uint32_t q = 0;
+        bool ok = true;
+        const int nbx = 1 + R / 64, ncp = nbx + (P.rw ? 1 : 0) + 1;  // copies per token and chunk
+        for (int it = it0; it < it1 && ok; ++it) {
+            const Item I = decode_item(A, it);
+            for (int t = 0; t < I.T[0] && ok; ++t, ++q) {
+                const uint32_t s = q % NS, u = q / NS;
+                if (u >= 1) ok = __all_sync(0xffffffffu, tc::mbar_wait(&ctl->empty[s], (u - 1) & 1, abort));
+                if (!ok) break;
+                if (lane == 0) {
                     uint32_t bytes = 0;
                     for (int ch = 0; ch < 2; ++ch)
                         if (I.exists[ch]) bytes += stage_bytes(A);
                     tc::mbar_arrive_expect_tx(&ctl->full[s], bytes);
-                    for (int ch = 0; ch < 2; ++ch) {
-                        if (!I.exists[ch]) continue;
+                }
+                __syncwarp();
+                if (lane < 2 * ncp) {
+                    const int ch = lane >= ncp ? 1 : 0, kind = lane - ch * ncp;
+                    if (ch ? I.exists[1] : I.exists[0]) {
                         const int row = I.bb * P.s + (2 * I.k + ch) * FL + t;
-                        tc::tma_load_4d(sm + OFF_X + s * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row, &ctl->full[s]);
-                        for (int a = 0; a < R / 64; ++a)
-                            tc::tma_load_5d(sm + OFF_B + s * 4096 + a * 2048 + ch * 1024, &tmb, 0, a, I.hh, 0, row,
-                                            &ctl->full[s]);
-                        if (P.rw)
+                        if (kind == 0)
+                            tc::tma_load_4d(sm + OFF_X + s * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row, &ctl->full[s]);
+                        else if (kind < nbx)
+                            tc::tma_load_5d(sm + OFF_B + s * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 0, kind - 1,
+                                            I.hh, 0, row, &ctl->full[s]);
+                        else if (P.rw && kind == nbx)
                             tc::tma_load_3d(sm + OFF_ROT + s * 1024 + ch * 512, &tmr, 0, I.hh, row, &ctl->full[s]);
-                        tc::tma_load_2d(sm + OFF_DA + s * 256 + ch * 128, &tmd, I.hh & ~3, row, &ctl->full[s]);
+                        else
+                            tc::tma_load_2d(sm + OFF_DA + s * 256 + ch * 128, &tmd, I.hh & ~3, row, &ctl->full[s]);
                     }
                 }
             }
+        }
+        if (lane == 0) {
+            if (!ok) fail(ctl, A.err, 11);
             // drain: every issued stage must land before the CTA exits (own bounded wait,
             // independent of the abort flag)
             int never = 0;
