@@ -82,6 +82,12 @@ typedef enum {
  * The flag is ignored (the carries are recomputed) when the forward and the backward of the
  * problem take different kernel paths (mm_path differs), whose carry layouts differ. */
 #define MM_FLAG_REUSE_CARRIES 0x2u
+/* moments_fwd only, for testing the device failure path: on the tensor-core path every CTA of the
+ * chunk-end kernel waits once, with a short poll limit, for an mbarrier phase that nothing
+ * completes.  The bounded wait gives up, the kernels wind down without faulting or hanging, the
+ * call's m2 / m1 are invalid, and mm_device_status() then reports MM_ERR_TIMEOUT; the next call
+ * (without the flag) on the same stream and device runs normally.  Ignored on the SIMT path. */
+#define MM_FLAG_TEST_WAIT_TIMEOUT 0x80000000u
 
 typedef struct {
     int64_t b, s, C, h, p, r; /* batch, padded sequence, channels, heads, per-head dim, state rank */

@@ -26,6 +26,7 @@ MM_F32, MM_BF16 = 0, 1
 ROT = {"none": 0, "pairwise": 1, "half": 2, "quat": 3}
 MM_FLAG_FORCE_GENERIC = 0x1
 MM_FLAG_REUSE_CARRIES = 0x2
+MM_FLAG_TEST_WAIT_TIMEOUT = 0x80000000  # testing only: see include/moments.h
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda", 5: "nonfinite",
           6: "timeout"}
 
@@ -74,6 +75,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.moments_bwd.argtypes = [pp, vp, vp, fp, fp, fp, i64p, fp, fp, vp, vp, fp, fp, fp, vp,
                                         ctypes.c_size_t, vp]
             lib.moments_bwd.restype = ctypes.c_int
+            lib.mm_device_status.argtypes = [vp, vp]
+            lib.mm_device_status.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -141,8 +144,9 @@ def _valid_host(valid_len, b):
 
 
 def moments_fwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, *, workspace=None, stream=None,
-                out=None):
-    """Forward call; returns (m2, m1) fp32 on the inputs' device."""
+                out=None, extra_flags=0):
+    """Forward call; returns (m2, m1) fp32 on the inputs' device.  ``extra_flags`` are OR-ed into the
+    problem's flags (MM_FLAG_TEST_WAIT_TIMEOUT for the failure-path test)."""
     lib = load()
     _check_dev(xhat, bhat, da, rot, initial)
     dev = xhat.device
@@ -152,12 +156,19 @@ def moments_fwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, *, workspac
     ws = workspace if workspace is not None else alloc_workspace(spec, False, dev)
     vh = _valid_host(valid_len, spec.b)
     st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
-    rc = lib.moments_fwd(ctypes.byref(spec.problem()), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot),
+    rc = lib.moments_fwd(ctypes.byref(spec.problem(extra_flags)), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot),
                          _ptr(initial), ctypes.cast(vh.data_ptr(), ctypes.POINTER(ctypes.c_int64)),
                          _ptr(m2), _ptr(m1), _ptr(ws), ws.numel(), ctypes.c_void_p(st))
     if rc:
         raise MomentsError(rc, "moments_fwd")
     return m2, m1
+
+
+def device_status(workspace, stream=None) -> int:
+    """mm_device_status of the call that last used ``workspace`` (synchronises the stream)."""
+    lib = load()
+    st = stream if stream is not None else torch.cuda.current_stream(workspace.device).cuda_stream
+    return int(lib.mm_device_status(_ptr(workspace), ctypes.c_void_p(st)))
 
 
 def moments_bwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, d_m2, d_m1, *, workspace=None,

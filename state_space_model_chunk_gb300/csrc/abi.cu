@@ -260,6 +260,7 @@ mm_status moments_fwd(const mm_problem* prob, const void* xhat, const void* bhat
     A.xhat = xhat; A.bhat = bhat; A.da = da; A.rot = rot; A.initial = initial; A.m2 = m2; A.m1 = m1;
     A.Hc = at<float>(workspace, L.Hc);
     A.Dn = at<float>(workspace, L.Dn);
+    A.test_wait_timeout = (prob->flags & MM_FLAG_TEST_WAIT_TIMEOUT) ? 1 : 0;
     A.err = at<int>(workspace, 0);
     if (cudaMemsetAsync(A.err, 0, sizeof(int), cs) != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
     cudaError_t e = fast ? fast_fwd(M, A, at<char>(workspace, L.fast), cs) : generic_fwd(M, bf16, A, cs);

@@ -177,6 +177,7 @@ cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char*, cudaStream
     fa.m2 = A.m2;
     fa.m1 = A.m1;
     fa.err = A.err;
+    fa.test_wait_timeout = A.test_wait_timeout;
     if (fa.items == 0) return cudaSuccess;  // nothing valid: m2 / m1 stay zero
     TensorMaps maps;
     cudaError_t e = encode_maps(P, A.xhat, A.bhat, A.rot, A.da, &maps);

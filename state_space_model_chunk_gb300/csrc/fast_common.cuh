@@ -21,6 +21,7 @@ struct FastArgs {
     float* m2;
     float* m1;
     int* err;       // device error word (0 = fine)
+    int test_wait_timeout;  // chunk-end kernel: one wait that nothing completes (failure-path test)
 };
 
 struct TensorMaps {

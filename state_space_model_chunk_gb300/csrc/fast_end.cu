@@ -44,6 +44,7 @@ struct Ctl {
     uint64_t full[NS], scaled[NS], empty[NS];
     uint64_t accfull[2], accfree[2];
     uint64_t fin;
+    uint64_t never_done;  // nothing arrives on it: the failure-path test waits for it
     uint32_t tbase;
     int abort;
 };
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(NTHR, 2)
             tc::mbar_init(&ctl->accfree[i], 4);
         }
         tc::mbar_init(&ctl->fin, 1);
+        tc::mbar_init(&ctl->never_done, 1);
         ctl->abort = 0;
         tc::fence_barrier_init();
     }
@@ -199,6 +201,9 @@ __global__ void __launch_bounds__(NTHR, 2)
                 fail(ctl, A.err, 33);
             }
         };
+        // failure-path test: a wait that gives up after a few thousand polls, then the CTA winds
+        // down like after any other timeout
+        if (A.test_wait_timeout) check(tc::mbar_wait(&ctl->never_done, 0, abort, 1u << 12));
         for (int it = it0; it < it1; ++it, ++li) {
             const EItem I = decode(P, it);
             const int nst = (I.T + TPS - 1) / TPS;

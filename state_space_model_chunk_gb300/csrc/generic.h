@@ -4,6 +4,7 @@
 
 struct GenericPtrs {
     int reuse_carries;  // backward: Hc / Dn already hold this problem's carries (from its forward)
+    int test_wait_timeout;  // forward, tensor-core path: MM_FLAG_TEST_WAIT_TIMEOUT
     const void* xhat;
     const void* bhat;
     const float* da;

@@ -135,6 +135,7 @@ def test_flag_values_match_the_header():
     flags = dict(re.findall(r"#define\s+(MM_FLAG_[A-Z_]+)\s+(0x[0-9a-fA-F]+)u", text))
     assert int(flags["MM_FLAG_FORCE_GENERIC"], 16) == binding.MM_FLAG_FORCE_GENERIC
     assert int(flags["MM_FLAG_REUSE_CARRIES"], 16) == binding.MM_FLAG_REUSE_CARRIES
+    assert int(flags["MM_FLAG_TEST_WAIT_TIMEOUT"], 16) == binding.MM_FLAG_TEST_WAIT_TIMEOUT
     spec = Spec(1, 64, 1, 2, 8, 16, 16)
     assert spec.problem(binding.MM_FLAG_REUSE_CARRIES).flags == binding.MM_FLAG_REUSE_CARRIES
 
