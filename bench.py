@@ -41,6 +41,8 @@ from state_space_model_chunk_gb300 import binding  # noqa: E402
 from state_space_model_chunk_gb300.synthetic import WORKLOADS, make_inputs, slice_bh  # noqa: E402
 
 SM_COUNT_GB300 = 152
+L2_FLUSH_BELOW = 3 * 129 * 2**20  # operands below this size get an L2 flush between timed steps
+FLUSH_BYTES = 512 * 2**20
 
 
 def parse():
@@ -314,6 +316,12 @@ def run_ours(args):
         binding.moments_bwd(spec, src["xhat"], src["bhat"], src["da"], r_, src["initial"], vl, src["d_m2"],
                             src["d_m1"], workspace=ws_b, out=grads, reuse_carries=reuse)
 
+    # operands smaller than a few L2s would stay cached from one step to the next: then every
+    # timed step gets its own events and L2 is flushed (a 512 MB write) between steps, outside them
+    operand_bytes = sum(v.numel() * v.element_size() for v in d.values())
+    flush = operand_bytes < L2_FLUSH_BELOW
+    scratch = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+
     warm = max(args.warmup, 3)
     for _ in range(warm):
         step(d)
@@ -327,16 +335,27 @@ def run_ours(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step(d)
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    if flush:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a_, b_ in evs:
+            scratch.fill_(1)  # evicts the previous step's operands from L2 (not timed)
+            a_.record(stream)
+            step(d)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a_.elapsed_time(b_) for a_, b_ in evs) / args.steps
+    else:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step(d)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / args.steps
     if dist:
         dist.barrier()
     lib.mm_profile_enable(0)
-    ms = ev0.elapsed_time(ev1) / args.steps
     clk = clocks.stop()
     kernels = collect_kernels(lib)
     launches = sum(c for _, c in kernels.values())
@@ -457,7 +476,11 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "path_fwd": "tcgen05" if binding.path(spec, False) == 1 else "simt",
                        "path_bwd": "tcgen05" if binding.path(spec, True) == 1 else "simt",
-                       "l2": "inputs larger than L2 (operands 1.7 GB), no flush",
+                       "l2": (f"operands {operand_bytes / 2**20:.0f} MiB, L2 flushed (512 MiB write) between "
+                              f"timed steps, each step timed by its own events" if flush else
+                              f"inputs larger than L2 (operands {operand_bytes / 2**30:.2f} GiB), no flush"),
+                       "chunks64_processed": int(sum((min(int(v), w.s) + 63) // 64 for v in vl)),
+                       "chunks64_total": int(w.b * (w.s // 64)),
                        "carries": "recomputed by the backward" if args.recompute_carries
                        else "forward's, reused by the backward"},
             "e2e": e2e, "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu, "clocks": clk,

@@ -60,8 +60,8 @@ typedef enum {
     MM_ERR_UNSUPPORTED = 2, /* valid arguments outside what this build implements          */
     MM_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than mm_workspace_bytes */
     MM_ERR_CUDA = 4,        /* a CUDA launch or enqueue failed                              */
-    MM_ERR_NONFINITE = 5,   /* reserved: debug finiteness check                             */
-    MM_ERR_TIMEOUT = 6      /* reserved: a bounded device-side wait gave up                 */
+    MM_ERR_NONFINITE = 5,   /* MM_FLAG_CHECK_FINITE found a NaN / inf output (mm_device_status) */
+    MM_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up (mm_device_status)        */
 } mm_status;
 
 typedef enum { MM_F32 = 0, MM_BF16 = 1 } mm_dtype;
@@ -82,6 +82,12 @@ typedef enum {
  * The flag is ignored (the carries are recomputed) when the forward and the backward of the
  * problem take different kernel paths (mm_path differs), whose carry layouts differ. */
 #define MM_FLAG_REUSE_CARRIES 0x2u
+/* Debug check of the results ("recalculated.rs", moments_phys_fwd: the `san` pass over (m2, m1)
+ * after the chunk loop, read as a finiteness check that leaves the values unchanged): after its
+ * kernels the call enqueues one more pass over its outputs (m2, m1; or the five gradients) that
+ * marks the workspace if any element is NaN or infinite.  mm_device_status() then reports
+ * MM_ERR_NONFINITE.  Off by default; it costs one read of the outputs. */
+#define MM_FLAG_CHECK_FINITE 0x4u
 /* moments_fwd only, for testing the device failure path: on the tensor-core path every CTA of the
  * chunk-end kernel waits once, with a short poll limit, for an mbarrier phase that nothing
  * completes.  The bounded wait gives up, the kernels wind down without faulting or hanging, the
@@ -138,9 +144,12 @@ void mm_profile_enable(int on);
 int mm_profile_collect(double* total_ms, int64_t* launches, int n);
 const char* mm_kernel_name(int id);
 
-/* Reads the device error word a previous call left in `workspace` (synchronises `stream`).
- * MM_OK, or MM_ERR_TIMEOUT if a bounded device-side wait of a tensor-core kernel gave up (the
- * outputs of that call are then invalid), or MM_ERR_CUDA.  Diagnostic; calls never need it. */
+/* Reads the device status words a previous call left in `workspace` (synchronises `stream`).
+ * MM_OK; MM_ERR_TIMEOUT if a bounded device-side wait of a tensor-core kernel gave up (the
+ * outputs of that call are then invalid); MM_ERR_NONFINITE if the call ran with
+ * MM_FLAG_CHECK_FINITE and an output holds a NaN or infinity; or MM_ERR_CUDA.
+ * workspace == NULL reads the status of the last moments_fwd_noalloc call on the current device
+ * (its fixed scratch holds the same words).  Diagnostic; calls never need it. */
 mm_status mm_device_status(const void* workspace, void* stream);
 
 /* ---- forward without a caller-provided workspace ----
@@ -152,11 +161,14 @@ mm_status mm_device_status(const void* workspace, void* stream);
  * The scratch is a fixed 16 MiB array that the library keeps in device memory on every GPU that
  * loads it, until the process exits.  Problems whose forward workspace (mm_workspace_bytes(prob,
  * 0)) exceeds 16 MiB are rejected with MM_ERR_WORKSPACE before anything is enqueued.  The call
- * allocates nothing.  The first call on each device looks up the array's device address with
- * that device current; make that first call before any stream capture.  Every call on a device
- * shares the one array: calls that can overlap on the GPU (other streams, other host threads)
- * race on it, so the caller must serialise them.  The array keeps the previous call's contents;
- * each call initialises everything it reads. */
+ * allocates nothing.  It runs on the current device; `stream` must belong to that device
+ * (else MM_ERR_INVALID_ARG).  The first call on each device (and the first after that device's
+ * context was reset) looks up the array's device address with that device current; make that
+ * first call before any stream capture: made during a capture it returns MM_ERR_UNSUPPORTED.
+ * Every call on a device shares the one array: calls that can overlap on the GPU (other
+ * streams, other host threads) race on it, so the caller must serialise them.  The array keeps
+ * the previous call's contents; each call initialises everything it reads.  Device-side status
+ * (a bounded wait that gave up, MM_FLAG_CHECK_FINITE) is read with mm_device_status(NULL, stream). */
 mm_status moments_fwd_noalloc(const mm_problem* prob, const void* xhat, const void* bhat, const float* da,
                               const float* rot, const float* initial, const int64_t* valid_len_host,
                               float* m2, float* m1, void* stream);

@@ -16,6 +16,7 @@ from __future__ import annotations
 import ctypes
 import os
 import threading
+import warnings
 from dataclasses import dataclass
 
 import torch
@@ -26,6 +27,7 @@ MM_F32, MM_BF16 = 0, 1
 ROT = {"none": 0, "pairwise": 1, "half": 2, "quat": 3}
 MM_FLAG_FORCE_GENERIC = 0x1
 MM_FLAG_REUSE_CARRIES = 0x2
+MM_FLAG_CHECK_FINITE = 0x4  # debug: outputs checked for NaN / inf, reported by device_status()
 MM_FLAG_TEST_WAIT_TIMEOUT = 0x80000000  # testing only: see include/moments.h
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda", 5: "nonfinite",
           6: "timeout"}
@@ -77,6 +79,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.moments_bwd.restype = ctypes.c_int
             lib.mm_device_status.argtypes = [vp, vp]
             lib.mm_device_status.restype = ctypes.c_int
+            lib.moments_fwd_noalloc.argtypes = [pp, vp, vp, fp, fp, fp, i64p, fp, fp, vp]
+            lib.moments_fwd_noalloc.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -119,6 +123,26 @@ def path(spec: Spec, backward: bool) -> int:
     return int(load().mm_path(ctypes.byref(spec.problem()), 1 if backward else 0))
 
 
+_warned = set()
+
+TC_RULES = ("bf16 operands, p = 64, r in {64, 128}, h % 4 == 0, s % 64 == 0, C <= 8 (C <= 4 in the "
+            "backward), rotation width (rope_dim/2 or 4 J) a multiple of 4 and at most 128")
+
+
+def _note_path(spec: Spec, backward: bool):
+    """Warn (once per problem shape) when a bf16 call falls to the SIMT kernels, which are about
+    65x slower than the tensor-core kernels; mm_path() gives the same answer programmatically."""
+    if spec.dtype != "bf16" or spec.force_generic:
+        return
+    key = (spec, backward)
+    if key in _warned:
+        return
+    _warned.add(key)
+    if path(spec, backward) == 0:
+        warnings.warn(f"moments_{'bwd' if backward else 'fwd'}: this bf16 problem runs on the SIMT kernels; "
+                      f"the tensor-core kernels need {TC_RULES}", RuntimeWarning, stacklevel=3)
+
+
 def alloc_workspace(spec: Spec, backward: bool, device) -> torch.Tensor:
     n = max(workspace_bytes(spec, backward), 256)
     return torch.empty(n, dtype=torch.uint8, device=device)
@@ -144,42 +168,52 @@ def _valid_host(valid_len, b):
 
 
 def moments_fwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, *, workspace=None, stream=None,
-                out=None, extra_flags=0):
+                out=None, extra_flags=0, check_finite=False):
     """Forward call; returns (m2, m1) fp32 on the inputs' device.  ``extra_flags`` are OR-ed into the
-    problem's flags (MM_FLAG_TEST_WAIT_TIMEOUT for the failure-path test)."""
+    problem's flags (MM_FLAG_TEST_WAIT_TIMEOUT for the failure-path test); ``check_finite`` sets
+    MM_FLAG_CHECK_FINITE (read the result with :func:`device_status` on the same workspace)."""
     lib = load()
     _check_dev(xhat, bhat, da, rot, initial)
+    _note_path(spec, False)
+    if check_finite:
+        extra_flags |= MM_FLAG_CHECK_FINITE
     dev = xhat.device
     m2, m1 = out if out is not None else (
         torch.empty((spec.b, spec.h, spec.r, spec.r), dtype=torch.float32, device=dev),
         torch.empty((spec.b, spec.h, spec.r), dtype=torch.float32, device=dev))
     ws = workspace if workspace is not None else alloc_workspace(spec, False, dev)
     vh = _valid_host(valid_len, spec.b)
-    st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
-    rc = lib.moments_fwd(ctypes.byref(spec.problem(extra_flags)), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot),
-                         _ptr(initial), ctypes.cast(vh.data_ptr(), ctypes.POINTER(ctypes.c_int64)),
-                         _ptr(m2), _ptr(m1), _ptr(ws), ws.numel(), ctypes.c_void_p(st))
+    with torch.cuda.device(dev):  # the kernels launch on the current device
+        st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+        rc = lib.moments_fwd(ctypes.byref(spec.problem(extra_flags)), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot),
+                             _ptr(initial), ctypes.cast(vh.data_ptr(), ctypes.POINTER(ctypes.c_int64)),
+                             _ptr(m2), _ptr(m1), _ptr(ws), ws.numel(), ctypes.c_void_p(st))
     if rc:
         raise MomentsError(rc, "moments_fwd")
     return m2, m1
 
 
-def device_status(workspace, stream=None) -> int:
-    """mm_device_status of the call that last used ``workspace`` (synchronises the stream)."""
+def device_status(workspace, stream=None, device=None) -> int:
+    """mm_device_status of the call that last used ``workspace`` (synchronises the stream); with
+    ``workspace=None``, of the last :func:`moments_fwd_noalloc` call on ``device``."""
     lib = load()
-    st = stream if stream is not None else torch.cuda.current_stream(workspace.device).cuda_stream
-    return int(lib.mm_device_status(_ptr(workspace), ctypes.c_void_p(st)))
+    dev = workspace.device if workspace is not None else torch.device(device if device is not None else "cuda")
+    with torch.cuda.device(dev):
+        st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+        return int(lib.mm_device_status(_ptr(workspace), ctypes.c_void_p(st)))
 
 
 def moments_bwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, d_m2, d_m1, *, workspace=None,
-                stream=None, out=None, reuse_carries=False):
+                stream=None, out=None, reuse_carries=False, check_finite=False):
     """Backward call; returns dict d_xhat, d_bhat, d_da, d_rot, d_initial.  ``reuse_carries``:
     ``workspace`` (sized for the backward) went through :func:`moments_fwd` of the same spec and
-    unchanged inputs, whose chunk carries the backward then takes instead of recomputing them."""
+    unchanged inputs, whose chunk carries the backward then takes instead of recomputing them.
+    ``check_finite`` sets MM_FLAG_CHECK_FINITE over the five gradients."""
     if reuse_carries and workspace is None:
         raise ValueError("reuse_carries needs the workspace the forward wrote")
     lib = load()
     _check_dev(xhat, bhat, da, rot, initial, d_m2, d_m1)
+    _note_path(spec, True)
     dev = xhat.device
     if out is None:
         out = dict(d_xhat=torch.empty_like(xhat), d_bhat=torch.empty_like(bhat), d_da=torch.empty_like(da),
@@ -187,13 +221,15 @@ def moments_bwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, d_m2, d_m1,
                    d_initial=torch.empty_like(initial))
     ws = workspace if workspace is not None else alloc_workspace(spec, True, dev)
     vh = _valid_host(valid_len, spec.b)
-    st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
-    prob = spec.problem(MM_FLAG_REUSE_CARRIES if reuse_carries else 0)
-    rc = lib.moments_bwd(ctypes.byref(prob), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot),
-                         _ptr(initial), ctypes.cast(vh.data_ptr(), ctypes.POINTER(ctypes.c_int64)),
-                         _ptr(d_m2), _ptr(d_m1), _ptr(out["d_xhat"]), _ptr(out["d_bhat"]),
-                         _ptr(out["d_da"]), _ptr(out["d_rot"]), _ptr(out["d_initial"]), _ptr(ws),
-                         ws.numel(), ctypes.c_void_p(st))
+    prob = spec.problem((MM_FLAG_REUSE_CARRIES if reuse_carries else 0) |
+                        (MM_FLAG_CHECK_FINITE if check_finite else 0))
+    with torch.cuda.device(dev):  # the kernels launch on the current device
+        st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+        rc = lib.moments_bwd(ctypes.byref(prob), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot),
+                             _ptr(initial), ctypes.cast(vh.data_ptr(), ctypes.POINTER(ctypes.c_int64)),
+                             _ptr(d_m2), _ptr(d_m1), _ptr(out["d_xhat"]), _ptr(out["d_bhat"]),
+                             _ptr(out["d_da"]), _ptr(out["d_rot"]), _ptr(out["d_initial"]), _ptr(ws),
+                             ws.numel(), ctypes.c_void_p(st))
     if rc:
         raise MomentsError(rc, "moments_bwd")
     return out
@@ -201,22 +237,21 @@ def moments_bwd(spec: Spec, xhat, bhat, da, rot, initial, valid_len, d_m2, d_m1,
 
 def moments_fwd_noalloc(spec: Spec, xhat, bhat, da, rot, initial, valid_len, *, stream=None, out=None):
     """Forward through ``moments_fwd_noalloc``: no workspace is passed or allocated; the library
-    uses its fixed 16 MiB device scratch (for callers that cannot allocate).  Calls that could
-    overlap on the GPU must be serialised by the caller."""
+    uses its fixed 16 MiB device scratch (for callers that cannot allocate).  Runs with the
+    inputs' device current.  Calls that could overlap on the GPU must be serialised by the
+    caller; :func:`device_status` with ``workspace=None`` reads the call's device status."""
     lib = load()
-    fn = lib.moments_fwd_noalloc
-    fn.argtypes = [ctypes.POINTER(Problem)] + [ctypes.c_void_p] * 5 + [ctypes.POINTER(ctypes.c_int64)] + \
-        [ctypes.c_void_p] * 3
-    fn.restype = ctypes.c_int
     _check_dev(xhat, bhat, da, rot, initial)
     dev = xhat.device
     m2, m1 = out if out is not None else (
         torch.empty((spec.b, spec.h, spec.r, spec.r), dtype=torch.float32, device=dev),
         torch.empty((spec.b, spec.h, spec.r), dtype=torch.float32, device=dev))
     vh = _valid_host(valid_len, spec.b)
-    st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
-    rc = fn(ctypes.byref(spec.problem()), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot), _ptr(initial),
-            ctypes.cast(vh.data_ptr(), ctypes.POINTER(ctypes.c_int64)), _ptr(m2), _ptr(m1), ctypes.c_void_p(st))
+    with torch.cuda.device(dev):  # the library takes the scratch of the current device
+        st = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+        rc = lib.moments_fwd_noalloc(ctypes.byref(spec.problem()), _ptr(xhat), _ptr(bhat), _ptr(da), _ptr(rot),
+                                     _ptr(initial), ctypes.cast(vh.data_ptr(), ctypes.POINTER(ctypes.c_int64)),
+                                     _ptr(m2), _ptr(m1), ctypes.c_void_p(st))
     if rc:
         raise MomentsError(rc, "moments_fwd_noalloc")
     return m2, m1

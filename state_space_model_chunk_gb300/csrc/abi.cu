@@ -7,14 +7,16 @@
 #include "../../include/moments.h"
 #include "common.cuh"
 #include "fast.h"
+#include "finite.h"
 #include "generic.h"
+#include "noalloc.h"
 #include "prof.h"
 
 namespace {
 
 constexpr size_t kAlign = 256;
 constexpr int kTrajSlots = 320;  // blocks of the SIMT backward (>= 2 per SM on 152 SMs)
-constexpr size_t kHeader = 256;  // workspace header: device error word at offset 0
+constexpr size_t kHeader = 256;  // workspace header: status words (timeout at offset 0, non-finite at 4)
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -106,6 +108,12 @@ Layout layout(const mm_problem* P, int backward) {
         L.traj = off; off = align_up(off + sizeof(float) * (size_t)kTrajSlots * P->chunk_len * pr);
     }
     L.total = off;
+    if (backward) {
+        // a backward-sized workspace also serves the forward (MM_FLAG_REUSE_CARRIES hands one
+        // workspace to both calls)
+        const size_t fwd_total = layout(P, 0).total;
+        if (fwd_total > L.total) L.total = fwd_total;
+    }
     return L;
 }
 
@@ -150,7 +158,7 @@ cudaEvent_t take_event() {
 }
 const char* kKernelNames[KID_COUNT] = {
     "chunk_end", "carry_scan", "fwd_chunk", "dsym", "bwd_chunk", "cot_scan", "correct",
-    "tc_fwd_chunk", "tc_chunk_end", "tc_bwd_chunk", "tc_correct"};
+    "tc_fwd_chunk", "tc_chunk_end", "tc_bwd_chunk", "tc_correct", "check_finite", "m2_reduce"};
 }  // namespace
 
 void mm_prof_mark(int kid, int begin, cudaStream_t st) {
@@ -213,15 +221,22 @@ int mm_profile_collect(double* total_ms, int64_t* launches, int n) {
 const char* mm_kernel_name(int id) { return (id >= 0 && id < KID_COUNT) ? kKernelNames[id] : "?"; }
 
 mm_status mm_device_status(const void* workspace, void* stream) {
-    if (!workspace) return MM_ERR_INVALID_ARG;
-    int v = 0;
+    if (!workspace) {  // the fixed scratch of moments_fwd_noalloc on the current device
+        void* p = nullptr;
+        const mm_status st = noalloc_scratch(stream, &p);
+        if (st != MM_OK) return st;
+        workspace = p;
+    }
+    int v[2] = {0, 0};  // [0]: a bounded device wait gave up; [1]: the finiteness check fired
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+    if (cudaMemcpyAsync(v, workspace, sizeof(v), cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
         cudaStreamSynchronize(cs) != cudaSuccess) {
         cudaGetLastError();
         return MM_ERR_CUDA;
     }
-    return v ? MM_ERR_TIMEOUT : MM_OK;
+    if (v[0]) return MM_ERR_TIMEOUT;
+    if (v[1]) return MM_ERR_NONFINITE;
+    return MM_OK;
 }
 
 const char* mm_status_string(mm_status s) {
@@ -262,8 +277,15 @@ mm_status moments_fwd(const mm_problem* prob, const void* xhat, const void* bhat
     A.Dn = at<float>(workspace, L.Dn);
     A.test_wait_timeout = (prob->flags & MM_FLAG_TEST_WAIT_TIMEOUT) ? 1 : 0;
     A.err = at<int>(workspace, 0);
-    if (cudaMemsetAsync(A.err, 0, sizeof(int), cs) != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
+    if (cudaMemsetAsync(A.err, 0, 2 * sizeof(int), cs) != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
     cudaError_t e = fast ? fast_fwd(M, A, at<char>(workspace, L.fast), cs) : generic_fwd(M, bf16, A, cs);
+    if (e == cudaSuccess && (prob->flags & MM_FLAG_CHECK_FINITE)) {
+        FiniteSegs fs{};
+        fs.n = 2;
+        fs.ptr[0] = m2; fs.bytes[0] = (int64_t)(sizeof(float) * nbh * prob->r * prob->r);
+        fs.ptr[1] = m1; fs.bytes[1] = (int64_t)(sizeof(float) * nbh * prob->r);
+        e = launch_finite_check(fs, at<int>(workspace, 4), cs);
+    }
     if (e != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
     return MM_OK;
 }
@@ -301,7 +323,7 @@ mm_status moments_bwd(const mm_problem* prob, const void* xhat, const void* bhat
     A.E = at<float>(workspace, L.E);
     A.dsym = at<float>(workspace, L.dsym);
     A.err = at<int>(workspace, 0);
-    if (cudaMemsetAsync(A.err, 0, sizeof(int), cs) != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
+    if (cudaMemsetAsync(A.err, 0, 2 * sizeof(int), cs) != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
     cudaError_t e;
     if (fast) {
         e = fast_bwd(M, A, at<char>(workspace, L.fast), cs);
@@ -318,6 +340,20 @@ mm_status moments_bwd(const mm_problem* prob, const void* xhat, const void* bhat
         int64_t chunks = (int64_t)prob->b * prob->h * (prob->s / prob->chunk_len);
         int grid = (int)(chunks < kTrajSlots ? chunks : kTrajSlots);
         e = generic_bwd(M, bf16, A, grid, cs);
+    }
+    if (e == cudaSuccess && (prob->flags & MM_FLAG_CHECK_FINITE)) {
+        FiniteSegs fs{};
+        const void* outs[5] = {d_xhat, d_bhat, d_da, d_rot, d_initial};
+        const size_t nbytes[5] = {es * nx, es * nb, sizeof(float) * ntok * prob->h, sizeof(float) * nrot,
+                                  sizeof(float) * (size_t)prob->b * prob->h * prob->p * prob->r};
+        for (int i = 0; i < 5; ++i) {
+            if (!outs[i] || !nbytes[i]) continue;
+            fs.ptr[fs.n] = outs[i];
+            fs.bytes[fs.n] = (int64_t)nbytes[i];
+            fs.bf16[fs.n] = (i < 2 && bf16) ? 1 : 0;
+            ++fs.n;
+        }
+        e = launch_finite_check(fs, at<int>(workspace, 4), cs);
     }
     if (e != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
     return MM_OK;

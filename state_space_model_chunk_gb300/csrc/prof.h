@@ -14,6 +14,8 @@ enum MMKernelId {
     KID_FAST_END,
     KID_FAST_BWD,
     KID_FAST_CORRECT,
+    KID_FINITE,
+    KID_M2_REDUCE,
     KID_COUNT
 };
 

@@ -1,4 +1,7 @@
-"""Shared test helpers: the oracle on torch inputs, and the normwise error metric."""
+"""Shared test helpers: the oracle on torch inputs, the error metrics, and the parity report."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -35,6 +38,50 @@ def rel_err(got, ref):
     return float(num / den)
 
 
+def max_rel_err(got, ref):
+    """Element-wise error against the tensor's scale: max |got - ref| / max |ref| (0/0 -> 0).
+
+    Unlike the normwise figure, one wrong element (an angle, a chunk-boundary d_da) cannot hide
+    behind the rest of the tensor: it shows at its own size relative to the largest value."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    den = float(np.max(np.abs(ref)))
+    num = float(np.max(np.abs(got - ref)))
+    if den == 0.0:
+        return num
+    return num / den
+
+
 def tolerance(w):
-    """fp32 inputs: 1e-4; bf16 inputs: 2e-2 (normwise, per output tensor)."""
+    """fp32 inputs: 1e-4; bf16 inputs: 2e-2 -- both normwise and element-wise (max-abs error over
+    the tensor's max |value|), per output tensor."""
     return 1e-4 if w.dtype == "f32" else 2e-2
+
+
+def report(label, errs):
+    """Append one line of per-tensor errors to the file named by $PARITY_REPORT, if set."""
+    path = os.environ.get("PARITY_REPORT")
+    if not path:
+        return
+    with open(path, "a") as f:
+        f.write(json.dumps({"case": label, "errors": errs}) + "\n")
+
+
+def compare(label, tol, pairs):
+    """Check every (name, got, ref) pair normwise and element-wise against `tol`; returns
+    {name: {"norm": e, "max": e}} and asserts with the full table on failure."""
+    errs = {}
+    for name, got, ref in pairs:
+        ref = np.asarray(ref, dtype=np.float64)
+        if ref.size == 0:
+            continue
+        g = got.detach().to("cpu", torch.float64).numpy() if isinstance(got, torch.Tensor) else np.asarray(got)
+        assert g.shape == ref.shape, (label, name, g.shape, ref.shape)
+        assert np.all(np.isfinite(g)), (label, name, "non-finite values")
+        errs[name] = {"norm": rel_err(g, ref), "max": max_rel_err(g, ref)}
+    report(label, errs)
+    bad = {k: v for k, v in errs.items() if not (v["norm"] <= tol and v["max"] <= tol)}
+    assert not bad, f"{label}: errors above {tol}: {bad} (all: {errs})"
+    return errs

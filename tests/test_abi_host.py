@@ -136,6 +136,7 @@ def test_flag_values_match_the_header():
     assert int(flags["MM_FLAG_FORCE_GENERIC"], 16) == binding.MM_FLAG_FORCE_GENERIC
     assert int(flags["MM_FLAG_REUSE_CARRIES"], 16) == binding.MM_FLAG_REUSE_CARRIES
     assert int(flags["MM_FLAG_TEST_WAIT_TIMEOUT"], 16) == binding.MM_FLAG_TEST_WAIT_TIMEOUT
+    assert int(flags["MM_FLAG_CHECK_FINITE"], 16) == binding.MM_FLAG_CHECK_FINITE
     spec = Spec(1, 64, 1, 2, 8, 16, 16)
     assert spec.problem(binding.MM_FLAG_REUSE_CARRIES).flags == binding.MM_FLAG_REUSE_CARRIES
 
@@ -147,3 +148,17 @@ def test_reuse_carries_needs_the_forward_workspace():
     x = torch.zeros((1, 64, 1, 2, 8))
     with pytest.raises(ValueError):
         binding.moments_bwd(spec, x, x, x, None, x, [60], x, x, reuse_carries=True)
+
+
+def test_check_finite_flag_is_accepted_and_changes_no_sizing():
+    """MM_FLAG_CHECK_FINITE (0x4) is a valid flag: the workspace size and the kernel path of a
+    problem do not depend on it (the check runs in the workspace header)."""
+    lib = binding.load()
+    for spec in (base_spec(), Spec(2, 256, 2, 4, 64, 128, 64, "pairwise", 64)):
+        for bwd in (0, 1):
+            plain = lib.mm_workspace_bytes(ctypes.byref(spec.problem()), bwd)
+            flagged = lib.mm_workspace_bytes(ctypes.byref(spec.problem(binding.MM_FLAG_CHECK_FINITE)), bwd)
+            assert plain == flagged > 0
+            assert lib.mm_path(ctypes.byref(spec.problem()), bwd) == \
+                lib.mm_path(ctypes.byref(spec.problem(binding.MM_FLAG_CHECK_FINITE)), bwd)
+    assert lib.mm_status_string(5) == b"non-finite values detected"
