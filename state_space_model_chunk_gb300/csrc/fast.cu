@@ -162,9 +162,11 @@ bool fast_supported(const MMParams& P, bool bf16, int backward) {
     return true;
 }
 
-size_t fast_scratch_bytes(const MMParams&, int backward) { return backward ? fastk::bwd_anchor_bytes() : 0; }
+size_t fast_scratch_bytes(const MMParams& P, int backward) {
+    return backward ? fastk::bwd_anchor_bytes() : fastk::fwd_partial_bytes(internal_params(P));
+}
 
-cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char*, cudaStream_t st) {
+cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cudaStream_t st) {
     using namespace fastk;
     const MMParams P = internal_params(P0);
     FastArgs fa;
@@ -176,13 +178,15 @@ cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char*, cudaStream
     fa.Dn = A.Dn;
     fa.m2 = A.m2;
     fa.m1 = A.m1;
+    fa.m2p = reinterpret_cast<float*>(scratch);
     fa.err = A.err;
     fa.test_wait_timeout = A.test_wait_timeout;
     if (fa.items == 0) return cudaSuccess;  // nothing valid: m2 / m1 stay zero
     TensorMaps maps;
     cudaError_t e = encode_maps(P, A.xhat, A.bhat, A.rot, A.da, &maps);
     if (e != cudaSuccess) return e;
-    const int grid = fa.items < sm_count() ? fa.items : sm_count();
+    int grid = fa.items < sm_count() ? fa.items : sm_count();
+    if (grid > kMaxFwdGrid) grid = kMaxFwdGrid;
     if ((e = launch_tc_end(fa, maps, st)) != cudaSuccess) return e;
     if ((e = generic_carry_scan(P, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
     return launch_tc_fwd(fa, maps, grid, st);

@@ -57,11 +57,13 @@ constexpr uint32_t OFF_ACUM = 174080;            // cumulative da, 2 chunks x 64
 constexpr uint32_t OFF_COEF = 174592;            // span cos|sin: 8 tokens x 2 chunks x 128 fp32
 constexpr uint32_t OFF_LT = 182784;              // span decay matrix L: 2 chunks x 8 x 8 fp32
 constexpr uint32_t OFF_M1T = 184320;             // d_m1 as a K = 16 MMA operand: rows hi | lo (bf16) | 0
-constexpr uint32_t OFF_PTR = 188416;             // per compute thread: 4 output row pointers of the item
+constexpr uint32_t OFF_PTR = 188416;             // per compute thread: 3 output row pointers of the item
+constexpr uint32_t OFF_DDA = 194560;             // d_da partials of the item: [2 chunks][64 tokens][4 warps]
 constexpr uint32_t OFF_CTL = 196608;
 constexpr uint32_t SMEM_BYTES = OFF_CTL + 512 + 1024;
 static_assert(OFF_SX % 1024 == 0 && OFF_SB % 1024 == 0 && OFF_PA % 1024 == 0 && OFF_M1T % 1024 == 0, "tiles");
 static_assert(OFF_ROT % 128 == 0 && OFF_IDA % 128 == 0 && OFF_CTL % 8 == 0, "tensor-copy slots");
+static_assert(OFF_PTR + 256 * 3 * 8 <= OFF_DDA && OFF_DDA + 2 * 64 * 4 * 4 <= OFF_CTL, "pointer table, d_da partials");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Ctl {
@@ -548,16 +550,18 @@ __global__ void __launch_bounds__(NTHR, 1)
             const bool half_ok = half ? I.exists[1] : I.exists[0];
             // this thread's output rows for token 0 of the item (null where it writes none): the
             // per-token steps only add the token stride
-            uint64_t* ptab = reinterpret_cast<uint64_t*>(sm + OFF_PTR) + ctid * 4;
+            uint64_t* ptab = reinterpret_cast<uint64_t*>(sm + OFF_PTR) + ctid * 3;
             ptab[0] = (half == 0 && chunk_ok) ? reinterpret_cast<uint64_t>(B.dx + off_x(P, I.bb, n * FL, 0, I.hh) + pp)
                                               : 0ull;
             ptab[1] = (m < R && half_ok)
                           ? reinterpret_cast<uint64_t>(B.db + off_b(P, I.bb, (2 * I.k + half) * FL, 0, I.hh) + m)
                           : 0ull;
-            ptab[2] = reinterpret_cast<uint64_t>(B.dda + off_da(P, I.bb, n * FL, I.hh));
-            ptab[3] = (P.rw > 0 && chunk_ok && n < I.proc)
+            ptab[2] = (P.rw > 0 && chunk_ok && n < I.proc)
                           ? reinterpret_cast<uint64_t>(B.drot + off_rot(P, I.bb, n * FL, I.hh))
                           : 0ull;
+            // this warp's d_da partials for its chunk (the four warps of a chunk are summed in a
+            // fixed order at the end of the item, so that d_da does not depend on timing)
+            float* ddap = reinterpret_cast<float*>(sm + OFF_DDA) + ch * 64 * 4 + ((warp & 1) + 2 * half);
             ok &= tc::mbar_wait(&ctl->itemfull, pr.next(B_ITEM), abort);
             // ---- item set-up: cumulative da of both chunks; D + D^T and d_m1 when (b,h) changes
             if (warp < 2) {
@@ -813,8 +817,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         }
                         // d_da_{t+1} = e_{t+1} <g_{t+1}, h_t>  (g holds g_{t+1} here)
                         const float dot = warp_sum((dotv[0] + dotv[1]) + (dotv[2] + dotv[3]));
-                        if (lane == 0 && t + 1 < I.T[0] && chunk_ok && n < I.proc)
-                            atomicAdd(reinterpret_cast<float*>(ptab[2]) + (int64_t)(t + 1) * P.h, e_of(t + 1) * dot);
+                        if (lane == 0 && t + 1 < I.T[0]) ddap[(t + 1) * 4] = e_of(t + 1) * dot;
                     };
                     // ---- d_c -> d_rot, G, cotangent recurrence -> g tile
                     auto step_g = [&](int t) {
@@ -824,7 +827,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         const bool live = t < Tch;
                         const float* cf = coefs + (o * 2 + ch) * 128;
                         const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + ch * 512);
-                        float* const drot_t = ptab[3] ? reinterpret_cast<float*>(ptab[3]) + (int64_t)t * P.h * P.rw
+                        float* const drot_t = ptab[2] ? reinterpret_cast<float*>(ptab[2]) + (int64_t)t * P.h * P.rw
                                                       : nullptr;
                         const bool rot_out = drot_t != nullptr;
                         if (!live) {  // past valid_len: d_c = 0, so g_t = e_{t+1} g_{t+1}
@@ -998,7 +1001,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         for (int e = 0; e < 16; ++e) dot = fmaf(gr[g][e], an[e], dot);
                     }
                     dot = warp_sum(dot);
-                    if (lane == 0 && Tch > 0) atomicAdd(B.dda + off_da(P, I.bb, n * FL, I.hh), e_of(0) * dot);
+                    if (lane == 0 && Tch > 0) ddap[0] = e_of(0) * dot;
                     if (Tch > 0) {
                         const float e0 = e_of(0);
                         float* dst = B.E + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
@@ -1012,6 +1015,16 @@ __global__ void __launch_bounds__(NTHR, 1)
                                         e0 * gr[g][e], e0 * gr[g][e + 1], e0 * gr[g][e + 2], e0 * gr[g][e + 3]);
                             }
                     }
+                }
+            }
+            // ---- d_da of the item's valid tokens: the four warps' partials of each chunk, in order
+            named_barrier_sync(2, NCW * 32);
+            if (ctid < 128) {
+                const int c2 = ctid >> 6, t = ctid & 63, n2 = 2 * I.k + c2;
+                const int T2 = c2 ? I.T[1] : I.T[0];
+                if (t < T2 && n2 < I.proc) {
+                    const float* pq = reinterpret_cast<const float*>(sm + OFF_DDA) + (c2 * 64 + t) * 4;
+                    B.dda[off_da(P, I.bb, n2 * FL + t, I.hh)] = ((pq[0] + pq[1]) + pq[2]) + pq[3];
                 }
             }
             __syncwarp();

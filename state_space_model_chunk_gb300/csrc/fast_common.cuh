@@ -20,6 +20,8 @@ struct FastArgs {
     float* Dn;      // [b,h,nc] chunk decays
     float* m2;
     float* m1;
+    float* m2p;     // forward: per-CTA partial moments of (b,h) shared with other CTAs, 2 slots per CTA
+                    // of r*r (m2) + r (m1) floats, summed in CTA order by the reduce kernel
     int* err;       // device error word (0 = fine)
     int test_wait_timeout;  // chunk-end kernel: one wait that nothing completes (failure-path test)
 };
@@ -32,6 +34,7 @@ struct TensorMaps {
 };
 
 constexpr int kMaxBwdGrid = 160;  // CTAs of the backward kernels (anchor slots in the workspace)
+constexpr int kMaxFwdGrid = 160;  // CTAs of the forward kernel (partial-moment slots in the workspace)
 
 __host__ __device__ inline int pairs_of(const MMParams& P, int bb) { return (mm_processed(P, bb) + 1) / 2; }
 
@@ -65,6 +68,10 @@ __device__ inline void locate(const FastArgs& A, int item, int& bb, int& hh, int
 
 __device__ inline int item_begin(const FastArgs& A, int cta) {
     return (int)(((int64_t)cta * A.items) / gridDim.x);
+}
+// The same for a kernel whose grid is not the one that walked the items.
+__host__ __device__ inline int item_begin_of(int items, int grid, int cta) {
+    return (int)(((int64_t)cta * items) / grid);
 }
 
 __device__ inline Item decode_item(const FastArgs& A, int item) {
@@ -198,6 +205,7 @@ cudaError_t encode_grad_maps(const MMParams& P, const void* dx, const void* db, 
 cudaError_t launch_tc_corr(const FastArgs& fa, const float* da, const float* E, void* dx, void* db, float* dda,
                            const TensorMaps& maps, cudaStream_t st);
 size_t bwd_anchor_bytes();
+size_t fwd_partial_bytes(const MMParams& P);  // internal chunking (nc = s / 64)
 cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, const float* dm2, const float* dm1, void* dx,
                           void* db, float* dda, float* drot, const TensorMaps& maps, int grid, cudaStream_t st);
 

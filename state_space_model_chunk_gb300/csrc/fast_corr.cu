@@ -45,10 +45,11 @@ constexpr uint32_t SL_DX = 3, SL_DB = 4;   // slot indices of d_xhat / d_bhat
 constexpr uint32_t DHT = 16384;            // dH tile: 64 rows x 2 blocks x 128 B
 constexpr uint32_t OFF_DH = NS * STAGE;    // 2 dH tiles
 constexpr uint32_t OFF_SC = OFF_DH + 2 * DHT;   // sc_t, 2 items x 64 fp32
-constexpr uint32_t OFF_OM = OFF_SC + 512;       // omega, 2 items x 64 fp32
-constexpr uint32_t OFF_MISC = OFF_OM + 512;     // dot partials [item][builder warp], then D_n [item]
+constexpr uint32_t OFF_OM = OFF_SC + 512;       // omega of the item, 64 fp32
+constexpr uint32_t OFF_OMR = OFF_OM + 256;      // <xhat, U> of every stage row: [2 stages][128 rows] fp32
+constexpr uint32_t OFF_MISC = OFF_OMR + 1024;   // dot partials [item][builder warp], then D_n [item]
 constexpr uint32_t OFF_CTL = OFF_MISC + 64;
-constexpr uint32_t SMEM_BYTES = OFF_CTL + 256 + 1024;
+constexpr uint32_t SMEM_BYTES = OFF_CTL + 128 + 1024;
 static_assert(OFF_DH % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -61,7 +62,7 @@ struct Ctl {
     uint32_t tbase;
     int abort;
 };
-static_assert(sizeof(Ctl) <= 256, "control block");
+static_assert(sizeof(Ctl) <= 128, "control block");
 
 constexpr uint32_t TM_BUF = 256;  // per accumulator buffer: U at +0 (64 columns), V at +64 (r columns)
 
@@ -257,10 +258,11 @@ __global__ void __launch_bounds__(NTHR, 1)
                 fail(ctl, A.err, 43);
             }
         };
+        float* om = reinterpret_cast<float*>(sm + OFF_OM);
+        float* omr = reinterpret_cast<float*>(sm + OFF_OMR);
         for (int it = it0; it < it1; ++it, ++li) {
             const CItem I = decode(P, it);
             const uint32_t ib = li & 1;
-            float* om = reinterpret_cast<float*>(sm + OFF_OM) + ib * 64;
             const float* sc = reinterpret_cast<const float*>(sm + OFF_SC) + ib * 64;
             check(tc::mbar_wait(&ctl->dhfull[ib], (li >> 1) & 1, abort));  // sc, D_n and the dot are ready
             // ---- the two 32-token stages
@@ -277,23 +279,35 @@ __global__ void __launch_bounds__(NTHR, 1)
                 tc::tmem_ld16(tu + 16 * qf, u);
                 tc::tmem_wait_ld();
                 unsigned char* const stg = sm + s * STAGE;
-                // omega partial: <xhat row, U row> over this quarter (xhat row from the stage tile)
-                float w = 0.f;
-                {
+                // <xhat row, U row> over all p columns, by the row's first-quarter thread alone
+                // (one thread, one fixed order: the sum does not depend on timing)
+                if (qf == 0) {
+                    float w = 0.f;
                     const unsigned char* xr = stg + k * 128;
+#pragma unroll 1
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        float uq[16];
+                        if (q2 == 0) {
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        const int j = 2 * qf + jj;
-                        const uint4 v = *reinterpret_cast<const uint4*>(xr + ((j ^ (k & 7)) << 4));
-                        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+                            for (int e = 0; e < 16; ++e) uq[e] = u[e];
+                        } else {
+                            tc::tmem_ld16(tu + 16 * q2, uq);
+                            tc::tmem_wait_ld();
+                        }
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            w = fmaf(__uint_as_float(wd[e] << 16), u[8 * jj + 2 * e], w);
-                            w = fmaf(__uint_as_float(wd[e] & 0xFFFF0000u), u[8 * jj + 2 * e + 1], w);
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int j = 2 * q2 + jj;
+                            const uint4 v = *reinterpret_cast<const uint4*>(xr + ((j ^ (k & 7)) << 4));
+                            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                w = fmaf(__uint_as_float(wd[e] << 16), uq[8 * jj + 2 * e], w);
+                                w = fmaf(__uint_as_float(wd[e] & 0xFFFF0000u), uq[8 * jj + 2 * e + 1], w);
+                            }
                         }
                     }
+                    if (row_ok) omr[st * 128 + k] = w;
                 }
-                if (row_ok) atomicAdd(&om[t], w);
                 const float scv = sc[t];
                 if (row_ok) {  // d_xhat row += sc U, in the stage's d_xhat slot (same layout as xhat)
                     unsigned char* dr = stg + SL_DX * SLOT + k * 128;
@@ -345,7 +359,14 @@ __global__ void __launch_bounds__(NTHR, 1)
                     tc::mbar_arrive(&ctl->upd[s]);
                 }
             }
-            named_barrier_sync(1, NEW * 32);  // omega complete
+            named_barrier_sync(1, NEW * 32);  // every row's <xhat, U> is in
+            if (etid < FL) {  // omega_t: the token's C rows, in channel order
+                const float* pr = omr + (etid / TPS) * 128 + (etid % TPS) * C;
+                float o = 0.f;
+                for (int c = 0; c < C; ++c) o += pr[c];
+                om[etid] = o;
+            }
+            named_barrier_sync(1, NEW * 32);
             // ---- d_da_s += D_n <dH, h_-> + sum_{j<s} sc_j omega_j
             if (etid < FL) {
                 const float base = misc[2 * NBW + ib] * (misc[NBW * ib] + misc[NBW * ib + 1]);
@@ -354,7 +375,6 @@ __global__ void __launch_bounds__(NTHR, 1)
                 B.dda[off_da(P, I.bb, I.n * FL + etid, I.hh)] += base + pre;
             }
             named_barrier_sync(1, NEW * 32);  // sc / D_n / omega / dot read: free for the next items
-            if (etid < FL) om[etid] = 0.f;
             if (etid == 0) tc::mbar_arrive(&ctl->scfree[ib]);
         }
     } else {

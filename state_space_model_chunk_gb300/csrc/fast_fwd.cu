@@ -252,6 +252,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
         float S[4][16];
         uint32_t q = 0, seg = 0;
+        int seg_k0 = 0, seg_it0 = it0;  // pair index and item of the current segment's first item
         bool ok = true;
         auto check = [&](bool r) {  // the first failed wait stops the whole CTA at once
             if (!r && ok) {
@@ -263,6 +264,10 @@ __global__ void __launch_bounds__(NTHR, 1)
             const Item I = decode_item(A, it);
             const int Tch = ch ? I.T[1] : I.T[0];
             const int n = 2 * I.k + ch;
+            if (I.seg_first) {
+                seg_k0 = I.k;
+                seg_it0 = it;
+            }
             // chunk-entry carry
             if (Tch > 0) {
                 const float* src = A.Hc + off_carry(P, I.bb, I.hh, n) + (int64_t)pp * R;
@@ -390,11 +395,16 @@ __global__ void __launch_bounds__(NTHR, 1)
                 }
             }
             if (I.seg_last) {
-                // flush the (b,h) moment accumulator: lanes are rows r1 of m2
+                // flush the (b,h) moment accumulator (lanes are rows r1 of m2) with plain stores:
+                // into m2 / m1 when this segment covers every chunk pair of (b,h), else into this
+                // CTA's partial slot (0 for its first segment, 1 for its last), which the reduce
+                // kernel sums in CTA order, so that the result does not depend on timing
                 check(tc::mbar_wait(&ctl->segdone, seg & 1, abort));
                 tc::tc_fence_after();
-                float* M2 = A.m2 + ((int64_t)I.bb * P.h + I.hh) * P.r * P.r;
-                float* M1 = A.m1 + ((int64_t)I.bb * P.h + I.hh) * P.r;
+                const bool whole = seg_k0 == 0 && I.k == pairs_of(P, I.bb) - 1;
+                float* M2 = whole ? A.m2 + ((int64_t)I.bb * P.h + I.hh) * P.r * P.r
+                                  : A.m2p + (int64_t)(2 * blockIdx.x + (seg_it0 == it0 ? 0 : 1)) * (P.r * P.r + P.r);
+                float* M1 = whole ? A.m1 + ((int64_t)I.bb * P.h + I.hh) * P.r : M2 + P.r * P.r;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     float v[16];
@@ -402,15 +412,16 @@ __global__ void __launch_bounds__(NTHR, 1)
                     tc::tmem_ld16(lane_addr + TM_M2 + c0, v);
                     tc::tmem_wait_ld();
                     if (m < R && c0 < R) {
+                        float4* dst = reinterpret_cast<float4*>(M2 + (int64_t)m * P.r + c0);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) atomicAdd(M2 + (int64_t)m * P.r + c0 + e, v[e]);
+                        for (int e = 0; e < 16; e += 4) dst[e / 4] = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
                     }
                 }
                 if (half == 0) {
                     float v[8];
                     tc::tmem_ld8(lane_addr + TM_M2 + 128, v);
                     tc::tmem_wait_ld();
-                    if (m < R) atomicAdd(M1 + m, v[0]);
+                    if (m < R) M1[m] = v[0];
                 }
                 tc::tc_fence_before();
                 __syncwarp();
@@ -425,6 +436,52 @@ __global__ void __launch_bounds__(NTHR, 1)
     if (warp == 0) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tbase, TM_COLS);
+    }
+}
+
+// Moments of the (b,h) pairs whose chunk pairs were split over several CTAs: the partial slots
+// of the CTAs that worked on them, summed in CTA order.  One block per (b,h); pairs done by one
+// CTA were stored by it directly.
+__global__ void __launch_bounds__(256) k_m2_reduce(const __grid_constant__ FastArgs A, int grid) {
+    const MMParams& P = A.P;
+    __shared__ int slots[kMaxFwdGrid];
+    __shared__ int nslots;
+    const int bb = blockIdx.x / P.h, hh = blockIdx.x - bb * P.h;
+    if (threadIdx.x == 0) {
+        int i0 = 0;
+        for (int b2 = 0; b2 < bb; ++b2) i0 += P.h * pairs_of(P, b2);
+        const int np = pairs_of(P, bb);
+        int n = 0;
+        if (np > 0) {
+            i0 += hh * np;
+            const int i1 = i0 + np;  // items [i0, i1) of (bb, hh)
+            // the CTAs whose ranges meet [i0, i1), in order: CTA c holds [begin(c), begin(c+1));
+            // start from an estimate of the CTA holding i0 and step to it
+            int c = (int)(((int64_t)i0 * grid) / A.items);
+            while (c + 1 < grid && item_begin_of(A.items, grid, c + 1) <= i0) ++c;
+            while (c > 0 && item_begin_of(A.items, grid, c) > i0) --c;
+            for (; c < grid && item_begin_of(A.items, grid, c) < i1 && n < kMaxFwdGrid; ++c) {
+                const int c_lo = item_begin_of(A.items, grid, c);
+                slots[n++] = 2 * c + (c_lo >= i0 ? 0 : 1);
+            }
+        }
+        nslots = n < 2 ? 0 : n;  // one CTA: it stored the pair itself
+    }
+    __syncthreads();
+    const int ns = nslots;
+    if (ns == 0) return;
+    const int nel4 = (P.r * P.r + P.r) / 4;  // r is a multiple of 4: whole float4 pieces
+    float4* M2 = reinterpret_cast<float4*>(A.m2 + ((int64_t)bb * P.h + hh) * P.r * P.r);
+    float4* M1 = reinterpret_cast<float4*>(A.m1 + ((int64_t)bb * P.h + hh) * P.r);
+    const float4* src = reinterpret_cast<const float4*>(A.m2p);
+    for (int e = threadIdx.x; e < nel4; e += blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < ns; ++i) {
+            const float4 v = src[(int64_t)slots[i] * nel4 + e];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        if (4 * e < P.r * P.r) M2[e] = acc;
+        else M1[e - P.r * P.r / 4] = acc;
     }
 }
 
@@ -447,7 +504,19 @@ cudaError_t launch_tc_fwd(const FastArgs& args, const TensorMaps& maps, int grid
     mm_prof_mark(KID_FAST_FWD, 1, st);
     kern<<<grid, NTHR, SMEM_BYTES, st>>>(args, maps.x, maps.b, maps.rot, maps.da);
     mm_prof_mark(KID_FAST_FWD, 0, st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (grid == 1) return cudaSuccess;  // one CTA stored every (b,h) itself
+    mm_prof_mark(KID_M2_REDUCE, 1, st);
+    k_m2_reduce<<<args.P.b * args.P.h, 256, 0, st>>>(args, grid);
+    mm_prof_mark(KID_M2_REDUCE, 0, st);
     return cudaGetLastError();
+}
+
+size_t fwd_partial_bytes(const MMParams& P) {
+    // the grid never exceeds the work items, whose number is at most b h ceil(nc / 2)
+    const int64_t items = (int64_t)P.b * P.h * ((P.nc + 1) / 2);
+    const int64_t grid = items < kMaxFwdGrid ? items : kMaxFwdGrid;
+    return (size_t)(2 * grid) * ((size_t)P.r * P.r + P.r) * sizeof(float);
 }
 
 }  // namespace fastk
