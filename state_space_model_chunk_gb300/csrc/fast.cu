@@ -132,7 +132,10 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
     } else {
         std::memset(&maps->rot, 0, sizeof(maps->rot));
     }
-    {   // da as [b*s, h] fp32; box = 4 heads of one token (16 bytes)
+    if (!da_by_tma(P)) {  // rows of h floats that are not 16-byte multiples: the kernels load da themselves
+        std::memset(&maps->da, 0, sizeof(maps->da));
+        std::memset(&maps->da64, 0, sizeof(maps->da64));
+    } else {   // da as [b*s, h] fp32; box = 4 heads of one token (16 bytes)
         cuuint64_t dims[2] = {(cuuint64_t)P.h, bs};
         cuuint64_t str[1] = {(cuuint64_t)P.h * 4};
         cuuint32_t box[2] = {4, 1};
@@ -155,7 +158,7 @@ bool fast_supported(const MMParams& P, bool bf16, int backward) {
     if (!bf16) return false;
     if (backward && P.C > 4) return false;  // two tokens' channel rows per K=16 step of the prefix
     if (P.p != 64 || (P.r != 64 && P.r != 128) || P.C < 1 || P.C > 8) return false;
-    if (P.s % fastk::FL || P.h % 4 || P.b > MM_MAX_B) return false;
+    if (P.s % fastk::FL || P.b > MM_MAX_B) return false;
     // rows of angles / quaternions are copied as 16-byte multiples, at most 128 floats
     if (P.rw % 4 || P.rw > 128) return false;
     if (!encode_fn()) return false;
@@ -179,6 +182,7 @@ cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     fa.m2 = A.m2;
     fa.m1 = A.m1;
     fa.m2p = reinterpret_cast<float*>(scratch);
+    fa.da = A.da;
     fa.err = A.err;
     fa.test_wait_timeout = A.test_wait_timeout;
     if (fa.items == 0) return cudaSuccess;  // nothing valid: m2 / m1 stay zero
@@ -202,6 +206,7 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     fa.items = count_items(P);
     fa.Hc = A.Hc;
     fa.Dn = A.Dn;
+    fa.da = A.da;
     fa.err = A.err;
     cudaError_t e;
     // d_da and d_rot are accumulated by the kernels (sums over rows and over two passes): start

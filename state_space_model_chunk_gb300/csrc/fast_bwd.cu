@@ -319,13 +319,24 @@ __global__ void __launch_bounds__(NTHR, 1)
             const Item I = decode_item(A, it);
             if (it > it0) wait_all(&ctl->itemdone, pr.next(B_ITEMDONE));
             if (!ok) break;
-            // the item's da: 64 tokens x 4 heads per existing chunk
+            // the item's da: 64 tokens x 4 heads per existing chunk (or this head alone, by plain
+            // loads before the arrival that publishes it)
+            if (!da_by_tma(P)) {
+                float* ida = reinterpret_cast<float*>(sm + OFF_IDA);
+                for (int i = lane; i < 2 * FL; i += 32) {
+                    const int ch = i / FL, t = i % FL;
+                    if (I.exists[ch])
+                        ida[(ch * FL + t) * 4 + (I.hh & 3)] =
+                            A.da[((int64_t)I.bb * P.s + (2 * I.k + ch) * FL + t) * P.h + I.hh];
+                }
+                __syncwarp();
+            }
             if (lane == 0) {
                 uint32_t bytes = 0;
-                for (int ch = 0; ch < 2; ++ch) bytes += I.exists[ch] ? 1024u : 0u;
+                for (int ch = 0; ch < 2; ++ch) bytes += (I.exists[ch] && da_by_tma(P)) ? 1024u : 0u;
                 tc::mbar_arrive_expect_tx(&ctl->itemfull, bytes);
                 for (int ch = 0; ch < 2; ++ch)
-                    if (I.exists[ch])
+                    if (I.exists[ch] && da_by_tma(P))
                         tc::tma_load_2d(sm + OFF_IDA + ch * 1024, &tmd, I.hh & ~3, I.bb * P.s + (2 * I.k + ch) * FL,
                                         &ctl->itemfull);
             }

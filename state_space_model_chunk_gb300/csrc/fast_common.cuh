@@ -20,6 +20,7 @@ struct FastArgs {
     float* Dn;      // [b,h,nc] chunk decays
     float* m2;
     float* m1;
+    const float* da;  // [b,s,h] (read with plain loads when h is not a multiple of 4)
     float* m2p;     // forward: per-CTA partial moments of (b,h) shared with other CTAs, 2 slots per CTA
                     // of r*r (m2) + r (m1) floats, summed in CTA order by the reduce kernel
     int* err;       // device error word (0 = fine)
@@ -129,11 +130,15 @@ struct TokenWalk {
     }
 };
 
+// da comes by tensor copies of 4-head groups when a row of da ([b*s, h] fp32) is a multiple of 16
+// bytes long, else by plain loads of the one head into the same shared-memory positions.
+__host__ __device__ inline bool da_by_tma(const MMParams& P) { return (P.h & 3) == 0; }
+
 // Transaction bytes of one chunk's share of a stage: C rows of xhat (64 bf16), C rows of each
 // 64-wide half of bhat, one token's rotation parameters and one 16-byte group of da.
 __host__ __device__ inline uint32_t stage_bytes(const FastArgs& A) {
     const MMParams& P = A.P;
-    return 128u * P.C + (uint32_t)(P.r / 64) * 128u * P.C + 4u * P.rw + 16u;
+    return 128u * P.C + (uint32_t)(P.r / 64) * 128u * P.C + 4u * P.rw + (da_by_tma(P) ? 16u : 0u);
 }
 
 // The four 16-column groups of a 128-column row that one thread owns.  Rotation partners

@@ -145,6 +145,16 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const uint32_t s = q % NS, u = q / NS;
                 if (u >= 1) ok = __all_sync(0xffffffffu, tc::mbar_wait(&ctl->empty[s], (u - 1) & 1, abort));
                 if (!ok) break;
+                if (!da_by_tma(P)) {
+                    // this head's da of the token, into the slot position the 4-head copy would fill,
+                    // stored before the arrival that publishes the stage
+                    if (lane < 2 && I.exists[lane]) {
+                        const int row = I.bb * P.s + (2 * I.k + lane) * FL + t;
+                        reinterpret_cast<float*>(sm + OFF_DA + s * 256 + lane * 128)[I.hh & 3] =
+                            A.da[(int64_t)row * P.h + I.hh];
+                    }
+                    __syncwarp();
+                }
                 if (lane == 0) {
                     uint32_t bytes = 0;
                     for (int ch = 0; ch < 2; ++ch)
@@ -163,7 +173,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                             I.hh, 0, row, &ctl->full[s]);
                         else if (P.rw && kind == nbx)
                             tc::tma_load_3d(sm + OFF_ROT + s * 1024 + ch * 512, &tmr, 0, I.hh, row, &ctl->full[s]);
-                        else
+                        else if (da_by_tma(P))
                             tc::tma_load_2d(sm + OFF_DA + s * 256 + ch * 128, &tmd, I.hh & ~3, row, &ctl->full[s]);
                     }
                 }

@@ -26,7 +26,7 @@ def expected_fast(w, backward):
     """Whether the tensor-core kernels implement this workload (else the SIMT kernels run)."""
     rw = w.rope_dim // 2 if w.rot in ("pairwise", "half") else (4 * w.quat_blocks if w.rot == "quat" else 0)
     return (w.dtype == "bf16" and w.p == 64 and w.r in (64, 128) and 1 <= w.C <= 8 and w.s % 64 == 0
-            and w.h % 4 == 0 and rw % 4 == 0 and rw <= 128 and (not backward or w.C <= 4))
+            and rw % 4 == 0 and rw <= 128 and (not backward or w.C <= 4))
 
 
 def run_gpu(w, inp, force_generic=False):
@@ -73,6 +73,11 @@ SMALL = [
     WORKLOADS["quat_s2048"].scaled(name="quat_partial_blocks", b=2, s=128, h=4, quat_blocks=20, C=2),
     WORKLOADS["tiny_fp32"].scaled(name="norot_odd", b=2, s=48, C=3, h=3, p=5, r=12, chunk_len=12, rot="none",
                                   rope_dim=0, valid="fixed:37"),
+    # head counts that are not multiples of 4 (da rows not 16-byte multiples) on the tensor-core kernels
+    WORKLOADS["large_s4096"].scaled(name="pairwise_h6", b=2, s=256, h=6, C=3, valid="fixed:230"),
+    WORKLOADS["quat_s2048"].scaled(name="quat_h5", b=1, s=192, h=5),
+    WORKLOADS["halfsplit_s1024"].scaled(name="half_r64_h3", b=2, s=256, h=3, chunk_len=32),
+    WORKLOADS["ragged_s16384"].scaled(name="ragged_h1", b=3, s=384, h=1, chunk_len=64),
 ]
 
 
