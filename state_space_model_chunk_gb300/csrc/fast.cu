@@ -70,7 +70,7 @@ cudaError_t encode_grad_maps(const MMParams& P, const void* dx, const void* db, 
     {   // as x32, over d_xhat
         cuuint64_t dims[4] = {(cuuint64_t)P.p, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
         cuuint64_t str[3] = {(cuuint64_t)P.p * 2, (cuuint64_t)P.h * P.p * 2, (cuuint64_t)P.C * P.h * P.p * 2};
-        cuuint32_t box[4] = {64, 1, (cuuint32_t)P.C, 32};
+        cuuint32_t box[4] = {64, 1, (cuuint32_t)P.C, (cuuint32_t)corr_tps(P)};
         if ((e = encode(&maps->dx32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, dx, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
@@ -78,7 +78,7 @@ cudaError_t encode_grad_maps(const MMParams& P, const void* dx, const void* db, 
     {   // as b32, over d_bhat
         cuuint64_t dims[5] = {64, (cuuint64_t)P.r / 64, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
         cuuint64_t str[4] = {128, (cuuint64_t)P.r * 2, (cuuint64_t)P.h * P.r * 2, (cuuint64_t)P.C * P.h * P.r * 2};
-        cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)P.C, 32};
+        cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)P.C, (cuuint32_t)corr_tps(P)};
         if ((e = encode(&maps->db32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, db, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
@@ -101,8 +101,8 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
         if ((e = encode(&maps->x8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, xhat, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
-        box[3] = 32;
-        if (P.C <= 4 && (e = encode(&maps->x32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, xhat, dims, str, box,
+        box[3] = (cuuint32_t)corr_tps(P);
+        if ((e = encode(&maps->x32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, xhat, dims, str, box,
                                     CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
     }
@@ -117,8 +117,8 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
         if ((e = encode(&maps->b8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bhat, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
-        box[4] = 32;
-        if (P.C <= 4 && (e = encode(&maps->b32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bhat, dims, str, box,
+        box[4] = (cuuint32_t)corr_tps(P);
+        if ((e = encode(&maps->b32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bhat, dims, str, box,
                                     CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
     }
@@ -156,7 +156,6 @@ int fastk_chunk() { return fastk::FL; }
 
 bool fast_supported(const MMParams& P, bool bf16, int backward) {
     if (!bf16) return false;
-    if (backward && P.C > 4) return false;  // two tokens' channel rows per K=16 step of the prefix
     if (P.p != 64 || (P.r != 64 && P.r != 128) || P.C < 1 || P.C > 8) return false;
     if (P.s % fastk::FL || P.b > MM_MAX_B) return false;
     // rows of angles / quaternions are copied as 16-byte multiples, at most 128 floats

@@ -1,5 +1,5 @@
 // fast_bwd.cu -- tcgen05 / TMA recompute backward of the state-moments operator (bf16 operands,
-// p = 64, r in {64, 128}, C <= 4).
+// p = 64, r in {64, 128}, C <= 8).
 //
 // Work item = a pair of 64-token chunks of one (batch row, head); the two chunks share the 128
 // TMEM lanes (row m = (chunk, p)) as in the forward.  This kernel is the chunk's own backward with
@@ -242,7 +242,7 @@ enum : uint32_t {
     B_ITEM = 6, B_SPAN, B_PA, B_P, B_C, B_DC, B_G, B_DX, B_ITEMDONE,
     U_PRE = 24, U_DC, U_DX, U_PA, U_C, U_G, U_SPAN
 };
-template <int ROTK, int LAYB>
+template <int ROTK, int LAYB, int CS>
 __global__ void __launch_bounds__(NTHR, 1)
     tc_bwd_kernel(const __grid_constant__ BwdArgs B, const __grid_constant__ CUtensorMap tmx,
                   const __grid_constant__ CUtensorMap tmb, const __grid_constant__ CUtensorMap tmr,
@@ -654,8 +654,10 @@ __global__ void __launch_bounds__(NTHR, 1)
                         const int b = ((nA - 1 - k) & 1) ^ 1;
                         ok &= tc::mbar_wait(&ctl->afull[b], (b ? na1 : na0) & 1, abort);
                         unsigned char* xb = sm + (b ? OFF_PA : OFF_SX);
-                        for (int i = ctid; i < SPAN * 64; i += NCW * 32) {
-                            const int jc = i & 7, c = (i >> 3) & 3, c2 = (i >> 5) & 1, j = i >> 6;
+                        // units of 8 bf16: (token j, chunk c2, channel slot c of 4 or 8, column group jc)
+                        for (int i = ctid; i < (SPAN * 16) << CS; i += NCW * 32) {
+                            const int jc = i & 7, c = (i >> 3) & ((1 << CS) - 1), c2 = (i >> (3 + CS)) & 1,
+                                      j = i >> (4 + CS);
                             if (c >= C) continue;
                             const int Tc = c2 ? I.T[1] : I.T[0];
                             const int t = k * SPAN + j, tend = min(k * SPAN + SPAN - 1, Tc - 1);
@@ -768,8 +770,9 @@ __global__ void __launch_bounds__(NTHR, 1)
                     auto build_pa = [&](int t) {
                         const int o = t - s0;
                         if (pr.once(U_PA)) ok &= tc::mbar_wait(&ctl->pafree, pr.next(B_PA), abort);
-                        for (int i = ctid; i < (o + 1) * 64; i += NCW * 32) {
-                            const int jc = i & 7, c = (i >> 3) & 3, c2 = (i >> 5) & 1, j = i >> 6;
+                        for (int i = ctid; i < ((o + 1) * 16) << CS; i += NCW * 32) {
+                            const int jc = i & 7, c = (i >> 3) & ((1 << CS) - 1), c2 = (i >> (3 + CS)) & 1,
+                                      j = i >> (4 + CS);
                             if (c >= C) continue;
                             const uint32_t off = j * 4096u + tc::sw128_chunk(16, c2, 8 * c2 + c, jc);
                             uint4 w = make_uint4(0, 0, 0, 0);
@@ -980,13 +983,13 @@ __global__ void __launch_bounds__(NTHR, 1)
                         if (ptab[0]) {
                             __nv_bfloat16* px = reinterpret_cast<__nv_bfloat16*>(ptab[0]) + (int64_t)t * C * hp;
 #pragma unroll
-                            for (int c = 0; c < 4; ++c)
+                            for (int c = 0; c < (1 << CS); ++c)
                                 if (c < C) px[c * hp] = __float2bfloat16_rn(v[c]);
                         }
                         if (ptab[1]) {
                             __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(ptab[1]) + (int64_t)t * C * hr;
 #pragma unroll
-                            for (int c = 0; c < 4; ++c)
+                            for (int c = 0; c < (1 << CS); ++c)
                                 if (c < C) pb[c * hr] = __float2bfloat16_rn(u[c]);
                         }
                     };
@@ -1072,12 +1075,17 @@ cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, const fl
     a.db = static_cast<__nv_bfloat16*>(db);
     a.dda = dda;
     a.drot = drot;
-    decltype(&tc_bwd_kernel<ROT_NONE, 0>) kern;
+    // channel slots per chunk in the span tiles: 4 when C <= 4, else 8
+    decltype(&tc_bwd_kernel<ROT_NONE, 0, 2>) kern;
+    const bool c8 = fa.P.C > 4;
     switch (fa.P.rot) {
-        case ROT_PAIRWISE: kern = tc_bwd_kernel<ROT_PAIRWISE, 0>; break;
-        case ROT_HALF: kern = fa.layoutB ? tc_bwd_kernel<ROT_HALF, 1> : tc_bwd_kernel<ROT_HALF, 0>; break;
-        case ROT_QUAT: kern = tc_bwd_kernel<ROT_QUAT, 0>; break;
-        default: kern = tc_bwd_kernel<ROT_NONE, 0>; break;
+        case ROT_PAIRWISE: kern = c8 ? tc_bwd_kernel<ROT_PAIRWISE, 0, 3> : tc_bwd_kernel<ROT_PAIRWISE, 0, 2>; break;
+        case ROT_HALF:
+            kern = fa.layoutB ? (c8 ? tc_bwd_kernel<ROT_HALF, 1, 3> : tc_bwd_kernel<ROT_HALF, 1, 2>)
+                              : (c8 ? tc_bwd_kernel<ROT_HALF, 0, 3> : tc_bwd_kernel<ROT_HALF, 0, 2>);
+            break;
+        case ROT_QUAT: kern = c8 ? tc_bwd_kernel<ROT_QUAT, 0, 3> : tc_bwd_kernel<ROT_QUAT, 0, 2>; break;
+        default: kern = c8 ? tc_bwd_kernel<ROT_NONE, 0, 3> : tc_bwd_kernel<ROT_NONE, 0, 2>; break;
     }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;

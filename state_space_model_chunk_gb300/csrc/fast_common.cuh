@@ -30,8 +30,8 @@ struct FastArgs {
 struct TensorMaps {
     CUtensorMap x, b, rot, da, da64;  // da: 4 heads x 1 token; da64: 4 heads x 64 tokens
     CUtensorMap x8, b8;               // xhat / bhat rows of 8 consecutive tokens
-    CUtensorMap x32, b32;             // ... and of 32
-    CUtensorMap dx32, db32;           // d_xhat / d_bhat rows of 32 tokens (backward only)
+    CUtensorMap x32, b32;             // ... and of corr_tps(P) tokens (the correction kernel's stages)
+    CUtensorMap dx32, db32;           // d_xhat / d_bhat rows of corr_tps(P) tokens (backward only)
 };
 
 constexpr int kMaxBwdGrid = 160;  // CTAs of the backward kernels (anchor slots in the workspace)
@@ -134,6 +134,10 @@ struct TokenWalk {
 // bytes long, else by plain loads of the one head into the same shared-memory positions.
 __host__ __device__ inline bool da_by_tma(const MMParams& P) { return (P.h & 3) == 0; }
 
+// Tokens per stage of the correction kernel: their (token, channel) rows fill at most the 128
+// lanes of one tensor-core tile.
+__host__ __device__ inline int corr_tps(const MMParams& P) { return P.C <= 4 ? 32 : 16; }
+
 // Transaction bytes of one chunk's share of a stage: C rows of xhat (64 bf16), C rows of each
 // 64-wide half of bhat, one token's rotation parameters and one 16-byte group of da.
 __host__ __device__ inline uint32_t stage_bytes(const FastArgs& A) {
@@ -205,7 +209,7 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
 int sm_count();
 cudaError_t launch_tc_fwd(const FastArgs& args, const TensorMaps& maps, int grid, cudaStream_t st);
 cudaError_t launch_tc_end(const FastArgs& fa, const TensorMaps& maps, cudaStream_t st);
-// Tensor maps over the d_xhat / d_bhat outputs, same geometry as x32 / b32 (C <= 4).
+// Tensor maps over the d_xhat / d_bhat outputs, same geometry as x32 / b32.
 cudaError_t encode_grad_maps(const MMParams& P, const void* dx, const void* db, TensorMaps* maps);
 cudaError_t launch_tc_corr(const FastArgs& fa, const float* da, const float* E, void* dx, void* db, float* dda,
                            const TensorMaps& maps, cudaStream_t st);

@@ -8,7 +8,8 @@
 //   V_{t,c} = dH^T xhat_{t,c} (r values)          d_bhat_{t,c} += sc_t V_{t,c}
 //   omega_t = sum_c <xhat_{t,c}, U_{t,c}>          d_da_s += D_n <dH, h_-(n)> + sum_{j<s} sc_j omega_j
 //
-// Over the rows (t, c) of 32 tokens these are U = Bhat dH^T (M = 32 C, N = p, K = r) and
+// Over the rows (t, c) of a stage of TPS tokens (32, or 16 when C > 4) these are U = Bhat dH^T
+// (M = TPS C <= 128, N = p, K = r) and
 // V = Xhat dH (M = 32 C, N = r, K = p).  One bf16 dH tile [p][r] in the 128-byte-swizzled layout
 // is the K-major B operand of the first and the MN-major B operand of the second; the xhat /
 // bhat rows and the d_xhat / d_bhat rows of the stage come by TMA.  The epilogue (lanes = rows
@@ -35,7 +36,6 @@ constexpr int NEW = 16;                    // epilogue warps: four per TMEM lane
 constexpr int NBW = 2;                     // builder warps
 constexpr int NTHR = (2 + NEW + NBW) * 32;
 static_assert(NBW == 2, "the epilogue sums two dot partials");
-constexpr int TPS = 32;                    // tokens per stage (rows 32 C <= 128)
 constexpr int NS = 2;                      // stages
 constexpr uint32_t SLOT = 16384;           // 128 rows x 128 B
 // xhat | bhat r 0..63 | bhat r 64..127 | d_xhat | d_bhat r 0..63 | d_bhat r 64..127: the gradient
@@ -46,7 +46,7 @@ constexpr uint32_t DHT = 16384;            // dH tile: 64 rows x 2 blocks x 128 
 constexpr uint32_t OFF_DH = NS * STAGE;    // 2 dH tiles
 constexpr uint32_t OFF_SC = OFF_DH + 2 * DHT;   // sc_t, 2 items x 64 fp32
 constexpr uint32_t OFF_OM = OFF_SC + 512;       // omega of the item, 64 fp32
-constexpr uint32_t OFF_OMR = OFF_OM + 256;      // <xhat, U> of every stage row: [2 stages][128 rows] fp32
+constexpr uint32_t OFF_OMR = OFF_OM + 256;      // <xhat, U> of the stage rows: [stage parity][128 rows] fp32
 constexpr uint32_t OFF_MISC = OFF_OMR + 1024;   // dot partials [item][builder warp], then D_n [item]
 constexpr uint32_t OFF_CTL = OFF_MISC + 64;
 constexpr uint32_t SMEM_BYTES = OFF_CTL + 128 + 1024;
@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     const int R = P.r, C = P.C;
     const int items = count_corr(P);
     const int it0 = range_begin(items, blockIdx.x), it1 = range_begin(items, blockIdx.x + 1);
+    const int TPS = corr_tps(P);                // tokens per stage: rows TPS * C <= 128
     const uint32_t rows = (uint32_t)TPS * C;
 
     // rows past 32 C of the stage slots, the r >= 64 half (r = 64) and omega start at zero
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(NTHR, 1)
 
     if (warp == 0) {
         // ================================================================ TMA producer
-        // Per stage: the xhat / bhat rows and the d_xhat / d_bhat rows of 32 tokens in; before a
+        // Per stage: the xhat / bhat rows and the d_xhat / d_bhat rows of TPS tokens in; before a
         // slot is reused, the stage it held goes back out (the updated gradient rows) by tensor
         // stores, whose reads of the slot complete before the new loads are issued.
         if (lane == 0) {
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(NTHR, 1)
             const uint32_t ib = li & 1;
             const float* sc = reinterpret_cast<const float*>(sm + OFF_SC) + ib * 64;
             check(tc::mbar_wait(&ctl->dhfull[ib], (li >> 1) & 1, abort));  // sc, D_n and the dot are ready
-            // ---- the two 32-token stages
+            // ---- the stages of TPS tokens
             for (int st = 0; st < FL / TPS; ++st, ++q) {
                 const uint32_t s = q % NS, ab = q & 1;
                 const int t = st * TPS + tl;
@@ -306,7 +307,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                             }
                         }
                     }
-                    if (row_ok) omr[st * 128 + k] = w;
+                    if (row_ok) omr[(st & 1) * 128 + k] = w;
                 }
                 const float scv = sc[t];
                 if (row_ok) {  // d_xhat row += sc U, in the stage's d_xhat slot (same layout as xhat)
@@ -358,15 +359,17 @@ __global__ void __launch_bounds__(NTHR, 1)
                     tc::mbar_arrive(&ctl->accfree[ab]);
                     tc::mbar_arrive(&ctl->upd[s]);
                 }
+                // omega of the stage's tokens: each token's C rows, in channel order (the row buffer
+                // alternates by stage, so the next stage's rows never overwrite ones still being read)
+                named_barrier_sync(1, NEW * 32);
+                if (etid < TPS) {
+                    const float* pr = omr + (st & 1) * 128 + etid * C;
+                    float o = 0.f;
+                    for (int c = 0; c < C; ++c) o += pr[c];
+                    om[st * TPS + etid] = o;
+                }
             }
-            named_barrier_sync(1, NEW * 32);  // every row's <xhat, U> is in
-            if (etid < FL) {  // omega_t: the token's C rows, in channel order
-                const float* pr = omr + (etid / TPS) * 128 + (etid % TPS) * C;
-                float o = 0.f;
-                for (int c = 0; c < C; ++c) o += pr[c];
-                om[etid] = o;
-            }
-            named_barrier_sync(1, NEW * 32);
+            named_barrier_sync(1, NEW * 32);  // omega of every token is in
             // ---- d_da_s += D_n <dH, h_-> + sum_{j<s} sc_j omega_j
             if (etid < FL) {
                 const float base = misc[2 * NBW + ib] * (misc[NBW * ib] + misc[NBW * ib + 1]);

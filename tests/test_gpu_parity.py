@@ -26,7 +26,7 @@ def expected_fast(w, backward):
     """Whether the tensor-core kernels implement this workload (else the SIMT kernels run)."""
     rw = w.rope_dim // 2 if w.rot in ("pairwise", "half") else (4 * w.quat_blocks if w.rot == "quat" else 0)
     return (w.dtype == "bf16" and w.p == 64 and w.r in (64, 128) and 1 <= w.C <= 8 and w.s % 64 == 0
-            and rw % 4 == 0 and rw <= 128 and (not backward or w.C <= 4))
+            and rw % 4 == 0 and rw <= 128)
 
 
 def run_gpu(w, inp, force_generic=False):
@@ -78,6 +78,10 @@ SMALL = [
     WORKLOADS["quat_s2048"].scaled(name="quat_h5", b=1, s=192, h=5),
     WORKLOADS["halfsplit_s1024"].scaled(name="half_r64_h3", b=2, s=256, h=3, chunk_len=32),
     WORKLOADS["ragged_s16384"].scaled(name="ragged_h1", b=3, s=384, h=1, chunk_len=64),
+    # five to eight channels (the correction kernel's 16-token stages)
+    WORKLOADS["large_s4096"].scaled(name="pairwise_c8", b=1, s=256, h=4, C=8, valid="fixed:241"),
+    WORKLOADS["quat_s2048"].scaled(name="quat_c5", b=2, s=192, h=2, C=5),
+    WORKLOADS["halfsplit_s1024"].scaled(name="half_r64_c7", b=1, s=320, h=3, C=7),
 ]
 
 
@@ -133,12 +137,12 @@ def test_parity_steep_decay_spans():
 
 
 @pytest.mark.parametrize("w", [SMALL[3], SMALL[0],
-                               WORKLOADS["large_s4096"].scaled(name="mixed_paths", b=1, s=128, h=4, C=6)],
-                         ids=["tensor_core", "simt", "mixed_paths"])
+                               WORKLOADS["large_s4096"].scaled(name="tc_c6", b=1, s=128, h=4, C=6)],
+                         ids=["tensor_core", "simt", "tensor_core_c6"])
 def test_backward_reusing_forward_carries(w):
     """MM_FLAG_REUSE_CARRIES: forward then backward on one workspace gives the gradients of a
-    backward that recomputes the carries (on the tensor-core path, the SIMT path, and a problem
-    whose forward and backward take different paths, where the flag is ignored)."""
+    backward that recomputes the carries (on the tensor-core path with four and six channels, and on
+    the SIMT path)."""
     inp = make_inputs(w)
     d = {k: v.to(DEV) for k, v in inp.items() if k != "valid_len"}
     spec = spec_of(w)
