@@ -72,7 +72,8 @@ __device__ __forceinline__ void fail(Ctl* ctl, int* err, int code) {
     atomicExch(err, code);
 }
 
-template <int ROTK, int LAYB>
+// DAT: da comes by 4-head tensor copies (h a multiple of 4), else by plain loads of the one head
+template <int ROTK, int LAYB, bool DAT>
 __global__ void __launch_bounds__(NTHR, 1)
     tc_fwd_kernel(const __grid_constant__ FastArgs A, const __grid_constant__ CUtensorMap tmx,
                   const __grid_constant__ CUtensorMap tmb, const __grid_constant__ CUtensorMap tmr,
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const uint32_t s = q % NS, u = q / NS;
                 if (u >= 1) ok = __all_sync(0xffffffffu, tc::mbar_wait(&ctl->empty[s], (u - 1) & 1, abort));
                 if (!ok) break;
-                if (!da_by_tma(P)) {
+                if (!DAT) {
                     // this head's da of the token, into the slot position the 4-head copy would fill,
                     // stored before the arrival that publishes the stage
                     if (lane < 2 && I.exists[lane]) {
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                             I.hh, 0, row, &ctl->full[s]);
                         else if (P.rw && kind == nbx)
                             tc::tma_load_3d(sm + OFF_ROT + s * 1024 + ch * 512, &tmr, 0, I.hh, row, &ctl->full[s]);
-                        else if (da_by_tma(P))
+                        else if (DAT)
                             tc::tma_load_2d(sm + OFF_DA + s * 256 + ch * 128, &tmd, I.hh & ~3, row, &ctl->full[s]);
                     }
                 }
@@ -502,12 +503,16 @@ namespace fastk {
 
 cudaError_t launch_tc_fwd(const FastArgs& args, const TensorMaps& maps, int grid, cudaStream_t st) {
     using namespace fastfwd;
-    decltype(&tc_fwd_kernel<ROT_NONE, 0>) kern;
+    decltype(&tc_fwd_kernel<ROT_NONE, 0, true>) kern;
+    const bool dat = da_by_tma(args.P);
     switch (args.P.rot) {
-        case ROT_PAIRWISE: kern = tc_fwd_kernel<ROT_PAIRWISE, 0>; break;
-        case ROT_HALF: kern = args.layoutB ? tc_fwd_kernel<ROT_HALF, 1> : tc_fwd_kernel<ROT_HALF, 0>; break;
-        case ROT_QUAT: kern = tc_fwd_kernel<ROT_QUAT, 0>; break;
-        default: kern = tc_fwd_kernel<ROT_NONE, 0>; break;
+        case ROT_PAIRWISE: kern = dat ? tc_fwd_kernel<ROT_PAIRWISE, 0, true> : tc_fwd_kernel<ROT_PAIRWISE, 0, false>; break;
+        case ROT_HALF:
+            kern = args.layoutB ? (dat ? tc_fwd_kernel<ROT_HALF, 1, true> : tc_fwd_kernel<ROT_HALF, 1, false>)
+                                : (dat ? tc_fwd_kernel<ROT_HALF, 0, true> : tc_fwd_kernel<ROT_HALF, 0, false>);
+            break;
+        case ROT_QUAT: kern = dat ? tc_fwd_kernel<ROT_QUAT, 0, true> : tc_fwd_kernel<ROT_QUAT, 0, false>; break;
+        default: kern = dat ? tc_fwd_kernel<ROT_NONE, 0, true> : tc_fwd_kernel<ROT_NONE, 0, false>; break;
     }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
