@@ -451,8 +451,8 @@ __global__ void __launch_bounds__(NTHR, 1)
 }
 
 // Moments of the (b,h) pairs whose chunk pairs were split over several CTAs: the partial slots
-// of the CTAs that worked on them, summed in CTA order.  One block per (b,h); pairs done by one
-// CTA were stored by it directly.
+// of the CTAs that worked on them, summed in CTA order.  Grid x is the (b,h), grid y a slice of
+// its r r + r moments; pairs done by one CTA were stored by it directly.
 __global__ void __launch_bounds__(256) k_m2_reduce(const __grid_constant__ FastArgs A, int grid) {
     const MMParams& P = A.P;
     __shared__ int slots[kMaxFwdGrid];
@@ -482,18 +482,21 @@ __global__ void __launch_bounds__(256) k_m2_reduce(const __grid_constant__ FastA
     const int ns = nslots;
     if (ns == 0) return;
     const int nel4 = (P.r * P.r + P.r) / 4;  // r is a multiple of 4: whole float4 pieces
+    // blockIdx.y picks a slice of blockDim.x float4 pieces: one piece per thread, its slot loads
+    // all independent, so the short reduction is not latency-bound on a few blocks
+    const int e = blockIdx.y * blockDim.x + threadIdx.x;
+    if (e >= nel4) return;
     float4* M2 = reinterpret_cast<float4*>(A.m2 + ((int64_t)bb * P.h + hh) * P.r * P.r);
     float4* M1 = reinterpret_cast<float4*>(A.m1 + ((int64_t)bb * P.h + hh) * P.r);
     const float4* src = reinterpret_cast<const float4*>(A.m2p);
-    for (int e = threadIdx.x; e < nel4; e += blockDim.x) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = 0; i < ns; ++i) {
-            const float4 v = src[(int64_t)slots[i] * nel4 + e];
-            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-        }
-        if (4 * e < P.r * P.r) M2[e] = acc;
-        else M1[e - P.r * P.r / 4] = acc;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int i = 0; i < ns; ++i) {
+        const float4 v = src[(int64_t)slots[i] * nel4 + e];
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
+    if (4 * e < P.r * P.r) M2[e] = acc;
+    else M1[e - P.r * P.r / 4] = acc;
 }
 
 }  // namespace fastfwd
@@ -522,7 +525,8 @@ cudaError_t launch_tc_fwd(const FastArgs& args, const TensorMaps& maps, int grid
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (grid == 1) return cudaSuccess;  // one CTA stored every (b,h) itself
     mm_prof_mark(KID_M2_REDUCE, 1, st);
-    k_m2_reduce<<<args.P.b * args.P.h, 256, 0, st>>>(args, grid);
+    const int nel4 = (args.P.r * args.P.r + args.P.r) / 4;
+    k_m2_reduce<<<dim3(args.P.b * args.P.h, (nel4 + 255) / 256), 256, 0, st>>>(args, grid);
     mm_prof_mark(KID_M2_REDUCE, 0, st);
     return cudaGetLastError();
 }
