@@ -111,6 +111,17 @@ __device__ __forceinline__ void ca_load16(uint32_t taddr, float (&v)[16]) {
     }
 }
 
+// eight bf16 values (one 16-byte piece of a tile) times L, rounded back to bf16
+__device__ __forceinline__ uint4 scale_bf16x8(const uint4 v, float L) {
+    float f[8];
+    fmul2(f[0], f[1], L, L, bf16lo(v.x), bf16hi(v.x));
+    fmul2(f[2], f[3], L, L, bf16lo(v.y), bf16hi(v.y));
+    fmul2(f[4], f[5], L, L, bf16lo(v.z), bf16hi(v.z));
+    fmul2(f[6], f[7], L, L, bf16lo(v.w), bf16hi(v.w));
+    return make_uint4(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]), tc::pack_bf16x2(f[4], f[5]),
+                      tc::pack_bf16x2(f[6], f[7]));
+}
+
 struct BwdArgs {
     FastArgs F;         // problem, items, Hc (carries), Dn, err
     float* E;           // [b,h,nc,p,r]: e_n of every chunk
@@ -194,12 +205,15 @@ __device__ __forceinline__ void rot_pass(const MMParams& P, int pass, int ka, in
             const float4 s4 = *reinterpret_cast<const float4*>(cf + 64 + ka + e4);
             const float cs[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 4; j += 2) {
                 const int e = e4 + j;
-                const float c_ = cs[j], s_ = TR ? -sn[j] : sn[j];
-                const float x = a[e], y = b[e];
-                a[e] = fmaf(c_, x, s_ * y);
-                b[e] = fmaf(c_, y, -s_ * x);
+                const float s0 = TR ? -sn[j] : sn[j], s1 = TR ? -sn[j + 1] : sn[j + 1];
+                const float x0 = a[e], x1 = a[e + 1], y0 = b[e], y1 = b[e + 1];
+                float u0, u1, w0, w1;
+                fmul2(u0, u1, s0, s1, y0, y1);    // s y
+                fmul2(w0, w1, -s0, -s1, x0, x1);  // -s x
+                ffma2(a[e], a[e + 1], cs[j], cs[j + 1], x0, x1, u0, u1);
+                ffma2(b[e], b[e + 1], cs[j], cs[j + 1], y0, y1, w0, w1);
             }
         }
     } else if (ROTK == ROT_QUAT) {
@@ -664,12 +678,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                             const float L = t < Tc ? __expf(acum[c2 * 64 + tend] - acum[c2 * 64 + t]) : 0.f;
                             uint4* px = reinterpret_cast<uint4*>(xb + j * 4096 + tc::sw128_chunk(16, c2, 8 * c2 + c, jc));
                             const uint4 v = *px;
-                            uint4 w;
-                            w.x = tc::pack_bf16x2(L * bf16lo(v.x), L * bf16hi(v.x));
-                            w.y = tc::pack_bf16x2(L * bf16lo(v.y), L * bf16hi(v.y));
-                            w.z = tc::pack_bf16x2(L * bf16lo(v.z), L * bf16hi(v.z));
-                            w.w = tc::pack_bf16x2(L * bf16lo(v.w), L * bf16hi(v.w));
-                            *px = w;
+                            *px = scale_bf16x8(v, L);
                         }
                         tc::fence_proxy_async_smem();
                         __syncwarp();
@@ -697,8 +706,9 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
                             for (int g = 0; g < 2; ++g)
 #pragma unroll
-                                for (int e = 0; e < 16; ++e)
-                                    S[2 * pass + g][e] = fmaf(Dk, S[2 * pass + g][e], W[g][e]);
+                                for (int e = 0; e < 16; e += 2)
+                                    ffma2(S[2 * pass + g][e], S[2 * pass + g][e + 1], Dk, Dk, S[2 * pass + g][e],
+                                          S[2 * pass + g][e + 1], W[g][e], W[g][e + 1]);
                         }
                         tc::tc_fence_before();
                         __syncwarp();
@@ -779,10 +789,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                             if (c2 ? I.exists[1] : I.exists[0]) {
                                 const float L = Lt[(c2 * 8 + o) * 8 + j];
                                 const uint4 v = *reinterpret_cast<const uint4*>(sm + OFF_SX + off);
-                                w.x = tc::pack_bf16x2(L * bf16lo(v.x), L * bf16hi(v.x));
-                                w.y = tc::pack_bf16x2(L * bf16lo(v.y), L * bf16hi(v.y));
-                                w.z = tc::pack_bf16x2(L * bf16lo(v.z), L * bf16hi(v.z));
-                                w.w = tc::pack_bf16x2(L * bf16lo(v.w), L * bf16hi(v.w));
+                                w = scale_bf16x8(v, L);
                             }
                             *reinterpret_cast<uint4*>(sm + OFF_PA + off) = w;
                         }
@@ -811,11 +818,11 @@ __global__ void __launch_bounds__(NTHR, 1)
                             tc::tmem_ld16(lane_addr + TM_AN + 16 * G[sb], ab);
                             tc::tmem_wait_ld();
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                ha[e] = fmaf(dsig, aa[e], ha[e]);
-                                hb[e] = fmaf(dsig, ab[e], hb[e]);
-                                dotv[e & 1] = fmaf(gr[sa][e], ha[e], dotv[e & 1]);
-                                dotv[2 + (e & 1)] = fmaf(gr[sb][e], hb[e], dotv[2 + (e & 1)]);
+                            for (int e = 0; e < 16; e += 2) {
+                                ffma2(ha[e], ha[e + 1], dsig, dsig, aa[e], aa[e + 1], ha[e], ha[e + 1]);
+                                ffma2(hb[e], hb[e + 1], dsig, dsig, ab[e], ab[e + 1], hb[e], hb[e + 1]);
+                                ffma2(dotv[0], dotv[1], gr[sa][e], gr[sa][e + 1], ha[e], ha[e + 1], dotv[0], dotv[1]);
+                                ffma2(dotv[2], dotv[3], gr[sb][e], gr[sb][e + 1], hb[e], hb[e + 1], dotv[2], dotv[3]);
                             }
                             rot_pass<ROTK, LAYB, false>(P, pass, 16 * G[sa], 16 * G[sb], group_rotated<ROTK>(P, G[sa]),
                                                         group_rotated<ROTK>(P, G[sb]), ha, hb, cf, qt);
@@ -851,7 +858,8 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
                             for (int g = 0; g < 4; ++g)
 #pragma unroll
-                                for (int e = 0; e < 16; ++e) gr[g][e] *= e_next;
+                                for (int e = 0; e < 16; e += 2)
+                                    fmul2(gr[g][e], gr[g][e + 1], gr[g][e], gr[g][e + 1], e_next, e_next);
                         } else {
 #pragma unroll
                         for (int pass = 0; pass < 2; ++pass) {
@@ -901,13 +909,15 @@ __global__ void __launch_bounds__(NTHR, 1)
                                         float cc[16];
                                         ca_load16(lane_addr + TM_CA + 8 * G[sa], cc);
 #pragma unroll
-                                        for (int e = 0; e < 16; ++e) v[e] = -db_[e] * cc[e];
+                                        for (int e = 0; e < 16; e += 2)
+                                            fmul2(v[e], v[e + 1], -db_[e], -db_[e + 1], cc[e], cc[e + 1]);
                                     }
                                     {
                                         float cc[16];
                                         ca_load16(lane_addr + TM_CA + 8 * G[sb], cc);
 #pragma unroll
-                                        for (int e = 0; e < 16; ++e) v[e] = fmaf(da_[e], cc[e], v[e]);
+                                        for (int e = 0; e < 16; e += 2)
+                                            ffma2(v[e], v[e + 1], da_[e], da_[e + 1], cc[e], cc[e + 1], v[e], v[e + 1]);
                                     }
                                     transpose_reduce16(v, lane);
                                     const int ang = 16 * G[sa] + (lane & 15);
@@ -951,9 +961,9 @@ __global__ void __launch_bounds__(NTHR, 1)
                             // G = derot^T(d_c); g_t = G_t + e_{t+1} g_{t+1}
                             rot_pass<ROTK, LAYB, true>(P, pass, 16 * G[sa], 16 * G[sb], act_a, act_b, da_, db_, cf, qt);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                gr[sa][e] = fmaf(e_next, gr[sa][e], da_[e]);
-                                gr[sb][e] = fmaf(e_next, gr[sb][e], db_[e]);
+                            for (int e = 0; e < 16; e += 2) {
+                                ffma2(gr[sa][e], gr[sa][e + 1], e_next, e_next, gr[sa][e], gr[sa][e + 1], da_[e], da_[e + 1]);
+                                ffma2(gr[sb][e], gr[sb][e + 1], e_next, e_next, gr[sb][e], gr[sb][e + 1], db_[e], db_[e + 1]);
                             }
                         }
                         tc::tc_fence_before();

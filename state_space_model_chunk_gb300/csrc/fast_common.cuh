@@ -168,6 +168,21 @@ __device__ __forceinline__ void hamilton(float qw, float qx, float qy, float qz,
     oz = qw * vz + qx * vy - qy * vx + qz * vw;
 }
 
+// Packed fp32x2 arithmetic (sm_100 and later): one instruction for two values, each rounded
+// exactly as the scalar fmaf / product it replaces, so using it changes no result.
+// (d0, d1) <- (a0, a1) * (b0, b1) + (c0, c1)
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
+    const float2 r = __ffma2_rn(make_float2(a0, a1), make_float2(b0, b1), make_float2(c0, c1));
+    d0 = r.x;
+    d1 = r.y;
+}
+// (d0, d1) <- (a0, a1) * (b0, b1)
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    const float2 r = __fmul2_rn(make_float2(a0, a1), make_float2(b0, b1));
+    d0 = r.x;
+    d1 = r.y;
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -332,9 +332,9 @@ __global__ void __launch_bounds__(NTHR, 1)
                     float(&b)[16] = Wt[sb];
                     if (live) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            S[sa][e] = fmaf(et, S[sa][e], a[e]);
-                            S[sb][e] = fmaf(et, S[sb][e], b[e]);
+                        for (int e = 0; e < 16; e += 2) {
+                            ffma2(S[sa][e], S[sa][e + 1], et, et, S[sa][e], S[sa][e + 1], a[e], a[e + 1]);
+                            ffma2(S[sb][e], S[sb][e + 1], et, et, S[sb][e], S[sb][e + 1], b[e], b[e + 1]);
                         }
                     }
 #pragma unroll
@@ -370,11 +370,14 @@ __global__ void __launch_bounds__(NTHR, 1)
                                 const float4 s4 = *reinterpret_cast<const float4*>(tbl + 32 + ti + e4);
                                 const float cs[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-                                for (int j = 0; j < 4; ++j) {
+                                for (int j = 0; j < 4; j += 2) {
                                     const int e = e4 + j;
-                                    const float x = a[e], y = b[e];
-                                    a[e] = fmaf(cs[j], x, sn[j] * y);
-                                    b[e] = fmaf(cs[j], y, -sn[j] * x);
+                                    const float x0 = a[e], x1 = a[e + 1], y0 = b[e], y1 = b[e + 1];
+                                    float u0, u1, w0, w1;
+                                    fmul2(u0, u1, sn[j], sn[j + 1], y0, y1);    // s y
+                                    fmul2(w0, w1, -sn[j], -sn[j + 1], x0, x1);  // -s x
+                                    ffma2(a[e], a[e + 1], cs[j], cs[j + 1], x0, x1, u0, u1);
+                                    ffma2(b[e], b[e + 1], cs[j], cs[j + 1], y0, y1, w0, w1);
                                 }
                             }
                         }
