@@ -34,12 +34,25 @@ __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete yet is suspended
+// until the phase completes or about `ns` nanoseconds have passed, instead of returning at once
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Polling loop of mbar_wait, kept out of line: a phase that has already completed costs one
-// try_wait (about 50 cycles) instead of the loop's setup (about 190 cycles measured).
+// try_wait (about 50 cycles) instead of the loop's setup (about 190 cycles measured).  Each poll
+// suspends for up to 1 us, so a waiting warp issues few instructions while it waits.
 static __device__ __noinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort,
                                                    uint32_t limit) {
     for (uint32_t i = 0; i < limit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_for(bar, parity, 1000u)) return true;
         if (*abort) return false;
         if (i > 64) __nanosleep(i > 4096 ? 256 : 32);
     }
