@@ -158,7 +158,7 @@ cudaEvent_t take_event() {
 }
 const char* kKernelNames[KID_COUNT] = {
     "chunk_end", "carry_scan", "fwd_chunk", "dsym", "bwd_chunk", "cot_scan", "correct",
-    "tc_fwd_chunk", "tc_chunk_end", "tc_bwd_chunk", "tc_correct", "check_finite", "m2_reduce"};
+    "tc_fwd_chunk", "tc_chunk_end", "tc_bwd_chunk", "tc_correct", "check_finite", "m2_reduce", "drot_sum"};
 }  // namespace
 
 void mm_prof_mark(int kid, int begin, cudaStream_t st) {

@@ -165,7 +165,9 @@ bool fast_supported(const MMParams& P, bool bf16, int backward) {
 }
 
 size_t fast_scratch_bytes(const MMParams& P, int backward) {
-    return backward ? fastk::bwd_anchor_bytes() : fastk::fwd_partial_bytes(internal_params(P));
+    if (!backward) return fastk::fwd_partial_bytes(internal_params(P));
+    const size_t a = fastk::bwd_anchor_bytes();  // a multiple of 256 bytes
+    return a + fastk::bwd_drot2_bytes(P);
 }
 
 cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cudaStream_t st) {
@@ -208,8 +210,8 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     fa.da = A.da;
     fa.err = A.err;
     cudaError_t e;
-    // d_da and d_rot are accumulated by the kernels (sums over rows and over two passes): start
-    // from zero.  d_xhat / d_bhat at positions at or past valid_len are exactly zero; every
+    // d_da and d_rot start from zero: the kernels write them for valid positions only (d_rot as
+    // two partial sums that a second pass adds; d_da then gets the correction added).  d_xhat / d_bhat at positions at or past valid_len are exactly zero; every
     // position before is written.
     const size_t bs = (size_t)P.b * P.s;
     if ((e = cudaMemsetAsync(A.dda, 0, sizeof(float) * bs * P.h, st)) != cudaSuccess) return e;
@@ -236,7 +238,8 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     }
     if (grid > kMaxBwdGrid) grid = kMaxBwdGrid;
     float* anchors = reinterpret_cast<float*>(scratch);
-    if ((e = launch_tc_bwd(fa, A.E, anchors, A.dm2, A.dm1, A.dxhat, A.dbhat, A.dda, A.drot, maps, grid, st)) !=
+    float* drot2 = reinterpret_cast<float*>(scratch + bwd_anchor_bytes());
+    if ((e = launch_tc_bwd(fa, A.E, anchors, drot2, A.dm2, A.dm1, A.dxhat, A.dbhat, A.dda, A.drot, maps, grid, st)) !=
         cudaSuccess)
         return e;
     if ((e = generic_cot_scan(P, A.E, A.Dn, A.dinit, st)) != cudaSuccess) return e;

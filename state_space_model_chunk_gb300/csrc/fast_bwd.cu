@@ -25,9 +25,10 @@
 //
 // Warp roles: 0-7 compute (two threads per row, 64 columns each, handled as two 32-column
 // passes whose rotation partners stay inside the pass), 8 TMA (all 32 lanes issue copies), 9 MMA.
-// d_rot and d_da are summed over p with warp transpose-reductions and added to global memory
-// (zeroed by the host).  Every wait is bounded; a timeout sets the workspace error word and the
-// CTA winds down.
+// d_rot and d_da are summed over each warp's 32 rows with warp transpose-reductions; the two
+// warps of a chunk's 64 rows are then combined in a fixed order (d_da through shared memory at
+// the end of the item, d_rot by k_drot_pair_sum after the kernel).  Every wait is bounded; a
+// timeout sets the workspace error word and the CTA winds down.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -131,7 +132,8 @@ struct BwdArgs {
     __nv_bfloat16* dx;  // d_xhat
     __nv_bfloat16* db;  // d_bhat
     float* dda;         // d_da (zeroed by the host; added into)
-    float* drot;        // d_rot (zeroed by the host; added into)
+    float* drot;        // d_rot (zeroed by the host): partial sums over rows 0-31 of each chunk
+    float* drot2;       // [b,s,h,rw] workspace: partial sums over rows 32-63
 };
 
 __device__ __forceinline__ void fail(Ctl* ctl, int* err, int code) {
@@ -581,8 +583,10 @@ __global__ void __launch_bounds__(NTHR, 1)
             ptab[1] = (m < R && half_ok)
                           ? reinterpret_cast<uint64_t>(B.db + off_b(P, I.bb, (2 * I.k + half) * FL, 0, I.hh) + m)
                           : 0ull;
+            // d_rot: the warp of rows 0-31 of a chunk writes its partial sums into d_rot, the warp
+            // of rows 32-63 into drot2; k_drot_pair_sum adds the two afterwards
             ptab[2] = (P.rw > 0 && chunk_ok && n < I.proc)
-                          ? reinterpret_cast<uint64_t>(B.drot + off_rot(P, I.bb, n * FL, I.hh))
+                          ? reinterpret_cast<uint64_t>(((warp & 1) ? B.drot2 : B.drot) + off_rot(P, I.bb, n * FL, I.hh))
                           : 0ull;
             // this warp's d_da partials for its chunk (the four warps of a chunk are summed in a
             // fixed order at the end of the item, so that d_da does not depend on timing)
@@ -848,9 +852,12 @@ __global__ void __launch_bounds__(NTHR, 1)
                         const bool live = t < Tch;
                         const float* cf = coefs + (o * 2 + ch) * 128;
                         const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + o * 1024 + ch * 512);
-                        float* const drot_t = ptab[2] ? reinterpret_cast<float*>(ptab[2]) + (int64_t)t * P.h * P.rw
-                                                      : nullptr;
-                        const bool rot_out = drot_t != nullptr;
+                        const bool rot_out = ptab[2] != 0ull;
+                        // this lane's d_rot partial of each pass, stored after the g tile has been
+                        // handed over (its row address is formed there too, so that it is not held
+                        // in registers through the passes)
+                        float drv[4] = {0.f, 0.f, 0.f, 0.f};
+                        int dri[4] = {-1, -1, -1, -1};  // [pass] (complex pairs), [2 pass + slot] (quaternions)
                         if (!live) {  // past valid_len: d_c = 0, so g_t = e_{t+1} g_{t+1}
                             tc::tc_fence_before();
                             __syncwarp();
@@ -889,7 +896,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     }
                                     transpose_reduce16(v, lane);
                                     const int ang = 8 * ((lane & 8) ? G[sb] : G[sa]) + (lane & 7);
-                                    if (lane < 16 && ang < P.na && rot_out) atomicAdd(drot_t + ang, v[0]);
+                                    if (lane < 16 && ang < P.na && rot_out) { drv[pass] = v[0]; dri[pass] = ang; }
                                 } else if (act_a) {
                                     float v[8];
                                     {
@@ -900,7 +907,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     }
                                     transpose_reduce8(v, lane);
                                     const int ang = 8 * G[sa] + (lane & 7);
-                                    if (lane < 8 && ang < P.na && rot_out) atomicAdd(drot_t + ang, v[0]);
+                                    if (lane < 8 && ang < P.na && rot_out) { drv[pass] = v[0]; dri[pass] = ang; }
                                 }
                             } else if (ROTK == ROT_HALF) {
                                 if (!(LAYB && pass == 1) && act_a) {
@@ -921,7 +928,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     }
                                     transpose_reduce16(v, lane);
                                     const int ang = 16 * G[sa] + (lane & 15);
-                                    if (lane < 16 && ang < P.na && rot_out) atomicAdd(drot_t + ang, v[0]);
+                                    if (lane < 16 && ang < P.na && rot_out) { drv[pass] = v[0]; dri[pass] = ang; }
                                 }
                             } else if (ROTK == ROT_QUAT) {
                                 // sum_p d_c (x) conj(c) per 4-block, then (.) (x) Q / |Q|^2
@@ -954,7 +961,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                                         hamilton(s0q, s1q, s2q, s3q, Q[0], Q[1], Q[2], Q[3], o0, o1, o2, o3);
                                         const float inv = 1.f / (Q[0] * Q[0] + Q[1] * Q[1] + Q[2] * Q[2] + Q[3] * Q[3]);
                                         const float val = comp == 0 ? o0 : comp == 1 ? o1 : comp == 2 ? o2 : o3;
-                                        atomicAdd(drot_t + 4 * blk + comp, inv * val);
+                                        drv[2 * pass + sl] = inv * val;
+                                        dri[2 * pass + sl] = 4 * blk + comp;
                                     }
                                 }
                             }
@@ -977,6 +985,12 @@ __global__ void __launch_bounds__(NTHR, 1)
                         tc::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&ctl->gfull);
+                        if (rot_out) {  // the row address only now, so it is not held through the passes
+                            float* const drot_t = reinterpret_cast<float*>(ptab[2]) + (int64_t)t * P.h * P.rw;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                if (dri[k] >= 0) drot_t[dri[k]] = drv[k];
+                        }
                     };
                     // ---- d_xhat (lanes = rows) and d_bhat (lanes = r) of token t
                     auto step_out = [&](int t) {
@@ -1065,15 +1079,34 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
 }
 
+// d_rot = (sum over rows 0-31) + (sum over rows 32-63) of every valid token, in that order: the
+// two row warps of a chunk store their partial sums with plain stores, one into d_rot and one into
+// the workspace, and this pass adds them (no atomics, and a result that does not depend on
+// timing).  One float4 per thread; rows past valid_len keep the zeros the host wrote.
+__global__ void __launch_bounds__(256) k_drot_pair_sum(const __grid_constant__ MMParams P, float* __restrict__ drot,
+                                                       const float* __restrict__ drot2, int64_t n4) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    const int64_t row = i / (P.rw >> 2);  // (bb, t, hh)
+    const int64_t bt = row / P.h;
+    const int bb = (int)(bt / P.s), t = (int)(bt - (int64_t)bb * P.s);
+    if (t >= P.valid[bb]) return;
+    float4 a = reinterpret_cast<float4*>(drot)[i];
+    const float4 c = reinterpret_cast<const float4*>(drot2)[i];
+    a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+    reinterpret_cast<float4*>(drot)[i] = a;
+}
+
 }  // namespace fastbwd
 
 // ----------------------------------------------------------------------------- host side
 namespace fastk {
 
 size_t bwd_anchor_bytes() { return (size_t)kMaxBwdGrid * fastbwd::NANCHOR * 128 * 128 * sizeof(float); }
+size_t bwd_drot2_bytes(const MMParams& P) { return (size_t)P.b * P.s * P.h * P.rw * sizeof(float); }
 
-cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, const float* dm2, const float* dm1, void* dx,
-                          void* db, float* dda, float* drot, const TensorMaps& maps, int grid, cudaStream_t st) {
+cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, float* drot2, const float* dm2, const float* dm1,
+                          void* dx, void* db, float* dda, float* drot, const TensorMaps& maps, int grid, cudaStream_t st) {
     using namespace fastbwd;
     BwdArgs a;
     a.F = fa;
@@ -1085,6 +1118,7 @@ cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, const fl
     a.db = static_cast<__nv_bfloat16*>(db);
     a.dda = dda;
     a.drot = drot;
+    a.drot2 = drot2;
     // channel slots per chunk in the span tiles: 4 when C <= 4, else 8
     decltype(&tc_bwd_kernel<ROT_NONE, 0, 2>) kern;
     const bool c8 = fa.P.C > 4;
@@ -1102,6 +1136,11 @@ cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, const fl
     mm_prof_mark(KID_FAST_BWD, 1, st);
     kern<<<grid, NTHR, SMEM_BYTES, st>>>(a, maps.x, maps.b, maps.rot, maps.da64);
     mm_prof_mark(KID_FAST_BWD, 0, st);
+    if ((e = cudaGetLastError()) != cudaSuccess || fa.P.rw == 0) return e;
+    const int64_t n4 = (int64_t)fa.P.b * fa.P.s * fa.P.h * (fa.P.rw >> 2);
+    mm_prof_mark(KID_DROT_SUM, 1, st);
+    k_drot_pair_sum<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(fa.P, drot, drot2, n4);
+    mm_prof_mark(KID_DROT_SUM, 0, st);
     return cudaGetLastError();
 }
 

@@ -229,8 +229,9 @@ cudaError_t encode_grad_maps(const MMParams& P, const void* dx, const void* db, 
 cudaError_t launch_tc_corr(const FastArgs& fa, const float* da, const float* E, void* dx, void* db, float* dda,
                            const TensorMaps& maps, cudaStream_t st);
 size_t bwd_anchor_bytes();
+size_t bwd_drot2_bytes(const MMParams& P);  // the backward's second d_rot partial, [b,s,h,rw] fp32
 size_t fwd_partial_bytes(const MMParams& P);  // internal chunking (nc = s / 64)
-cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, const float* dm2, const float* dm1, void* dx,
-                          void* db, float* dda, float* drot, const TensorMaps& maps, int grid, cudaStream_t st);
+cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, float* drot2, const float* dm2, const float* dm1,
+                          void* dx, void* db, float* dda, float* drot, const TensorMaps& maps, int grid, cudaStream_t st);
 
 }  // namespace fastk

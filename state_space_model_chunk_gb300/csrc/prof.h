@@ -16,6 +16,7 @@ enum MMKernelId {
     KID_FAST_CORRECT,
     KID_FINITE,
     KID_M2_REDUCE,
+    KID_DROT_SUM,
     KID_COUNT
 };
 
