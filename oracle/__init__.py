@@ -11,6 +11,9 @@ shares no code with it.
 * ``chunked_ref.py`` -- a NumPy restatement of the pages' own chunkwise algorithm
   (``chunk_decay``, ``chunk_states``, ``rotate_chunk``, ``boundary_carries``,
   ``moments_phys_bwd``), used only to pin the token-level oracle.
+* ``rotation_steps.py`` -- the per-token cumulative rotation built from per-token steps (angle
+  steps summed, quaternion steps multiplied) and that build's gradient, for calls that pass the
+  rotation as steps.
 """
 from __future__ import annotations
 
