@@ -38,7 +38,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from state_space_model_chunk_gb300 import binding  # noqa: E402
-from state_space_model_chunk_gb300.synthetic import WORKLOADS, make_inputs, slice_bh  # noqa: E402
+from state_space_model_chunk_gb300.synthetic import WORKLOADS, make_inputs, make_rot_steps, slice_bh  # noqa: E402
 
 SM_COUNT_GB300 = 152
 L2_FLUSH_BELOW = 3 * 129 * 2**20  # operands below this size get an L2 flush between timed steps
@@ -58,6 +58,9 @@ def parse():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size (profiling runs)")
     ap.add_argument("--recompute-carries", action="store_true",
                     help="backward recomputes the chunk carries instead of taking the forward's")
+    ap.add_argument("--rot-steps", action="store_true",
+                    help="pass the rotation as per-token steps (MM_FLAG_ROT_STEPS): the library builds the "
+                         "cumulative rotation and returns the gradient w.r.t. the steps")
     return ap.parse_args()
 
 
@@ -179,9 +182,12 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------- CPU oracle
-def oracle_sample(w, inp, pairs, seq):
-    """Run the oracle (fwd + bwd) on (b,h) pairs over the first `seq` tokens; returns seconds."""
+def oracle_sample(w, inp, pairs, seq, rot_steps=False):
+    """Run the oracle (fwd + bwd) on (b,h) pairs over the first `seq` tokens; returns seconds.
+    With `rot_steps` the input rotation is per-token steps: the oracle builds the cumulative
+    rotation and takes the gradient back to the steps, inside the timing."""
     import oracle
+    from oracle import rotation_steps
     subs = [slice_bh(inp, bb, hh) for bb, hh in pairs]
     st = {k: torch.cat([s[k] for s in subs], 0) for k in subs[0]}
     f = lambda t: t.to(torch.float64).numpy()
@@ -189,14 +195,17 @@ def oracle_sample(w, inp, pairs, seq):
     rot = f(st["rot"][:, :seq])
     vl = np.minimum(st["valid_len"].numpy(), seq)
     t0 = time.perf_counter()
-    oracle.moments_fwd(x, bh, da, rot, f(st["initial"]), vl, rot_kind=w.rot, rope_dim=w.rope_dim,
+    cum = rotation_steps.build(rot, w.rot) if rot_steps else rot
+    oracle.moments_fwd(x, bh, da, cum, f(st["initial"]), vl, rot_kind=w.rot, rope_dim=w.rope_dim,
                        quat_blocks=w.quat_blocks)
-    oracle.moments_bwd(x, bh, da, rot, f(st["initial"]), vl, f(st["d_m2"]), f(st["d_m1"]), rot_kind=w.rot,
-                       rope_dim=w.rope_dim, quat_blocks=w.quat_blocks)
+    g = oracle.moments_bwd(x, bh, da, cum, f(st["initial"]), vl, f(st["d_m2"]), f(st["d_m1"]), rot_kind=w.rot,
+                           rope_dim=w.rope_dim, quat_blocks=w.quat_blocks)
+    if rot_steps:
+        rotation_steps.build_vjp(rot, g["d_rot"], w.rot)
     return time.perf_counter() - t0, int(vl.sum())
 
 
-def cpu_baseline(w, inp, budget_s=15.0):
+def cpu_baseline(w, inp, budget_s=15.0, rot_steps=False):
     import oracle
     oracle.build()
     threads = oracle.threads()
@@ -204,10 +213,10 @@ def cpu_baseline(w, inp, budget_s=15.0):
     # calibrate on a short prefix, then size the sample to about `budget_s` seconds
     pairs = [(int(rng.integers(w.b)), int(rng.integers(w.h))) for _ in range(threads)]
     probe = min(w.s, 256)
-    dt, _ = oracle_sample(w, inp, pairs, probe)
+    dt, _ = oracle_sample(w, inp, pairs, probe, rot_steps)
     seq = int(min(w.s, max(probe, probe * budget_s / max(dt, 1e-3))))
     seq = max(w.chunk_len, seq // w.chunk_len * w.chunk_len)
-    dt, toks = oracle_sample(w, inp, pairs, seq)
+    dt, toks = oracle_sample(w, inp, pairs, seq, rot_steps)
     value = toks / w.h / dt  # token-head work divided by heads = tokens of the metric
     return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(pairs)} (b,h) pairs x first {seq} tokens of {w.name}, fp64 fwd+bwd, "
@@ -222,15 +231,17 @@ def run_reference(args):
     oracle.build()
     w = WORKLOADS[args.workload]
     inp = make_inputs(w)
+    if args.rot_steps and w.rot != "none":
+        inp["rot"] = make_rot_steps(w)
     threads = oracle.threads()
     rng = np.random.default_rng(0)
     pairs = [(int(rng.integers(w.b)), int(rng.integers(w.h))) for _ in range(threads)]
     seq = min(w.s, 256)
     for _ in range(args.warmup):
-        oracle_sample(w, inp, pairs, seq)
+        oracle_sample(w, inp, pairs, seq, args.rot_steps)
     tot_t, tot_tok = 0.0, 0
     for _ in range(args.steps):
-        dt, toks = oracle_sample(w, inp, pairs, seq)
+        dt, toks = oracle_sample(w, inp, pairs, seq, args.rot_steps)
         tot_t += dt
         tot_tok += toks
     value = tot_tok / w.h / tot_t
@@ -289,9 +300,12 @@ def run_ours(args):
     if args.batch:
         w = w.scaled(b=args.batch)
     inp = make_inputs(w)   # every rank runs its own replica of the workload (weak scaling)
+    steps = args.rot_steps and w.rot != "none"
+    if steps:  # the rotation as per-token steps; the library builds the cumulative rotation
+        inp["rot"] = make_rot_steps(w)
     ntok = tokens_of(inp, w.s)
     spec = binding.Spec(w.b, w.s, w.C, w.h, w.p, w.r, w.chunk_len, w.rot, w.rope_dim, w.quat_blocks, w.dtype,
-                        args.force_generic)
+                        args.force_generic, steps)
     lib = binding.load()
     d = {k: v.to(dev) for k, v in inp.items() if k != "valid_len"}
     rot = d["rot"] if d["rot"].numel() else None
@@ -454,7 +468,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, inp)
+        cpu = cpu_baseline(w, inp, rot_steps=steps)
 
     # whole-step algorithmic rate (F per token-head, fwd+bwd) against the sustained bf16 peak
     step_tflops = None
@@ -482,7 +496,9 @@ def run_ours(args):
                        "chunks64_processed": int(sum((min(int(v), w.s) + 63) // 64 for v in vl)),
                        "chunks64_total": int(w.b * (w.s // 64)),
                        "carries": "recomputed by the backward" if args.recompute_carries
-                       else "forward's, reused by the backward"},
+                       else "forward's, reused by the backward",
+                       "rotation_input": "per-token steps, cumulative rotation built on the GPU" if steps
+                       else "cumulative"},
             "e2e": e2e, "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu, "clocks": clk,
             "kernels_ms_per_step": {k: v[0] / args.steps for k, v in kernels.items()},
             "step_tflops": step_tflops,

@@ -88,6 +88,20 @@ typedef enum {
  * marks the workspace if any element is NaN or infinite.  mm_device_status() then reports
  * MM_ERR_NONFINITE.  Off by default; it costs one read of the outputs. */
 #define MM_FLAG_CHECK_FINITE 0x4u
+/* The rotation is given as per-token steps instead of the cumulative rotation: `rot` holds angle
+ * steps [b, s, h, rope_dim/2] (complex kinds) or quaternion steps [b, s, h, J, 4], and the library
+ * builds the cumulative rotation the operator takes ("recalculated.rs", RotPrim: cumulative
+ * angles / cumulative unit quaternions; their producer, RotationSeq / rotation::quat_mul, is named
+ * there but not given).  Reading: angles theta_t = sum_{u<=t} dtheta_u (inclusive prefix sum along
+ * the sequence); quaternions Q_t = q_t (x) Q_{t-1} from Q_{-1} = 1 (Hamilton product as
+ * quat_mul_prim).  moments_bwd then returns in d_rot the gradient w.r.t. the steps (same shape as
+ * `rot`): d_dtheta_u = sum_{t>=u} d_theta_t; G_t = dQ_t + conj(q_{t+1}) (x) G_{t+1},
+ * d_q_t = G_t (x) conj(Q_{t-1}).  Steps past valid_len get zero gradient.  The build and its
+ * gradient run as extra passes over [b, s, h, rw] in the workspace (mm_workspace_bytes counts
+ * them when the flag is set); a backward that takes the forward's carries
+ * (MM_FLAG_REUSE_CARRIES, honoured) also takes the cumulative rotation the forward built.
+ * Ignored when the problem has no rotation. */
+#define MM_FLAG_ROT_STEPS 0x8u
 /* moments_fwd only, for testing the device failure path: on the tensor-core path every CTA of the
  * chunk-end kernel waits once, with a short poll limit, for an mbarrier phase that nothing
  * completes.  The bounded wait gives up, the kernels wind down without faulting or hanging, the

@@ -28,6 +28,7 @@ ROT = {"none": 0, "pairwise": 1, "half": 2, "quat": 3}
 MM_FLAG_FORCE_GENERIC = 0x1
 MM_FLAG_REUSE_CARRIES = 0x2
 MM_FLAG_CHECK_FINITE = 0x4  # debug: outputs checked for NaN / inf, reported by device_status()
+MM_FLAG_ROT_STEPS = 0x8  # rot holds per-token steps; the library builds the cumulative rotation
 MM_FLAG_TEST_WAIT_TIMEOUT = 0x80000000  # testing only: see include/moments.h
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda", 5: "nonfinite",
           6: "timeout"}
@@ -100,18 +101,22 @@ class Spec:
     quat_blocks: int = 0
     dtype: str = "bf16"
     force_generic: bool = False
+    rot_steps: bool = False  # rot is per-token steps (MM_FLAG_ROT_STEPS); d_rot is w.r.t. the steps
 
     def problem(self, extra_flags: int = 0) -> Problem:
+        flags = (MM_FLAG_FORCE_GENERIC if self.force_generic else 0) | \
+            (MM_FLAG_ROT_STEPS if self.rot_steps else 0) | extra_flags
         return Problem(self.b, self.s, self.C, self.h, self.p, self.r, self.chunk_len,
                        MM_BF16 if self.dtype == "bf16" else MM_F32, ROT[self.rot], self.rope_dim,
-                       self.quat_blocks, (MM_FLAG_FORCE_GENERIC if self.force_generic else 0) | extra_flags, 0)
+                       self.quat_blocks, flags, 0)
 
     @staticmethod
-    def from_tensors(xhat, bhat, chunk_len, rot="none", rope_dim=0, quat_blocks=0, force_generic=False):
+    def from_tensors(xhat, bhat, chunk_len, rot="none", rope_dim=0, quat_blocks=0, force_generic=False,
+                     rot_steps=False):
         b, s, C, h, p = xhat.shape
         r = bhat.shape[-1]
         dt = "bf16" if xhat.dtype == torch.bfloat16 else "f32"
-        return Spec(b, s, C, h, p, r, chunk_len, rot, rope_dim, quat_blocks, dt, force_generic)
+        return Spec(b, s, C, h, p, r, chunk_len, rot, rope_dim, quat_blocks, dt, force_generic, rot_steps)
 
 
 def workspace_bytes(spec: Spec, backward: bool) -> int:
@@ -283,7 +288,9 @@ class Moments(torch.autograd.Function):
         return g["d_xhat"], g["d_bhat"], g["d_da"], g["d_rot"], g["d_initial"], None, None
 
 
-def moments(xhat, bhat, da, rot, initial, valid_len, chunk_len, rot_kind="none", rope_dim=0, quat_blocks=0):
-    """Differentiable (m2, m1); see :class:`Moments`."""
-    spec = Spec.from_tensors(xhat, bhat, chunk_len, rot_kind, rope_dim, quat_blocks)
+def moments(xhat, bhat, da, rot, initial, valid_len, chunk_len, rot_kind="none", rope_dim=0, quat_blocks=0,
+            rot_steps=False):
+    """Differentiable (m2, m1); see :class:`Moments`.  ``rot_steps``: ``rot`` holds per-token
+    steps (angle increments or per-token quaternions) and its gradient is w.r.t. them."""
+    spec = Spec.from_tensors(xhat, bhat, chunk_len, rot_kind, rope_dim, quat_blocks, rot_steps=rot_steps)
     return Moments.apply(xhat, bhat, da, rot, initial, valid_len, spec)

@@ -11,6 +11,7 @@
 #include "generic.h"
 #include "noalloc.h"
 #include "prof.h"
+#include "rot_steps.h"
 
 namespace {
 
@@ -22,6 +23,8 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
     size_t Hc = 0, Dn = 0, E = 0, dsym = 0, traj = 0, fast = 0, total = 0;
+    size_t cum = 0, dcum = 0, rsc = 0;  // MM_FLAG_ROT_STEPS: cumulative rotation, its gradient, scan scratch
+    bool steps = false;
 };
 
 bool valid_problem(const mm_problem* P) {
@@ -98,6 +101,12 @@ Layout layout(const mm_problem* P, int backward) {
     size_t off = kHeader;  // header: device error word
     L.Hc = off; off = align_up(off + sizeof(float) * nbh * nc * pr);
     L.Dn = off; off = align_up(off + sizeof(float) * nbh * nc);
+    // MM_FLAG_ROT_STEPS: the cumulative rotation sits right after the carries, at the same offset
+    // in the forward's and the backward's layout, so a backward reusing the forward's carries
+    // reuses it too
+    L.steps = (P->flags & MM_FLAG_ROT_STEPS) && M.rw > 0;
+    const size_t nrot = sizeof(float) * (size_t)P->b * P->s * P->h * M.rw;
+    if (L.steps) { L.cum = off; off = align_up(off + nrot); }
     if (backward) {
         L.E = off; off = align_up(off + sizeof(float) * nbh * nc * pr);
         L.dsym = off; off = align_up(off + sizeof(float) * nbh * (size_t)P->r * P->r);
@@ -106,6 +115,10 @@ Layout layout(const mm_problem* P, int backward) {
         L.fast = off; off = align_up(off + fast_scratch_bytes(M, backward));
     } else if (backward) {
         L.traj = off; off = align_up(off + sizeof(float) * (size_t)kTrajSlots * P->chunk_len * pr);
+    }
+    if (L.steps) {
+        if (backward) { L.dcum = off; off = align_up(off + nrot); }
+        L.rsc = off; off = align_up(off + rot_steps_scratch_bytes(M));
     }
     L.total = off;
     if (backward) {
@@ -158,7 +171,7 @@ cudaEvent_t take_event() {
 }
 const char* kKernelNames[KID_COUNT] = {
     "chunk_end", "carry_scan", "fwd_chunk", "dsym", "bwd_chunk", "cot_scan", "correct",
-    "tc_fwd_chunk", "tc_chunk_end", "tc_bwd_chunk", "tc_correct", "check_finite", "m2_reduce", "drot_sum"};
+    "tc_fwd_chunk", "tc_chunk_end", "tc_bwd_chunk", "tc_correct", "check_finite", "m2_reduce", "drot_sum", "rot_steps"};
 }  // namespace
 
 void mm_prof_mark(int kid, int begin, cudaStream_t st) {
@@ -278,7 +291,12 @@ mm_status moments_fwd(const mm_problem* prob, const void* xhat, const void* bhat
     A.test_wait_timeout = (prob->flags & MM_FLAG_TEST_WAIT_TIMEOUT) ? 1 : 0;
     A.err = at<int>(workspace, 0);
     if (cudaMemsetAsync(A.err, 0, 2 * sizeof(int), cs) != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
-    cudaError_t e = fast ? fast_fwd(M, A, at<char>(workspace, L.fast), cs) : generic_fwd(M, bf16, A, cs);
+    cudaError_t e = cudaSuccess;
+    if (L.steps) {  // the operator runs on the cumulative rotation built from the steps
+        e = rot_steps_build(M, rot, at<float>(workspace, L.cum), at<void>(workspace, L.rsc), cs);
+        A.rot = at<float>(workspace, L.cum);
+    }
+    if (e == cudaSuccess) e = fast ? fast_fwd(M, A, at<char>(workspace, L.fast), cs) : generic_fwd(M, bf16, A, cs);
     if (e == cudaSuccess && (prob->flags & MM_FLAG_CHECK_FINITE)) {
         FiniteSegs fs{};
         fs.n = 2;
@@ -324,15 +342,22 @@ mm_status moments_bwd(const mm_problem* prob, const void* xhat, const void* bhat
     A.dsym = at<float>(workspace, L.dsym);
     A.err = at<int>(workspace, 0);
     if (cudaMemsetAsync(A.err, 0, 2 * sizeof(int), cs) != cudaSuccess) { cudaGetLastError(); return MM_ERR_CUDA; }
-    cudaError_t e;
-    if (fast) {
+    cudaError_t e = cudaSuccess;
+    if (L.steps) {  // the operator's gradient w.r.t. the cumulative rotation goes to the workspace
+        // (the forward of the same problem left the cumulative rotation where the carries are)
+        if (!A.reuse_carries) e = rot_steps_build(M, rot, at<float>(workspace, L.cum), at<void>(workspace, L.rsc), cs);
+        A.rot = at<float>(workspace, L.cum);
+        A.drot = at<float>(workspace, L.dcum);
+    }
+    if (e != cudaSuccess) {
+    } else if (fast) {
         e = fast_bwd(M, A, at<char>(workspace, L.fast), cs);
     } else {
         // every gradient position not written by a kernel must read zero
         if (cudaMemsetAsync(d_xhat, 0, es * nx, cs) != cudaSuccess ||
             cudaMemsetAsync(d_bhat, 0, es * nb, cs) != cudaSuccess ||
             cudaMemsetAsync(d_da, 0, sizeof(float) * ntok * prob->h, cs) != cudaSuccess ||
-            (nrot && cudaMemsetAsync(d_rot, 0, sizeof(float) * nrot, cs) != cudaSuccess)) {
+            (nrot && cudaMemsetAsync(A.drot, 0, sizeof(float) * nrot, cs) != cudaSuccess)) {
             cudaGetLastError();
             return MM_ERR_CUDA;
         }
@@ -341,6 +366,8 @@ mm_status moments_bwd(const mm_problem* prob, const void* xhat, const void* bhat
         int grid = (int)(chunks < kTrajSlots ? chunks : kTrajSlots);
         e = generic_bwd(M, bf16, A, grid, cs);
     }
+    if (e == cudaSuccess && L.steps)  // through the build: the gradient w.r.t. the steps
+        e = rot_steps_vjp(M, rot, A.rot, A.drot, d_rot, at<void>(workspace, L.rsc), cs);
     if (e == cudaSuccess && (prob->flags & MM_FLAG_CHECK_FINITE)) {
         FiniteSegs fs{};
         const void* outs[5] = {d_xhat, d_bhat, d_da, d_rot, d_initial};

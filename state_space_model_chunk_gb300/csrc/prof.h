@@ -17,6 +17,7 @@ enum MMKernelId {
     KID_FINITE,
     KID_M2_REDUCE,
     KID_DROT_SUM,
+    KID_ROT_STEPS,
     KID_COUNT
 };
 

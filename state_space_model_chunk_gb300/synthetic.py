@@ -132,6 +132,24 @@ def _quat_walk(b, s, h, J, g):
     return out.to(torch.float32)
 
 
+def make_rot_steps(w: Workload) -> torch.Tensor:
+    """Per-token rotation steps for calls made with the rotation given as steps: angle steps
+    [b,s,h,rope_dim/2] ~ U(-0.3, 0.3) (the distribution the cumulative angles above are summed
+    from), or per-token unit quaternions [b,s,h,J,4] = normalise((1,0,0,0) + 0.05 N(0,1)^4),
+    drawn and normalised in fp64 and stored fp32.  A generator of its own (seed + 1000), so the
+    other inputs of the workload do not change."""
+    g = torch.Generator("cpu")
+    g.manual_seed(w.seed + 1000)
+    b, s, h = w.b, w.s, w.h
+    if w.rot in ("pairwise", "half"):
+        return (torch.rand((b, s, h, w.n_angles), generator=g) * 0.6 - 0.3).contiguous()
+    if w.rot == "quat":
+        q = torch.randn((b, s, h, w.quat_blocks, 4), generator=g, dtype=torch.float64) * QUAT_STEP_STD
+        q[..., 0] += 1.0
+        return (q / q.norm(dim=-1, keepdim=True)).to(torch.float32).contiguous()
+    return torch.zeros((b, s, h, 0))
+
+
 def slice_bh(inp: dict, bsel: int, hsel: int) -> dict:
     """The inputs of one (batch row, head) pair as a b=1, h=1 problem."""
     out = {}

@@ -137,6 +137,7 @@ def test_flag_values_match_the_header():
     assert int(flags["MM_FLAG_REUSE_CARRIES"], 16) == binding.MM_FLAG_REUSE_CARRIES
     assert int(flags["MM_FLAG_TEST_WAIT_TIMEOUT"], 16) == binding.MM_FLAG_TEST_WAIT_TIMEOUT
     assert int(flags["MM_FLAG_CHECK_FINITE"], 16) == binding.MM_FLAG_CHECK_FINITE
+    assert int(flags["MM_FLAG_ROT_STEPS"], 16) == binding.MM_FLAG_ROT_STEPS
     spec = Spec(1, 64, 1, 2, 8, 16, 16)
     assert spec.problem(binding.MM_FLAG_REUSE_CARRIES).flags == binding.MM_FLAG_REUSE_CARRIES
 
@@ -162,3 +163,24 @@ def test_check_finite_flag_is_accepted_and_changes_no_sizing():
             assert lib.mm_path(ctypes.byref(spec.problem()), bwd) == \
                 lib.mm_path(ctypes.byref(spec.problem(binding.MM_FLAG_CHECK_FINITE)), bwd)
     assert lib.mm_status_string(5) == b"non-finite values detected"
+
+
+def test_rotation_steps_flag_sizes_the_build():
+    """MM_FLAG_ROT_STEPS adds the cumulative rotation (both calls), its gradient (backward) and the
+    scans' scratch to the workspace of a rotated problem, leaves a problem without rotation alone,
+    and does not change the kernel path."""
+    lib = binding.load()
+    for spec in (base_spec(), Spec(2, 256, 2, 4, 64, 128, 64, "pairwise", 64),
+                 Spec(2, 256, 1, 4, 64, 128, 64, "quat", 0, 8)):
+        flagged = spec.problem(binding.MM_FLAG_ROT_STEPS)
+        nrot = 4 * spec.b * spec.s * spec.h * (spec.rope_dim // 2 if spec.rot != "quat" else 4 * spec.quat_blocks)
+        for bwd in (0, 1):
+            plain = lib.mm_workspace_bytes(ctypes.byref(spec.problem()), bwd)
+            more = lib.mm_workspace_bytes(ctypes.byref(flagged), bwd)
+            assert more >= plain + (2 if bwd else 1) * nrot and more % 256 == 0
+            assert lib.mm_path(ctypes.byref(spec.problem()), bwd) == lib.mm_path(ctypes.byref(flagged), bwd)
+    none = Spec(2, 256, 2, 4, 64, 128, 64)
+    for bwd in (0, 1):
+        assert lib.mm_workspace_bytes(ctypes.byref(none.problem(binding.MM_FLAG_ROT_STEPS)), bwd) == \
+            lib.mm_workspace_bytes(ctypes.byref(none.problem()), bwd)
+    assert Spec(**{**base_spec().__dict__, "rot_steps": True}).problem().flags & binding.MM_FLAG_ROT_STEPS
