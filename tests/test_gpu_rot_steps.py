@@ -25,6 +25,12 @@ CASES = [
     (WORKLOADS["quat_s2048"].scaled(name="steps_quat", b=2, s=384, h=3, quat_blocks=20, valid="ragged"), False),
     (WORKLOADS["quat_s2048"].scaled(name="steps_quat_simt", b=1, s=256, h=2, quat_blocks=8), True),
     (WORKLOADS["large_s4096"].scaled(name="steps_pairwise_simt", b=1, s=320, h=2, rope_dim=24), True),
+    # the scans' last 64-token chunk partial (s = 80), fp32 on the SIMT kernels
+    (WORKLOADS["tiny_fp32"].scaled(name="steps_partial_chunk", b=2, s=80, h=3, valid="fixed:71"), False),
+    (WORKLOADS["tiny_fp32"].scaled(name="steps_quat_partial", b=1, s=80, h=2, rot="quat", rope_dim=0,
+                                   quat_blocks=3, valid="fixed:80"), False),
+    # nothing valid: every output and gradient is zero
+    (WORKLOADS["large_s4096"].scaled(name="steps_none_valid", b=1, s=128, h=4, valid="fixed:0"), False),
 ]
 
 
