@@ -75,11 +75,11 @@ cudaError_t encode_grad_maps(const MMParams& P, const void* dx, const void* db, 
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
     }
-    {   // as b32, over d_bhat
-        cuuint64_t dims[5] = {64, (cuuint64_t)P.r / 64, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
-        cuuint64_t str[4] = {128, (cuuint64_t)P.r * 2, (cuuint64_t)P.h * P.r * 2, (cuuint64_t)P.C * P.h * P.r * 2};
-        cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)P.C, (cuuint32_t)corr_tps(P)};
-        if ((e = encode(&maps->db32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, db, dims, str, box,
+    {   // as b32, over d_bhat (a box's columns past r are skipped by the stores)
+        cuuint64_t dims[4] = {(cuuint64_t)P.r, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
+        cuuint64_t str[3] = {(cuuint64_t)P.r * 2, (cuuint64_t)P.h * P.r * 2, (cuuint64_t)P.C * P.h * P.r * 2};
+        cuuint32_t box[4] = {64, 1, (cuuint32_t)P.C, (cuuint32_t)corr_tps(P)};
+        if ((e = encode(&maps->db32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, db, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
     }
@@ -106,19 +106,20 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
                                     CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
     }
-    {   // bhat as [b*s, C, h, r/64, 64] bf16; box = one 64-wide half of the C rows
-        cuuint64_t dims[5] = {64, (cuuint64_t)P.r / 64, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
-        cuuint64_t str[4] = {128, (cuuint64_t)P.r * 2, (cuuint64_t)P.h * P.r * 2, (cuuint64_t)P.C * P.h * P.r * 2};
-        cuuint32_t box[5] = {64, 1, 1, (cuuint32_t)P.C, 1};
-        if ((e = encode(&maps->b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bhat, dims, str, box,
+    {   // bhat as [b*s, C, h, r] bf16; box = 64 columns (from column 64 a) of the C rows: columns
+        // past r read as zeros, so an r below 128 leaves the tiles' tail zero
+        cuuint64_t dims[4] = {(cuuint64_t)P.r, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
+        cuuint64_t str[3] = {(cuuint64_t)P.r * 2, (cuuint64_t)P.h * P.r * 2, (cuuint64_t)P.C * P.h * P.r * 2};
+        cuuint32_t box[4] = {64, 1, (cuuint32_t)P.C, 1};
+        if ((e = encode(&maps->b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, bhat, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
-        box[4] = 8;
-        if ((e = encode(&maps->b8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bhat, dims, str, box,
+        box[3] = 8;
+        if ((e = encode(&maps->b8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, bhat, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
-        box[4] = (cuuint32_t)corr_tps(P);
-        if ((e = encode(&maps->b32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bhat, dims, str, box,
+        box[3] = (cuuint32_t)corr_tps(P);
+        if ((e = encode(&maps->b32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, bhat, dims, str, box,
                                     CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
             return e;
     }
@@ -156,7 +157,10 @@ int fastk_chunk() { return fastk::FL; }
 
 bool fast_supported(const MMParams& P, bool bf16, int backward) {
     if (!bf16) return false;
-    if (P.p != 64 || (P.r != 64 && P.r != 128) || P.C < 1 || P.C > 8) return false;
+    // r: a multiple of 16 up to 128 (the tiles hold 128 columns, and the columns past r load as
+    // zeros); half-split pairs columns r / 2 apart, which the thread layouts hold for 64 or 128 only
+    if (P.p != 64 || P.r < 16 || P.r > 128 || P.r % 16 || P.C < 1 || P.C > 8) return false;
+    if (P.rot == ROT_HALF && P.r != 64 && P.r != 128) return false;
     if (P.s % fastk::FL || P.b > MM_MAX_B) return false;
     // rows of angles / quaternions are copied as 16-byte multiples, at most 128 floats
     if (P.rw % 4 || P.rw > 128) return false;

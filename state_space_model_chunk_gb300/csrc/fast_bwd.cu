@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     tc::tc_fence_after();
     const uint32_t tbase = ctl->tbase;
     volatile int* abort = &ctl->abort;
-    const uint32_t stage_tx = (uint32_t)C * 128u * (1u + (uint32_t)R / 64u);  // xhat + bhat rows of one chunk
+    const uint32_t stage_tx = (uint32_t)C * 128u * (1u + (uint32_t)(R + 63) / 64u);  // xhat + bhat rows of one chunk
 
     if (warp == WARP_TMA) {
         // ====================================================================== TMA producer
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         uint32_t slots = 0;         // per slot j: bit j = parity of its next release, bit 8 + j = release pending
         Par pr;
         bool ok = true;
-        const int nbx = 1 + R / 64;  // copies per token and chunk: xhat rows, bhat column blocks
+        const int nbx = 1 + (R + 63) / 64;  // copies per token and chunk: xhat rows, bhat column blocks
         auto wait_all = [&](uint64_t* bar, uint32_t parity) {
             ok = __all_sync(0xffffffffu, ok && tc::mbar_wait(bar, parity, abort));
         };
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     if (kind == 0)
                         tc::tma_load_4d(xb + jj * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row, &ctl->afull[b]);
                     else
-                        tc::tma_load_5d(bt + jj * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 0, kind - 1, I.hh, 0,
+                        tc::tma_load_4d(bt + jj * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 64 * (kind - 1), I.hh, 0,
                                         row, &ctl->afull[b]);
                 }
                 if (b) ++na1; else ++na0;
@@ -431,8 +431,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     tc::tma_load_4d(sm + OFF_SX + jj * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row,
                                                     &ctl->spanfull);
                                 else if (kind < nbx)
-                                    tc::tma_load_5d(sm + OFF_SB + jj * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 0,
-                                                    kind - 1, I.hh, 0, row, &ctl->spanfull);
+                                    tc::tma_load_4d(sm + OFF_SB + jj * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 64 * (kind - 1),
+                                                    I.hh, 0, row, &ctl->spanfull);
                                 else
                                     tc::tma_load_3d(sm + OFF_ROT + jj * 1024 + ch * 512, &tmr, 0, I.hh, row,
                                                     &ctl->spanfull);

@@ -142,7 +142,7 @@ __host__ __device__ inline int corr_tps(const MMParams& P) { return P.C <= 4 ? 3
 // 64-wide half of bhat, one token's rotation parameters and one 16-byte group of da.
 __host__ __device__ inline uint32_t stage_bytes(const FastArgs& A) {
     const MMParams& P = A.P;
-    return 128u * P.C + (uint32_t)(P.r / 64) * 128u * P.C + 4u * P.rw + (da_by_tma(P) ? 16u : 0u);
+    return 128u * P.C + (uint32_t)((P.r + 63) / 64) * 128u * P.C + 4u * P.rw + (da_by_tma(P) ? 16u : 0u);
 }
 
 // The four 16-column groups of a 128-column row that one thread owns.  Rotation partners

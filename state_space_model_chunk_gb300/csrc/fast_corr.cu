@@ -173,8 +173,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                 if (!tc::mbar_wait(&ctl->upd[s], (qq / NS) & 1, abort)) return false;
                 unsigned char* stg = sm + s * STAGE;
                 tc::tma_store_4d(&tmdx32, 0, shh[s], 0, srow[s], stg + SL_DX * SLOT);
-                for (int a = 0; a < R / 64; ++a)
-                    tc::tma_store_5d(&tmdb32, 0, a, shh[s], 0, srow[s], stg + (SL_DB + a) * SLOT);
+                for (int a = 0; a < (R + 63) / 64; ++a)
+                    tc::tma_store_4d(&tmdb32, 64 * a, shh[s], 0, srow[s], stg + (SL_DB + a) * SLOT);
                 tc::bulk_commit();
                 tc::bulk_wait_read0();
                 return true;
@@ -185,13 +185,13 @@ __global__ void __launch_bounds__(NTHR, 1)
                     const uint32_t s = q % NS;
                     if (q >= NS && !(ok = store_back(q - NS))) break;
                     unsigned char* stg = sm + s * STAGE;
-                    tc::mbar_arrive_expect_tx(&ctl->full[s], 2u * rows * 128u * (1u + (uint32_t)R / 64u));
+                    tc::mbar_arrive_expect_tx(&ctl->full[s], 2u * rows * 128u * (1u + (uint32_t)(R + 63) / 64u));
                     const int row = I.bb * P.s + I.n * FL + st * TPS;
                     tc::tma_load_4d(stg, &tmx32, 0, I.hh, 0, row, &ctl->full[s]);
                     tc::tma_load_4d(stg + SL_DX * SLOT, &tmdx32, 0, I.hh, 0, row, &ctl->full[s]);
-                    for (int a = 0; a < R / 64; ++a) {
-                        tc::tma_load_5d(stg + (1 + a) * SLOT, &tmb32, 0, a, I.hh, 0, row, &ctl->full[s]);
-                        tc::tma_load_5d(stg + (SL_DB + a) * SLOT, &tmdb32, 0, a, I.hh, 0, row, &ctl->full[s]);
+                    for (int a = 0; a < (R + 63) / 64; ++a) {
+                        tc::tma_load_4d(stg + (1 + a) * SLOT, &tmb32, 64 * a, I.hh, 0, row, &ctl->full[s]);
+                        tc::tma_load_4d(stg + (SL_DB + a) * SLOT, &tmdb32, 64 * a, I.hh, 0, row, &ctl->full[s]);
                     }
                     srow[s] = row;
                     shh[s] = I.hh;

@@ -148,12 +148,12 @@ __global__ void __launch_bounds__(NTHR, 2)
                         for (int t = 0; t < I.T; ++t) dst[t * 4 + (I.hh & 3)] = src[(int64_t)t * P.h];
                     }
                     const uint32_t bytes =
-                        rows * 128u * (1u + (uint32_t)R / 64u) + ((st == 0 && da_by_tma(P)) ? 1024u : 0u);
+                        rows * 128u * (1u + (uint32_t)(R + 63) / 64u) + ((st == 0 && da_by_tma(P)) ? 1024u : 0u);
                     tc::mbar_arrive_expect_tx(&ctl->full[s], bytes);
                     const int row = I.bb * P.s + I.n * FL + st * TPS;
                     tc::tma_load_4d(stg, &tmx8, 0, I.hh, 0, row, &ctl->full[s]);
-                    for (int a = 0; a < R / 64; ++a)
-                        tc::tma_load_5d(stg + (1 + a) * SLOT, &tmb8, 0, a, I.hh, 0, row, &ctl->full[s]);
+                    for (int a = 0; a < (R + 63) / 64; ++a)
+                        tc::tma_load_4d(stg + (1 + a) * SLOT, &tmb8, 64 * a, I.hh, 0, row, &ctl->full[s]);
                     if (st == 0 && da_by_tma(P))
                         tc::tma_load_2d(stg + 3 * SLOT, &tmd64, I.hh & ~3, I.bb * P.s + I.n * FL, &ctl->full[s]);
                 }

@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         // made warp-uniform so that all lanes leave together.
         uint32_t q = 0;
         bool ok = true;
-        const int nbx = 1 + R / 64, ncp = nbx + (P.rw ? 1 : 0) + 1;  // copies per token and chunk
+        const int nbx = 1 + (R + 63) / 64, ncp = nbx + (P.rw ? 1 : 0) + 1;  // copies per token and chunk
         for (int it = it0; it < it1 && ok; ++it) {
             const Item I = decode_item(A, it);
             for (int t = 0; t < I.T[0] && ok; ++t, ++q) {
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         if (kind == 0)
                             tc::tma_load_4d(sm + OFF_X + s * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row, &ctl->full[s]);
                         else if (kind < nbx)
-                            tc::tma_load_5d(sm + OFF_B + s * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 0, kind - 1,
+                            tc::tma_load_4d(sm + OFF_B + s * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 64 * (kind - 1),
                                             I.hh, 0, row, &ctl->full[s]);
                         else if (P.rw && kind == nbx)
                             tc::tma_load_3d(sm + OFF_ROT + s * 1024 + ch * 512, &tmr, 0, I.hh, row, &ctl->full[s]);

@@ -25,7 +25,8 @@ def spec_of(w, force_generic=False):
 def expected_fast(w, backward):
     """Whether the tensor-core kernels implement this workload (else the SIMT kernels run)."""
     rw = w.rope_dim // 2 if w.rot in ("pairwise", "half") else (4 * w.quat_blocks if w.rot == "quat" else 0)
-    return (w.dtype == "bf16" and w.p == 64 and w.r in (64, 128) and 1 <= w.C <= 8 and w.s % 64 == 0
+    r_ok = w.r in (64, 128) if w.rot == "half" else (w.r % 16 == 0 and 16 <= w.r <= 128)
+    return (w.dtype == "bf16" and w.p == 64 and r_ok and 1 <= w.C <= 8 and w.s % 64 == 0
             and rw % 4 == 0 and rw <= 128)
 
 
@@ -70,6 +71,13 @@ SMALL = [
     WORKLOADS["large_s4096"].scaled(name="large_fp32_small", b=1, s=128, h=2, dtype="f32", xb_scale="unit"),
     WORKLOADS["halfsplit_s1024"].scaled(name="half_partial_rope", b=2, s=192, h=3, rope_dim=20, chunk_len=32),
     WORKLOADS["large_s4096"].scaled(name="pairwise_r96_c3", b=2, s=128, C=3, h=2, r=96, rope_dim=40),
+    # r below 128 on the tensor cores (the tiles' tail columns load as zeros)
+    WORKLOADS["quat_s2048"].scaled(name="quat_r32", b=2, s=192, h=3, r=32, quat_blocks=8),
+    WORKLOADS["large_s4096"].scaled(name="pairwise_r48_c5", b=1, s=256, h=3, C=5, r=48, rope_dim=24,
+                                    valid="fixed:200"),
+    WORKLOADS["large_s4096"].scaled(name="norot_r112", b=2, s=128, h=2, r=112, rot="none", rope_dim=0),
+    # half-split with r = 96 pairs columns 48 apart: the SIMT kernels
+    WORKLOADS["halfsplit_s1024"].scaled(name="half_r96_simt", b=1, s=128, h=2, r=96, rope_dim=32),
     WORKLOADS["quat_s2048"].scaled(name="quat_partial_blocks", b=2, s=128, h=4, quat_blocks=20, C=2),
     WORKLOADS["tiny_fp32"].scaled(name="norot_odd", b=2, s=48, C=3, h=3, p=5, r=12, chunk_len=12, rot="none",
                                   rope_dim=0, valid="fixed:37"),
