@@ -252,7 +252,8 @@ def run_reference(args):
         "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "b": w.b, "s": w.s, "C": w.C, "h": w.h, "p": w.p, "r": w.r,
-                   "chunk_len": w.chunk_len, "rotation": w.rot},
+                   "chunk_len": w.chunk_len, "rotation": w.rot,
+                   "rotation_input": "per-token steps" if args.rot_steps and w.rot != "none" else "cumulative"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
