@@ -67,6 +67,8 @@ void fill_params(const mm_problem* P, const int64_t* valid_host, MMParams* out) 
     out->na = (P->rot == MM_ROT_PAIRWISE || P->rot == MM_ROT_HALF) ? (int)(P->rope_dim / 2) : 0;
     out->J = (P->rot == MM_ROT_QUAT) ? (int)P->quat_blocks : 0;
     out->rw = rot_width(P);
+    out->heads = out->h;
+    out->groups = 1;
     for (int64_t i = 0; i < P->b && valid_host; ++i) {
         int64_t v = valid_host[i];
         out->valid[i] = (int)(v < 0 ? 0 : (v > P->s ? P->s : v));
@@ -100,7 +102,10 @@ Layout layout(const mm_problem* P, int backward) {
     const size_t nc = (size_t)P->s / l_eff;
     size_t off = kHeader;  // header: device error word
     L.Hc = off; off = align_up(off + sizeof(float) * nbh * nc * pr);
-    L.Dn = off; off = align_up(off + sizeof(float) * nbh * nc);
+    // chunk decays: per head, or on the tensor-core path per 64-row group of a head (each group
+    // runs as a head of its own)
+    const size_t groups = (fast && P->p > 64) ? (size_t)P->p / 64 : 1;
+    L.Dn = off; off = align_up(off + sizeof(float) * nbh * groups * nc);
     // MM_FLAG_ROT_STEPS: the cumulative rotation sits right after the carries, at the same offset
     // in the forward's and the backward's layout, so a backward reusing the forward's carries
     // reuses it too
@@ -171,7 +176,8 @@ cudaEvent_t take_event() {
 }
 const char* kKernelNames[KID_COUNT] = {
     "chunk_end", "carry_scan", "fwd_chunk", "dsym", "bwd_chunk", "cot_scan", "correct",
-    "tc_fwd_chunk", "tc_chunk_end", "tc_bwd_chunk", "tc_correct", "check_finite", "m2_reduce", "drot_sum", "rot_steps"};
+    "tc_fwd_chunk", "tc_chunk_end", "tc_bwd_chunk", "tc_correct", "check_finite", "m2_reduce", "drot_sum", "rot_steps",
+    "group_sum"};
 }  // namespace
 
 void mm_prof_mark(int kid, int begin, cudaStream_t st) {

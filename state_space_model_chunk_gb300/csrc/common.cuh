@@ -16,6 +16,13 @@ struct MMParams {
     int na;                       // complex kinds: angles per token (rope_dim / 2); else 0
     int J;                        // quaternion blocks; else 0
     int rw;                       // floats of rot per (b, t, h): na or 4 J
+    // The tensor-core path splits a head's p state rows into `groups` groups of 64 rows and runs
+    // each group as a head of its own: h = heads * groups and p = 64 there, so that tensors
+    // indexed by state row (xhat, states, carries, d_xhat, d_initial) keep their layout, while the
+    // tensors shared by a head's rows (bhat, da, rot and their gradients, d_m2, d_m1) are indexed
+    // by the caller's head, h / groups.  Outside that path groups = 1 and heads = h.
+    int heads;
+    int groups;
     int valid[MM_MAX_B];          // valid_len per batch row, clamped to [0, s]
 };
 
@@ -35,14 +42,15 @@ __host__ __device__ inline int mm_chunk_rows(const MMParams& P, int bb, int n) {
 __device__ __forceinline__ int64_t off_x(const MMParams& P, int bb, int t, int c, int hh) {
     return ((((int64_t)bb * P.s + t) * P.C + c) * P.h + hh) * P.p;
 }
+// bhat / da / rot and their gradients: hh is the caller's head (see MMParams::heads)
 __device__ __forceinline__ int64_t off_b(const MMParams& P, int bb, int t, int c, int hh) {
-    return ((((int64_t)bb * P.s + t) * P.C + c) * P.h + hh) * P.r;
+    return ((((int64_t)bb * P.s + t) * P.C + c) * P.heads + hh) * P.r;
 }
 __device__ __forceinline__ int64_t off_da(const MMParams& P, int bb, int t, int hh) {
-    return ((int64_t)bb * P.s + t) * P.h + hh;
+    return ((int64_t)bb * P.s + t) * P.heads + hh;
 }
 __device__ __forceinline__ int64_t off_rot(const MMParams& P, int bb, int t, int hh) {
-    return (((int64_t)bb * P.s + t) * P.h + hh) * P.rw;
+    return (((int64_t)bb * P.s + t) * P.heads + hh) * P.rw;
 }
 // [b, h, nc, p, r] carries / cotangent carries
 __device__ __forceinline__ int64_t off_carry(const MMParams& P, int bb, int hh, int n) {

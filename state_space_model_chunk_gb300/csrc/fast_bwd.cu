@@ -1,5 +1,5 @@
 // fast_bwd.cu -- tcgen05 / TMA recompute backward of the state-moments operator (bf16 operands,
-// p = 64, r in {64, 128}, C <= 8).
+// 64 state rows per head -- larger p as 64-row groups run as heads --, r up to 128, C <= 8).
 //
 // Work item = a pair of 64-token chunks of one (batch row, head); the two chunks share the 128
 // TMEM lanes (row m = (chunk, p)) as in the forward.  This kernel is the chunk's own backward with
@@ -134,6 +134,9 @@ struct BwdArgs {
     float* dda;         // d_da (zeroed by the host; added into)
     float* drot;        // d_rot (zeroed by the host): partial sums over rows 0-31 of each chunk
     float* drot2;       // [b,s,h,rw] workspace: partial sums over rows 32-63
+    // elements between the slices of consecutive 64-row groups (MMParams::groups) in db, dda,
+    // drot and drot2; 0 with one group
+    int64_t db_slice, dda_slice, drot_slice;
 };
 
 __device__ __forceinline__ void fail(Ctl* ctl, int* err, int code) {
@@ -342,8 +345,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                 for (int i = lane; i < 2 * FL; i += 32) {
                     const int ch = i / FL, t = i % FL;
                     if (I.exists[ch])
-                        ida[(ch * FL + t) * 4 + (I.hh & 3)] =
-                            A.da[((int64_t)I.bb * P.s + (2 * I.k + ch) * FL + t) * P.h + I.hh];
+                        ida[(ch * FL + t) * 4 + (I.hd & 3)] =
+                            A.da[((int64_t)I.bb * P.s + (2 * I.k + ch) * FL + t) * P.heads + I.hd];
                 }
                 __syncwarp();
             }
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 tc::mbar_arrive_expect_tx(&ctl->itemfull, bytes);
                 for (int ch = 0; ch < 2; ++ch)
                     if (I.exists[ch] && da_by_tma(P))
-                        tc::tma_load_2d(sm + OFF_IDA + ch * 1024, &tmd, I.hh & ~3, I.bb * P.s + (2 * I.k + ch) * FL,
+                        tc::tma_load_2d(sm + OFF_IDA + ch * 1024, &tmd, I.hd & ~3, I.bb * P.s + (2 * I.k + ch) * FL,
                                         &ctl->itemfull);
             }
             // forward sweep: spans 0 .. nsp-2 alternate between the two span buffers (the last
@@ -378,7 +381,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     if (kind == 0)
                         tc::tma_load_4d(xb + jj * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row, &ctl->afull[b]);
                     else
-                        tc::tma_load_4d(bt + jj * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 64 * (kind - 1), I.hh, 0,
+                        tc::tma_load_4d(bt + jj * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 64 * (kind - 1), I.hd, 0,
                                         row, &ctl->afull[b]);
                 }
                 if (b) ++na1; else ++na0;
@@ -432,9 +435,9 @@ __global__ void __launch_bounds__(NTHR, 1)
                                                     &ctl->spanfull);
                                 else if (kind < nbx)
                                     tc::tma_load_4d(sm + OFF_SB + jj * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 64 * (kind - 1),
-                                                    I.hh, 0, row, &ctl->spanfull);
+                                                    I.hd, 0, row, &ctl->spanfull);
                                 else
-                                    tc::tma_load_3d(sm + OFF_ROT + jj * 1024 + ch * 512, &tmr, 0, I.hh, row,
+                                    tc::tma_load_3d(sm + OFF_ROT + jj * 1024 + ch * 512, &tmr, 0, I.hd, row,
                                                     &ctl->spanfull);
                             }
                         }
@@ -580,13 +583,16 @@ __global__ void __launch_bounds__(NTHR, 1)
             uint64_t* ptab = reinterpret_cast<uint64_t*>(sm + OFF_PTR) + ctid * 3;
             ptab[0] = (half == 0 && chunk_ok) ? reinterpret_cast<uint64_t>(B.dx + off_x(P, I.bb, n * FL, 0, I.hh) + pp)
                                               : 0ull;
+            // (with row groups, d_bhat / d_rot / d_da of group g go to slice g of their buffers)
             ptab[1] = (m < R && half_ok)
-                          ? reinterpret_cast<uint64_t>(B.db + off_b(P, I.bb, (2 * I.k + half) * FL, 0, I.hh) + m)
+                          ? reinterpret_cast<uint64_t>(B.db + I.grp * B.db_slice +
+                                                       off_b(P, I.bb, (2 * I.k + half) * FL, 0, I.hd) + m)
                           : 0ull;
             // d_rot: the warp of rows 0-31 of a chunk writes its partial sums into d_rot, the warp
-            // of rows 32-63 into drot2; k_drot_pair_sum adds the two afterwards
+            // of rows 32-63 into drot2; a second pass adds the two afterwards
             ptab[2] = (P.rw > 0 && chunk_ok && n < I.proc)
-                          ? reinterpret_cast<uint64_t>(((warp & 1) ? B.drot2 : B.drot) + off_rot(P, I.bb, n * FL, I.hh))
+                          ? reinterpret_cast<uint64_t>(((warp & 1) ? B.drot2 : B.drot) + I.grp * B.drot_slice +
+                                                       off_rot(P, I.bb, n * FL, I.hd))
                           : 0ull;
             // this warp's d_da partials for its chunk (the four warps of a chunk are summed in a
             // fixed order at the end of the item, so that d_da does not depend on timing)
@@ -595,8 +601,8 @@ __global__ void __launch_bounds__(NTHR, 1)
             // ---- item set-up: cumulative da of both chunks; D + D^T and d_m1 when (b,h) changes
             if (warp < 2) {
                 const int c2 = warp;
-                const float v0 = ida[(c2 * 64 + 2 * lane) * 4 + (I.hh & 3)];
-                const float v1 = ida[(c2 * 64 + 2 * lane + 1) * 4 + (I.hh & 3)];
+                const float v0 = ida[(c2 * 64 + 2 * lane) * 4 + (I.hd & 3)];
+                const float v1 = ida[(c2 * 64 + 2 * lane + 1) * 4 + (I.hd & 3)];
                 float s = v0 + v1;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -606,8 +612,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                 acum[c2 * 64 + 2 * lane + 1] = s;
                 acum[c2 * 64 + 2 * lane] = s - v1;
             }
-            if (ctl->loaded_b != I.bb || ctl->loaded_h != I.hh) {
-                const float* D = B.dm2 + ((int64_t)I.bb * P.h + I.hh) * R * R;
+            if (ctl->loaded_b != I.bb || ctl->loaded_h != I.hd) {
+                const float* D = B.dm2 + ((int64_t)I.bb * P.heads + I.hd) * R * R;
                 unsigned char* ds = sm + OFF_DS;
                 for (int i = ctid; i < 128 * 128 / 2; i += NCW * 32) {
                     const int r2 = i >> 6, r1 = (i & 63) * 2;
@@ -619,7 +625,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                     *reinterpret_cast<uint32_t*>(ds + tc::sw128_offset(128, r2, r1)) = tc::pack_bf16x2(a0, a1);
                 }
                 // d_m1 split into bf16 hi + lo rows of the K = 16 operand (rows 2..15 zero)
-                const float* dm1 = B.dm1 + ((int64_t)I.bb * P.h + I.hh) * R;
+                const float* dm1 = B.dm1 + ((int64_t)I.bb * P.heads + I.hd) * R;
                 for (int i = ctid; i < 16 * 128 / 2; i += NCW * 32) {
                     const int k = i >> 6, nn = (i & 63) * 2;
                     float v0 = 0.f, v1 = 0.f;
@@ -637,10 +643,10 @@ __global__ void __launch_bounds__(NTHR, 1)
             named_barrier_sync(1, NCW * 32);
             if (ctid == 0) {
                 ctl->loaded_b = I.bb;
-                ctl->loaded_h = I.hh;
+                ctl->loaded_h = I.hd;
             }
             const float* ac = acum + ch * 64;
-            auto e_of = [&](int t) -> float { return __expf(ida[(ch * 64 + t) * 4 + (I.hh & 3)]); };
+            auto e_of = [&](int t) -> float { return __expf(ida[(ch * 64 + t) * 4 + (I.hd & 3)]); };
 
             {
                 // ================================ phase A: forward sweep, anchors
@@ -986,7 +992,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&ctl->gfull);
                         if (rot_out) {  // the row address only now, so it is not held through the passes
-                            float* const drot_t = reinterpret_cast<float*>(ptab[2]) + (int64_t)t * P.h * P.rw;
+                            float* const drot_t = reinterpret_cast<float*>(ptab[2]) + (int64_t)t * P.heads * P.rw;
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
                                 if (dri[k] >= 0) drot_t[dri[k]] = drv[k];
@@ -1003,7 +1009,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         tc::tc_fence_before();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&ctl->dxfree);
-                        const int64_t hp = (int64_t)P.h * P.p, hr = (int64_t)P.h * P.r;
+                        const int64_t hp = (int64_t)P.h * P.p, hr = (int64_t)P.heads * P.r;
                         if (ptab[0]) {
                             __nv_bfloat16* px = reinterpret_cast<__nv_bfloat16*>(ptab[0]) + (int64_t)t * C * hp;
 #pragma unroll
@@ -1062,7 +1068,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const int T2 = c2 ? I.T[1] : I.T[0];
                 if (t < T2 && n2 < I.proc) {
                     const float* pq = reinterpret_cast<const float*>(sm + OFF_DDA) + (c2 * 64 + t) * 4;
-                    B.dda[off_da(P, I.bb, n2 * FL + t, I.hh)] = ((pq[0] + pq[1]) + pq[2]) + pq[3];
+                    B.dda[I.grp * B.dda_slice + off_da(P, I.bb, n2 * FL + t, I.hd)] = ((pq[0] + pq[1]) + pq[2]) + pq[3];
                 }
             }
             __syncwarp();
@@ -1088,7 +1094,7 @@ __global__ void __launch_bounds__(256) k_drot_pair_sum(const __grid_constant__ M
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n4) return;
     const int64_t row = i / (P.rw >> 2);  // (bb, t, hh)
-    const int64_t bt = row / P.h;
+    const int64_t bt = row / P.heads;
     const int bb = (int)(bt / P.s), t = (int)(bt - (int64_t)bb * P.s);
     if (t >= P.valid[bb]) return;
     float4 a = reinterpret_cast<float4*>(drot)[i];
@@ -1103,7 +1109,7 @@ __global__ void __launch_bounds__(256) k_drot_pair_sum(const __grid_constant__ M
 namespace fastk {
 
 size_t bwd_anchor_bytes() { return (size_t)kMaxBwdGrid * fastbwd::NANCHOR * 128 * 128 * sizeof(float); }
-size_t bwd_drot2_bytes(const MMParams& P) { return (size_t)P.b * P.s * P.h * P.rw * sizeof(float); }
+size_t bwd_drot2_bytes(const MMParams& P) { return (size_t)P.b * P.s * P.heads * P.rw * sizeof(float); }
 
 cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, float* drot2, const float* dm2, const float* dm1,
                           void* dx, void* db, float* dda, float* drot, const TensorMaps& maps, int grid, cudaStream_t st) {
@@ -1119,6 +1125,11 @@ cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, float* d
     a.dda = dda;
     a.drot = drot;
     a.drot2 = drot2;
+    const int64_t ntok = (int64_t)fa.P.b * fa.P.s;
+    const bool grouped = fa.P.groups > 1;
+    a.db_slice = grouped ? ntok * fa.P.C * fa.P.heads * fa.P.r : 0;
+    a.dda_slice = grouped ? ntok * fa.P.heads : 0;
+    a.drot_slice = grouped ? ntok * fa.P.heads * fa.P.rw : 0;
     // channel slots per chunk in the span tiles: 4 when C <= 4, else 8
     decltype(&tc_bwd_kernel<ROT_NONE, 0, 2>) kern;
     const bool c8 = fa.P.C > 4;
@@ -1137,7 +1148,9 @@ cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, float* d
     kern<<<grid, NTHR, SMEM_BYTES, st>>>(a, maps.x, maps.b, maps.rot, maps.da64);
     mm_prof_mark(KID_FAST_BWD, 0, st);
     if ((e = cudaGetLastError()) != cudaSuccess || fa.P.rw == 0) return e;
-    const int64_t n4 = (int64_t)fa.P.b * fa.P.s * fa.P.h * (fa.P.rw >> 2);
+    // with row groups the per-group slices are summed by the caller instead
+    if (fa.P.groups > 1) return e;
+    const int64_t n4 = (int64_t)fa.P.b * fa.P.s * fa.P.heads * (fa.P.rw >> 2);
     mm_prof_mark(KID_DROT_SUM, 1, st);
     k_drot_pair_sum<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(fa.P, drot, drot2, n4);
     mm_prof_mark(KID_DROT_SUM, 0, st);

@@ -16,7 +16,7 @@ struct FastArgs {
     MMParams P;     // internal chunking: l = 64, nc = s / 64
     int layoutB;    // 1: half-split rotation with r = 64 (partner columns 32 apart)
     int items;      // work items (chunk pairs) of the whole problem
-    float* Hc;      // [b,h,nc,p,r] chunk carries / chunk-end states
+    float* Hc;      // [b,h,nc,p,r] chunk carries / chunk-end states (h, p: the 64-row groups as heads)
     float* Dn;      // [b,h,nc] chunk decays
     float* m2;
     float* m1;
@@ -47,6 +47,7 @@ __host__ inline int count_items(const MMParams& P) {
 
 struct Item {
     int bb, hh, k;   // batch row, head, pair index (chunks 2k and 2k+1)
+    int hd, grp;     // the caller's head and the 64-row group of hh (MMParams::groups)
     int proc;        // processed chunks of the row
     int T[2];        // valid tokens of both chunks (T[0] >= T[1])
     bool exists[2];  // chunk inside the sequence
@@ -79,6 +80,8 @@ __device__ inline Item decode_item(const FastArgs& A, int item) {
     const MMParams& P = A.P;
     Item I;
     locate(A, item, I.bb, I.hh, I.k);
+    I.hd = I.hh / P.groups;
+    I.grp = I.hh - I.hd * P.groups;
     I.proc = mm_processed(P, I.bb);
     for (int ch = 0; ch < 2; ++ch) {
         const int n = 2 * I.k + ch;
@@ -132,7 +135,7 @@ struct TokenWalk {
 
 // da comes by tensor copies of 4-head groups when a row of da ([b*s, h] fp32) is a multiple of 16
 // bytes long, else by plain loads of the one head into the same shared-memory positions.
-__host__ __device__ inline bool da_by_tma(const MMParams& P) { return (P.h & 3) == 0; }
+__host__ __device__ inline bool da_by_tma(const MMParams& P) { return (P.heads & 3) == 0; }
 
 // Tokens per stage of the correction kernel: their (token, channel) rows fill at most the 128
 // lanes of one tensor-core tile.

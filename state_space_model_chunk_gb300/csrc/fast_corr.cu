@@ -68,6 +68,7 @@ constexpr uint32_t TM_BUF = 256;  // per accumulator buffer: U at +0 (64 columns
 
 struct CItem {
     int bb, hh, n;
+    int hd, grp;  // the caller's head and the 64-row group of hh (MMParams::groups)
 };
 
 __host__ __device__ inline int count_corr(const MMParams& P) {
@@ -95,6 +96,8 @@ __device__ inline CItem decode(const MMParams& P, int item) {
     I.bb = bb;
     I.hh = rem / per;
     I.n = rem - I.hh * per;
+    I.hd = I.hh / P.groups;
+    I.grp = I.hh - I.hd * P.groups;
     return I;
 }
 
@@ -111,7 +114,7 @@ struct CorrArgs {
     const float* E;    // [b,h,nc,p,r] dH(n+1) per chunk
     __nv_bfloat16* dx;
     __nv_bfloat16* db;
-    float* dda;
+    float* dda;        // with row groups: one [b,s,h] slice per group, summed afterwards
 };
 
 __global__ void __launch_bounds__(NTHR, 1)
@@ -167,14 +170,16 @@ __global__ void __launch_bounds__(NTHR, 1)
         if (lane == 0) {
             uint32_t q = 0;
             bool ok = true;
-            int srow[NS] = {0, 0}, shh[NS] = {0, 0};  // global row and head of the stage each slot holds
+            // global row and head of the stage each slot holds, and the d_bhat row and head (with
+            // row groups d_bhat goes to one [b*s] slice per group: the map's rows are group-major)
+            int srow[NS] = {0, 0}, shh[NS] = {0, 0}, sbrow[NS] = {0, 0}, shd[NS] = {0, 0};
             auto store_back = [&](uint32_t qq) -> bool {
                 const uint32_t s = qq % NS;
                 if (!tc::mbar_wait(&ctl->upd[s], (qq / NS) & 1, abort)) return false;
                 unsigned char* stg = sm + s * STAGE;
                 tc::tma_store_4d(&tmdx32, 0, shh[s], 0, srow[s], stg + SL_DX * SLOT);
                 for (int a = 0; a < (R + 63) / 64; ++a)
-                    tc::tma_store_4d(&tmdb32, 64 * a, shh[s], 0, srow[s], stg + (SL_DB + a) * SLOT);
+                    tc::tma_store_4d(&tmdb32, 64 * a, shd[s], 0, sbrow[s], stg + (SL_DB + a) * SLOT);
                 tc::bulk_commit();
                 tc::bulk_wait_read0();
                 return true;
@@ -187,14 +192,17 @@ __global__ void __launch_bounds__(NTHR, 1)
                     unsigned char* stg = sm + s * STAGE;
                     tc::mbar_arrive_expect_tx(&ctl->full[s], 2u * rows * 128u * (1u + (uint32_t)(R + 63) / 64u));
                     const int row = I.bb * P.s + I.n * FL + st * TPS;
+                    const int brow = I.grp * P.b * P.s + row;
                     tc::tma_load_4d(stg, &tmx32, 0, I.hh, 0, row, &ctl->full[s]);
                     tc::tma_load_4d(stg + SL_DX * SLOT, &tmdx32, 0, I.hh, 0, row, &ctl->full[s]);
                     for (int a = 0; a < (R + 63) / 64; ++a) {
-                        tc::tma_load_4d(stg + (1 + a) * SLOT, &tmb32, 64 * a, I.hh, 0, row, &ctl->full[s]);
-                        tc::tma_load_4d(stg + (SL_DB + a) * SLOT, &tmdb32, 64 * a, I.hh, 0, row, &ctl->full[s]);
+                        tc::tma_load_4d(stg + (1 + a) * SLOT, &tmb32, 64 * a, I.hd, 0, row, &ctl->full[s]);
+                        tc::tma_load_4d(stg + (SL_DB + a) * SLOT, &tmdb32, 64 * a, I.hd, 0, brow, &ctl->full[s]);
                     }
                     srow[s] = row;
                     shh[s] = I.hh;
+                    sbrow[s] = brow;
+                    shd[s] = I.hd;
                 }
             }
             // the last stages go out too
@@ -375,7 +383,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const float base = misc[2 * NBW + ib] * (misc[NBW * ib] + misc[NBW * ib + 1]);
                 float pre = 0.f;
                 for (int j = 0; j < etid; ++j) pre = fmaf(sc[j], om[j], pre);
-                B.dda[off_da(P, I.bb, I.n * FL + etid, I.hh)] += base + pre;
+                B.dda[(int64_t)I.grp * P.b * P.s * P.heads + off_da(P, I.bb, I.n * FL + etid, I.hd)] += base + pre;
             }
             named_barrier_sync(1, NEW * 32);  // sc / D_n / omega / dot read: free for the next items
             if (etid == 0) tc::mbar_arrive(&ctl->scfree[ib]);
@@ -399,8 +407,8 @@ __global__ void __launch_bounds__(NTHR, 1)
             if (bw == 0) {  // all 64 tokens of the chunk are valid
                 float* sc = reinterpret_cast<float*>(sm + OFF_SC) + ib * 64;
                 const int t0 = 2 * lane, t1 = t0 + 1;
-                const float v0 = B.da[off_da(P, I.bb, I.n * FL + t0, I.hh)];
-                const float v1 = B.da[off_da(P, I.bb, I.n * FL + t1, I.hh)];
+                const float v0 = B.da[off_da(P, I.bb, I.n * FL + t0, I.hd)];
+                const float v1 = B.da[off_da(P, I.bb, I.n * FL + t1, I.hd)];
                 float sum = v0 + v1;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {

@@ -52,6 +52,7 @@ static_assert(sizeof(Ctl) <= 256, "control block");
 
 struct EItem {
     int bb, hh, n, T, proc;
+    int hd;  // the caller's head (hh is a 64-row group of it, MMParams::groups)
 };
 
 __host__ __device__ inline int count_chunks(const MMParams& P) {
@@ -75,6 +76,7 @@ __device__ inline EItem decode(const MMParams& P, int item) {
     const int pr = I.proc > 0 ? I.proc : 1;
     I.hh = rem / pr;
     I.n = rem - I.hh * pr;
+    I.hd = I.hh / P.groups;
     I.T = mm_chunk_rows(P, bb, I.n);
     return I;
 }
@@ -144,8 +146,8 @@ __global__ void __launch_bounds__(NTHR, 2)
                         // this head's da of the chunk, into the positions the 4-head copy would fill,
                         // before the arrival that publishes the stage
                         float* dst = reinterpret_cast<float*>(stg + 3 * SLOT);
-                        const float* src = A.da + ((int64_t)I.bb * P.s + I.n * FL) * P.h + I.hh;
-                        for (int t = 0; t < I.T; ++t) dst[t * 4 + (I.hh & 3)] = src[(int64_t)t * P.h];
+                        const float* src = A.da + ((int64_t)I.bb * P.s + I.n * FL) * P.heads + I.hd;
+                        for (int t = 0; t < I.T; ++t) dst[t * 4 + (I.hd & 3)] = src[(int64_t)t * P.heads];
                     }
                     const uint32_t bytes =
                         rows * 128u * (1u + (uint32_t)(R + 63) / 64u) + ((st == 0 && da_by_tma(P)) ? 1024u : 0u);
@@ -153,9 +155,9 @@ __global__ void __launch_bounds__(NTHR, 2)
                     const int row = I.bb * P.s + I.n * FL + st * TPS;
                     tc::tma_load_4d(stg, &tmx8, 0, I.hh, 0, row, &ctl->full[s]);
                     for (int a = 0; a < (R + 63) / 64; ++a)
-                        tc::tma_load_4d(stg + (1 + a) * SLOT, &tmb8, 64 * a, I.hh, 0, row, &ctl->full[s]);
+                        tc::tma_load_4d(stg + (1 + a) * SLOT, &tmb8, 64 * a, I.hd, 0, row, &ctl->full[s]);
                     if (st == 0 && da_by_tma(P))
-                        tc::tma_load_2d(stg + 3 * SLOT, &tmd64, I.hh & ~3, I.bb * P.s + I.n * FL, &ctl->full[s]);
+                        tc::tma_load_2d(stg + 3 * SLOT, &tmd64, I.hd & ~3, I.bb * P.s + I.n * FL, &ctl->full[s]);
                 }
             }
             if (!ok) fail(ctl, A.err, 31);
@@ -224,8 +226,8 @@ __global__ void __launch_bounds__(NTHR, 2)
                     // decay weights of the chunk: inclusive cumulative sum of da by a warp scan
                     const float* da = reinterpret_cast<const float*>(stg + 3 * SLOT);
                     const int t0 = 2 * lane, t1 = t0 + 1;
-                    const float v0 = t0 < I.T ? da[t0 * 4 + (I.hh & 3)] : 0.f;
-                    const float v1 = t1 < I.T ? da[t1 * 4 + (I.hh & 3)] : 0.f;
+                    const float v0 = t0 < I.T ? da[t0 * 4 + (I.hd & 3)] : 0.f;
+                    const float v1 = t1 < I.T ? da[t1 * 4 + (I.hd & 3)] : 0.f;
                     float sum = v0 + v1;
 #pragma unroll
                     for (int off = 1; off < 32; off <<= 1) {

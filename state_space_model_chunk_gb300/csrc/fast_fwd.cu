@@ -1,5 +1,5 @@
-// fast_fwd.cu -- tcgen05 / TMA forward of the state-moments operator (bf16 operands, p = 64,
-// r in {64, 128}, C <= 8).
+// fast_fwd.cu -- tcgen05 / TMA forward of the state-moments operator (bf16 operands, 64 state
+// rows per head -- larger p as 64-row groups run as heads --, r up to 128, C <= 8).
 //
 // One persistent CTA per SM walks a contiguous range of work items; an item is a pair of
 // 64-token chunks of one (batch row, head).  The two chunks share the 128 TMEM lanes:
@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                     // stored before the arrival that publishes the stage
                     if (lane < 2 && I.exists[lane]) {
                         const int row = I.bb * P.s + (2 * I.k + lane) * FL + t;
-                        reinterpret_cast<float*>(sm + OFF_DA + s * 256 + lane * 128)[I.hh & 3] =
-                            A.da[(int64_t)row * P.h + I.hh];
+                        reinterpret_cast<float*>(sm + OFF_DA + s * 256 + lane * 128)[I.hd & 3] =
+                            A.da[(int64_t)row * P.heads + I.hd];
                     }
                     __syncwarp();
                 }
@@ -171,11 +171,11 @@ __global__ void __launch_bounds__(NTHR, 1)
                             tc::tma_load_4d(sm + OFF_X + s * 4096 + ch * 3072, &tmx, 0, I.hh, 0, row, &ctl->full[s]);
                         else if (kind < nbx)
                             tc::tma_load_4d(sm + OFF_B + s * 4096 + (kind - 1) * 2048 + ch * 1024, &tmb, 64 * (kind - 1),
-                                            I.hh, 0, row, &ctl->full[s]);
+                                            I.hd, 0, row, &ctl->full[s]);
                         else if (P.rw && kind == nbx)
-                            tc::tma_load_3d(sm + OFF_ROT + s * 1024 + ch * 512, &tmr, 0, I.hh, row, &ctl->full[s]);
+                            tc::tma_load_3d(sm + OFF_ROT + s * 1024 + ch * 512, &tmr, 0, I.hd, row, &ctl->full[s]);
                         else if (DAT)
-                            tc::tma_load_2d(sm + OFF_DA + s * 256 + ch * 128, &tmd, I.hh & ~3, row, &ctl->full[s]);
+                            tc::tma_load_2d(sm + OFF_DA + s * 256 + ch * 128, &tmd, I.hd & ~3, row, &ctl->full[s]);
                     }
                 }
             }
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const uint32_t s = q % NS, u = q / NS;
                 check(tc::mbar_wait(&ctl->full[s], u & 1, abort));
                 const bool live = t < Tch;
-                const float et = live ? __expf(reinterpret_cast<const float*>(sm + OFF_DA + s * 256 + ch * 128)[I.hh & 3])
+                const float et = live ? __expf(reinterpret_cast<const float*>(sm + OFF_DA + s * 256 + ch * 128)[I.hd & 3])
                                       : 1.f;
                 const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + s * 1024 + ch * 512);
                 if (ROTK == ROT_PAIRWISE || ROTK == ROT_HALF) {

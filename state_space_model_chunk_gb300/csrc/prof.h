@@ -18,6 +18,7 @@ enum MMKernelId {
     KID_M2_REDUCE,
     KID_DROT_SUM,
     KID_ROT_STEPS,
+    KID_GROUP_SUM,
     KID_COUNT
 };
 

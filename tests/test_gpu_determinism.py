@@ -18,6 +18,8 @@ CASES = [
     WORKLOADS["quat_s2048"],  # 1024 chunk pairs on 152 CTAs: every (b,h) spread over several CTAs
     WORKLOADS["ragged_s16384"].scaled(name="ragged_det", b=3, s=2048, h=4),
     WORKLOADS["large_s4096"].scaled(name="large_det", b=2, s=512, h=8, valid="fixed:450"),
+    # two 64-row groups per head: their slices are summed in group order
+    WORKLOADS["large_s4096"].scaled(name="p128_det", b=2, s=512, h=4, p=128, valid="fixed:450"),
 ]
 
 

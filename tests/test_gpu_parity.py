@@ -26,7 +26,8 @@ def expected_fast(w, backward):
     """Whether the tensor-core kernels implement this workload (else the SIMT kernels run)."""
     rw = w.rope_dim // 2 if w.rot in ("pairwise", "half") else (4 * w.quat_blocks if w.rot == "quat" else 0)
     r_ok = w.r in (64, 128) if w.rot == "half" else (w.r % 16 == 0 and 16 <= w.r <= 128)
-    return (w.dtype == "bf16" and w.p == 64 and r_ok and 1 <= w.C <= 8 and w.s % 64 == 0
+    p_ok = w.p % 64 == 0 and 64 <= w.p <= 512
+    return (w.dtype == "bf16" and p_ok and r_ok and 1 <= w.C <= 8 and w.s % 64 == 0
             and rw % 4 == 0 and rw <= 128)
 
 
@@ -90,6 +91,14 @@ SMALL = [
     WORKLOADS["large_s4096"].scaled(name="pairwise_c8", b=1, s=256, h=4, C=8, valid="fixed:241"),
     WORKLOADS["quat_s2048"].scaled(name="quat_c5", b=2, s=192, h=2, C=5),
     WORKLOADS["halfsplit_s1024"].scaled(name="half_r64_c7", b=1, s=320, h=3, C=7),
+    # p above 64 on the tensor cores: each head's state rows run as groups of 64, whose moments
+    # and d_bhat / d_da / d_rot are summed afterwards
+    WORKLOADS["large_s4096"].scaled(name="pairwise_p128_h3", b=2, s=192, h=3, p=128, valid="fixed:150"),
+    WORKLOADS["quat_s2048"].scaled(name="quat_p128_h4", b=1, s=256, h=4, p=128, quat_blocks=20),
+    WORKLOADS["halfsplit_s1024"].scaled(name="half_p192_r64", b=2, s=128, h=2, p=192, C=2),
+    WORKLOADS["large_s4096"].scaled(name="norot_p256_r32", b=1, s=128, h=2, p=256, r=32, rot="none", rope_dim=0),
+    WORKLOADS["ragged_s16384"].scaled(name="ragged_p128_c5", b=3, s=256, h=2, p=128, C=5, r=80, rot="pairwise",
+                                      rope_dim=48, chunk_len=64),
 ]
 
 
@@ -145,8 +154,10 @@ def test_parity_steep_decay_spans():
 
 
 @pytest.mark.parametrize("w", [SMALL[3], SMALL[0],
-                               WORKLOADS["large_s4096"].scaled(name="tc_c6", b=1, s=128, h=4, C=6)],
-                         ids=["tensor_core", "simt", "tensor_core_c6"])
+                               WORKLOADS["large_s4096"].scaled(name="tc_c6", b=1, s=128, h=4, C=6),
+                               WORKLOADS["large_s4096"].scaled(name="tc_p128", b=2, s=192, h=2, p=128,
+                                                               valid="fixed:130")],
+                         ids=["tensor_core", "simt", "tensor_core_c6", "tensor_core_p128"])
 def test_backward_reusing_forward_carries(w):
     """MM_FLAG_REUSE_CARRIES: forward then backward on one workspace gives the gradients of a
     backward that recomputes the carries (on the tensor-core path with four and six channels, and on
