@@ -80,6 +80,7 @@ struct Ctl {
     uint32_t tbase;
     int abort;
     int loaded_b, loaded_h;
+    float* dda_row[2];  // d_da of the item's two chunks at token 0 (the row stride is the head count)
 };
 static_assert(sizeof(Ctl) <= 512, "control block");
 
@@ -601,8 +602,13 @@ __global__ void __launch_bounds__(NTHR, 1)
             // ---- item set-up: cumulative da of both chunks; D + D^T and d_m1 when (b,h) changes
             if (warp < 2) {
                 const int c2 = warp;
+                float* const idw = reinterpret_cast<float*>(sm + OFF_IDA);
                 const float v0 = ida[(c2 * 64 + 2 * lane) * 4 + (I.hd & 3)];
                 const float v1 = ida[(c2 * 64 + 2 * lane + 1) * 4 + (I.hd & 3)];
+                // this head's da into slot 0 of each token's 4-head group, so that the token steps
+                // read it without the head index (each lane rewrites only its own two tokens)
+                idw[(c2 * 64 + 2 * lane) * 4] = v0;
+                idw[(c2 * 64 + 2 * lane + 1) * 4] = v1;
                 float s = v0 + v1;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -644,9 +650,11 @@ __global__ void __launch_bounds__(NTHR, 1)
             if (ctid == 0) {
                 ctl->loaded_b = I.bb;
                 ctl->loaded_h = I.hd;
+                for (int c2 = 0; c2 < 2; ++c2)
+                    ctl->dda_row[c2] = B.dda + I.grp * B.dda_slice + off_da(P, I.bb, (2 * I.k + c2) * FL, I.hd);
             }
             const float* ac = acum + ch * 64;
-            auto e_of = [&](int t) -> float { return __expf(ida[(ch * 64 + t) * 4 + (I.hd & 3)]); };
+            auto e_of = [&](int t) -> float { return __expf(ida[(ch * 64 + t) * 4]); };
 
             {
                 // ================================ phase A: forward sweep, anchors
@@ -1068,7 +1076,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const int T2 = c2 ? I.T[1] : I.T[0];
                 if (t < T2 && n2 < I.proc) {
                     const float* pq = reinterpret_cast<const float*>(sm + OFF_DDA) + (c2 * 64 + t) * 4;
-                    B.dda[I.grp * B.dda_slice + off_da(P, I.bb, n2 * FL + t, I.hd)] = ((pq[0] + pq[1]) + pq[2]) + pq[3];
+                    ctl->dda_row[c2][(int64_t)t * P.heads] = ((pq[0] + pq[1]) + pq[2]) + pq[3];
                 }
             }
             __syncwarp();

@@ -416,9 +416,12 @@ __global__ void __launch_bounds__(NTHR, 1)
                 check(tc::mbar_wait(&ctl->segdone, seg & 1, abort));
                 tc::tc_fence_after();
                 const bool whole = seg_k0 == 0 && I.k == pairs_of(P, I.bb) - 1;
-                float* M2 = whole ? A.m2 + ((int64_t)I.bb * P.h + I.hh) * P.r * P.r
+                // the item's head again (the token steps use only the caller's head, I.hd)
+                int fb, fh, fk;
+                locate(A, it, fb, fh, fk);
+                float* M2 = whole ? A.m2 + ((int64_t)fb * P.h + fh) * P.r * P.r
                                   : A.m2p + (int64_t)(2 * blockIdx.x + (seg_it0 == it0 ? 0 : 1)) * (P.r * P.r + P.r);
-                float* M1 = whole ? A.m1 + ((int64_t)I.bb * P.h + I.hh) * P.r : M2 + P.r * P.r;
+                float* M1 = whole ? A.m1 + ((int64_t)fb * P.h + fh) * P.r : M2 + P.r * P.r;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     float v[16];

@@ -14,6 +14,8 @@ pytestmark = pytest.mark.gpu
 MM_OK, MM_ERR_NONFINITE = 0, 5
 
 CASES = [WORKLOADS["large_s4096"].scaled(name="finite_tc", b=2, s=256, h=4, C=2),  # tensor-core kernels
+         # tensor-core kernels with two 64-row groups per head (outputs summed from group slices)
+         WORKLOADS["large_s4096"].scaled(name="finite_tc_p128", b=1, s=128, h=2, C=2, p=128),
          WORKLOADS["tiny_fp32"]]                                                       # SIMT kernels
 
 

@@ -29,6 +29,10 @@ CASES = [
     (WORKLOADS["tiny_fp32"].scaled(name="steps_partial_chunk", b=2, s=80, h=3, valid="fixed:71"), False),
     (WORKLOADS["tiny_fp32"].scaled(name="steps_quat_partial", b=1, s=80, h=2, rot="quat", rope_dim=0,
                                    quat_blocks=3, valid="fixed:80"), False),
+    # two 64-row groups per head on the tensor cores
+    (WORKLOADS["quat_s2048"].scaled(name="steps_quat_p128", b=2, s=192, h=2, p=128, quat_blocks=12,
+                                    valid="ragged"), False),
+    (WORKLOADS["large_s4096"].scaled(name="steps_pairwise_p192", b=1, s=256, h=3, p=192, C=2), False),
     # nothing valid: every output and gradient is zero
     (WORKLOADS["large_s4096"].scaled(name="steps_none_valid", b=1, s=128, h=4, valid="fixed:0"), False),
 ]

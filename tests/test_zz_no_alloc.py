@@ -32,6 +32,8 @@ CASES = [
     WORKLOADS["tiny_fp32"],                                                  # SIMT kernels
     WORKLOADS["large_s4096"].scaled(name="noalloc_tc", b=2, s=256, h=4, valid="fixed:200"),  # tensor-core kernels
     WORKLOADS["halfsplit_s1024"],
+    # two 64-row groups per head: the groups' moments go through the array too
+    WORKLOADS["quat_s2048"].scaled(name="noalloc_p128", b=2, s=256, h=2, p=128, valid="fixed:190"),
 ]
 # run through the array between the two compared calls: other shapes, values and valid lengths
 OTHER = WORKLOADS["quat_s2048"].scaled(name="noalloc_other", b=2, s=512, h=4, valid="fixed:333", seed=17)
