@@ -370,7 +370,7 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     }
     if (grid > kMaxBwdGrid) grid = kMaxBwdGrid;
     float* anchors = reinterpret_cast<float*>(scratch);
-    if ((e = launch_tc_bwd(fa, A.E, anchors, drot2, A.dm2, A.dm1, A.dxhat, db, dda, drot, maps, grid, st)) !=
+    if ((e = launch_tc_bwd(fa, A.E, anchors, drot2, A.dm2, A.dm1, A.dxhat, db, dda, drot, A.rot, maps, grid, st)) !=
         cudaSuccess)
         return e;
     if ((e = generic_cot_scan(P, A.E, A.Dn, A.dinit, st)) != cudaSuccess) return e;
@@ -380,6 +380,6 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     // partials, then the G rows-32-63 ones)
     if ((e = group_sum_bf16(db, A.dbhat, G, (int64_t)nb, st)) != cudaSuccess) return e;
     if ((e = group_sum_f32(dda, A.dda, 1, G, (int64_t)nda, st)) != cudaSuccess) return e;
-    if (P.rw) return group_sum_f32(drot, A.drot, 1, 2 * G, (int64_t)nrot, st);
-    return cudaSuccess;
+    if (P.rw && (e = group_sum_f32(drot, A.drot, 1, 2 * G, (int64_t)nrot, st)) != cudaSuccess) return e;
+    return launch_drot_finish(P, A.drot, nullptr, A.rot, st);  // quaternions: the factor Q / |Q|^2
 }

@@ -945,7 +945,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     if (lane < 16 && ang < P.na && rot_out) { drv[pass] = v[0]; dri[pass] = ang; }
                                 }
                             } else if (ROTK == ROT_QUAT) {
-                                // sum_p d_c (x) conj(c) per 4-block, then (.) (x) Q / |Q|^2
+                                // sum_p d_c (x) conj(c) per 4-block; the factor (.) (x) Q / |Q|^2, linear,
+                                // is applied once the two row halves' partial sums are added
 #pragma unroll
                                 for (int sl = 0; sl < 2; ++sl) {
                                     if (!(sl ? act_b : act_a)) continue;
@@ -963,20 +964,10 @@ __global__ void __launch_bounds__(NTHR, 1)
                                     }
                                     transpose_reduce16(v, lane);
                                     // lanes 4i..4i+3 (i < 4) hold the 4 components of block i
-                                    const int l0 = lane & ~3, comp = lane & 3;
-                                    const float s0q = __shfl_sync(0xffffffffu, v[0], l0);
-                                    const float s1q = __shfl_sync(0xffffffffu, v[0], l0 + 1);
-                                    const float s2q = __shfl_sync(0xffffffffu, v[0], l0 + 2);
-                                    const float s3q = __shfl_sync(0xffffffffu, v[0], l0 + 3);
                                     const int blk = 4 * G[gsl] + ((lane >> 2) & 3);
                                     if (lane < 16 && blk < P.J && rot_out) {
-                                        const float* Q = qt + 4 * blk;
-                                        float o0, o1, o2, o3;
-                                        hamilton(s0q, s1q, s2q, s3q, Q[0], Q[1], Q[2], Q[3], o0, o1, o2, o3);
-                                        const float inv = 1.f / (Q[0] * Q[0] + Q[1] * Q[1] + Q[2] * Q[2] + Q[3] * Q[3]);
-                                        const float val = comp == 0 ? o0 : comp == 1 ? o1 : comp == 2 ? o2 : o3;
-                                        drv[2 * pass + sl] = inv * val;
-                                        dri[2 * pass + sl] = 4 * blk + comp;
+                                        drv[2 * pass + sl] = v[0];
+                                        dri[2 * pass + sl] = 4 * blk + (lane & 3);
                                     }
                                 }
                             }
@@ -1096,9 +1087,12 @@ __global__ void __launch_bounds__(NTHR, 1)
 // d_rot = (sum over rows 0-31) + (sum over rows 32-63) of every valid token, in that order: the
 // two row warps of a chunk store their partial sums with plain stores, one into d_rot and one into
 // the workspace, and this pass adds them (no atomics, and a result that does not depend on
-// timing).  One float4 per thread; rows past valid_len keep the zeros the host wrote.
-__global__ void __launch_bounds__(256) k_drot_pair_sum(const __grid_constant__ MMParams P, float* __restrict__ drot,
-                                                       const float* __restrict__ drot2, int64_t n4) {
+// timing); drot2 null: d_rot already holds the sum.  Quaternions (rot not null): the summed
+// sum_p d_c (x) conj(c) of each block times Q / |Q|^2, Q the block's cumulative quaternion.  One
+// float4 (a quaternion block) per thread; rows past valid_len keep the zeros the host wrote.
+__global__ void __launch_bounds__(256) k_drot_finish(const __grid_constant__ MMParams P, float* __restrict__ drot,
+                                                     const float* __restrict__ drot2, const float* __restrict__ rot,
+                                                     int64_t n4) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n4) return;
     const int64_t row = i / (P.rw >> 2);  // (bb, t, hh)
@@ -1106,8 +1100,17 @@ __global__ void __launch_bounds__(256) k_drot_pair_sum(const __grid_constant__ M
     const int bb = (int)(bt / P.s), t = (int)(bt - (int64_t)bb * P.s);
     if (t >= P.valid[bb]) return;
     float4 a = reinterpret_cast<float4*>(drot)[i];
-    const float4 c = reinterpret_cast<const float4*>(drot2)[i];
-    a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+    if (drot2) {
+        const float4 c = reinterpret_cast<const float4*>(drot2)[i];
+        a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+    }
+    if (rot) {
+        const float4 q = reinterpret_cast<const float4*>(rot)[i];
+        float o0, o1, o2, o3;
+        hamilton(a.x, a.y, a.z, a.w, q.x, q.y, q.z, q.w, o0, o1, o2, o3);
+        const float inv = 1.f / (q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w);
+        a = make_float4(inv * o0, inv * o1, inv * o2, inv * o3);
+    }
     reinterpret_cast<float4*>(drot)[i] = a;
 }
 
@@ -1120,7 +1123,8 @@ size_t bwd_anchor_bytes() { return (size_t)kMaxBwdGrid * fastbwd::NANCHOR * 128 
 size_t bwd_drot2_bytes(const MMParams& P) { return (size_t)P.b * P.s * P.heads * P.rw * sizeof(float); }
 
 cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, float* drot2, const float* dm2, const float* dm1,
-                          void* dx, void* db, float* dda, float* drot, const TensorMaps& maps, int grid, cudaStream_t st) {
+                          void* dx, void* db, float* dda, float* drot, const float* rot, const TensorMaps& maps, int grid,
+                          cudaStream_t st) {
     using namespace fastbwd;
     BwdArgs a;
     a.F = fa;
@@ -1156,11 +1160,17 @@ cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, float* d
     kern<<<grid, NTHR, SMEM_BYTES, st>>>(a, maps.x, maps.b, maps.rot, maps.da64);
     mm_prof_mark(KID_FAST_BWD, 0, st);
     if ((e = cudaGetLastError()) != cudaSuccess || fa.P.rw == 0) return e;
-    // with row groups the per-group slices are summed by the caller instead
+    // with row groups the per-group slices are summed by the caller, which then finishes d_rot
     if (fa.P.groups > 1) return e;
-    const int64_t n4 = (int64_t)fa.P.b * fa.P.s * fa.P.heads * (fa.P.rw >> 2);
+    return launch_drot_finish(fa.P, drot, drot2, rot, st);
+}
+
+cudaError_t launch_drot_finish(const MMParams& P, float* drot, const float* drot2, const float* rot, cudaStream_t st) {
+    using namespace fastbwd;
+    if (P.rw == 0 || (!drot2 && P.rot != ROT_QUAT)) return cudaSuccess;
+    const int64_t n4 = (int64_t)P.b * P.s * P.heads * (P.rw >> 2);
     mm_prof_mark(KID_DROT_SUM, 1, st);
-    k_drot_pair_sum<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(fa.P, drot, drot2, n4);
+    k_drot_finish<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(P, drot, drot2, P.rot == ROT_QUAT ? rot : nullptr, n4);
     mm_prof_mark(KID_DROT_SUM, 0, st);
     return cudaGetLastError();
 }

@@ -234,7 +234,12 @@ cudaError_t launch_tc_corr(const FastArgs& fa, const float* da, const float* E, 
 size_t bwd_anchor_bytes();
 size_t bwd_drot2_bytes(const MMParams& P);  // the backward's second d_rot partial, [b,s,h,rw] fp32
 size_t fwd_partial_bytes(const MMParams& P);  // internal chunking (nc = s / 64)
+// rot: the cumulative rotation (quaternions: d_rot is finished with each block's Q / |Q|^2)
 cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, float* drot2, const float* dm2, const float* dm1,
-                          void* dx, void* db, float* dda, float* drot, const TensorMaps& maps, int grid, cudaStream_t st);
+                          void* dx, void* db, float* dda, float* drot, const float* rot, const TensorMaps& maps, int grid,
+                          cudaStream_t st);
+// d_rot from the backward's partial sums: drot += drot2 (drot2 may be null), then for quaternions
+// the factor Q / |Q|^2 of each block; positions past valid_len stay as they are
+cudaError_t launch_drot_finish(const MMParams& P, float* drot, const float* drot2, const float* rot, cudaStream_t st);
 
 }  // namespace fastk
