@@ -422,13 +422,17 @@ def run_ours(args):
 
         run_steps(2)
         torch.cuda.synchronize()
-        # one step's host-to-device copy on its own (not part of the figure: what the fill costs)
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c0.record(cstream)
-        issue_copy(0)
-        c1.record(cstream)
-        torch.cuda.synchronize()
-        copy_ms = c0.elapsed_time(c1)
+        # one step's host-to-device copy on its own (not part of the figure: what the fill costs),
+        # the median of three
+        samples = []
+        for _ in range(3):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(cstream)
+            issue_copy(0)
+            c1.record(cstream)
+            torch.cuda.synchronize()
+            samples.append(c0.elapsed_time(c1))
+        copy_ms = sorted(samples)[1]
         if dist:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
