@@ -854,9 +854,10 @@ __global__ void __launch_bounds__(NTHR, 1)
                             tc::mbar_arrive(&ctl->pfree);
                             tc::mbar_arrive(&ctl->cfull);
                         }
-                        // d_da_{t+1} = e_{t+1} <g_{t+1}, h_t>  (g holds g_{t+1} here)
+                        // d_da_{t+1} = e_{t+1} <g_{t+1}, h_t>  (g holds g_{t+1} here, and e_next
+                        // e_{t+1}: step_g of token t+1 ran last, in this span or the one after it)
                         const float dot = warp_sum((dotv[0] + dotv[1]) + (dotv[2] + dotv[3]));
-                        if (lane == 0 && t + 1 < I.T[0]) ddap[(t + 1) * 4] = e_of(t + 1) * dot;
+                        if (lane == 0 && t + 1 < I.T[0]) ddap[(t + 1) * 4] = e_next * dot;
                     };
                     // ---- d_c -> d_rot, G, cotangent recurrence -> g tile
                     auto step_g = [&](int t) {
