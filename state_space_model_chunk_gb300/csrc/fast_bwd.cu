@@ -844,8 +844,13 @@ __global__ void __launch_bounds__(NTHR, 1)
                             }
                             rot_pass<ROTK, LAYB, false>(P, pass, 16 * G[sa], 16 * G[sb], group_rotated<ROTK>(P, G[sa]),
                                                         group_rotated<ROTK>(P, G[sb]), ha, hb, cf, qt);
-                            ca_store16(lane_addr + TM_CA + 8 * G[sa], ha, !live);
-                            ca_store16(lane_addr + TM_CA + 8 * G[sb], hb, !live);
+                            if (live) {  // (warp-uniform: no per-word select on the common path)
+                                ca_store16(lane_addr + TM_CA + 8 * G[sa], ha, false);
+                                ca_store16(lane_addr + TM_CA + 8 * G[sb], hb, false);
+                            } else {
+                                ca_store16(lane_addr + TM_CA + 8 * G[sa], ha, true);
+                                ca_store16(lane_addr + TM_CA + 8 * G[sb], hb, true);
+                            }
                         }
                         tc::tmem_wait_st();
                         tc::tc_fence_before();
