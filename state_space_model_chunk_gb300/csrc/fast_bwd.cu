@@ -798,18 +798,24 @@ __global__ void __launch_bounds__(NTHR, 1)
                     auto build_pa = [&](int t) {
                         const int o = t - s0;
                         if (pr.once(U_PA)) ok &= tc::mbar_wait(&ctl->pafree, pr.next(B_PA), abort);
-                        for (int i = ctid; i < ((o + 1) * 16) << CS; i += NCW * 32) {
-                            const int jc = i & 7, c = (i >> 3) & ((1 << CS) - 1), c2 = (i >> (3 + CS)) & 1,
-                                      j = i >> (4 + CS);
-                            if (c >= C) continue;
-                            const uint32_t off = j * 4096u + tc::sw128_chunk(16, c2, 8 * c2 + c, jc);
-                            uint4 w = make_uint4(0, 0, 0, 0);
-                            if (c2 ? I.exists[1] : I.exists[0]) {
-                                const float L = Lt[(c2 * 8 + o) * 8 + j];
-                                const uint4 v = *reinterpret_cast<const uint4*>(sm + OFF_SX + off);
-                                w = scale_bf16x8(v, L);
+                        // this thread's unit of a token row -- (chunk c2, channel slot c, 16-byte column
+                        // block jc) -- is the same in every row it handles: the stride is whole rows
+                        constexpr int UPR = 16 << CS;  // units per token row
+                        const int u = ctid & (UPR - 1);
+                        const int jc = u & 7, c = (u >> 3) & ((1 << CS) - 1), c2 = u >> (3 + CS);
+                        if (c < C) {
+                            const uint32_t base = tc::sw128_chunk(16, c2, 8 * c2 + c, jc);
+                            const bool ex = c2 ? I.exists[1] : I.exists[0];
+                            for (int j = ctid / UPR; j <= o; j += (NCW * 32) / UPR) {
+                                const uint32_t off = j * 4096u + base;
+                                uint4 w = make_uint4(0, 0, 0, 0);
+                                if (ex) {
+                                    const float L = Lt[(c2 * 8 + o) * 8 + j];
+                                    const uint4 v = *reinterpret_cast<const uint4*>(sm + OFF_SX + off);
+                                    w = scale_bf16x8(v, L);
+                                }
+                                *reinterpret_cast<uint4*>(sm + OFF_PA + off) = w;
                             }
-                            *reinterpret_cast<uint4*>(sm + OFF_PA + off) = w;
                         }
                         tc::fence_proxy_async_smem();
                         __syncwarp();
