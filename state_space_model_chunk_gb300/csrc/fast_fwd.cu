@@ -301,6 +301,12 @@ __global__ void __launch_bounds__(NTHR, 1)
                 const uint32_t s = q % NS, u = q / NS;
                 check(tc::mbar_wait(&ctl->full[s], u & 1, abort));
                 const bool live = t < Tch;
+                if (t == Tch) {  // the chunk's valid tokens are done: from here its c rows are zero
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) S[g][e] = 0.f;
+                }
                 const float et = live ? __expf(reinterpret_cast<const float*>(sm + OFF_DA + s * 256 + ch * 128)[I.hd & 3])
                                       : 1.f;
                 const float* qt = reinterpret_cast<const float*>(sm + OFF_ROT + s * 1024 + ch * 512);
@@ -398,8 +404,9 @@ __global__ void __launch_bounds__(NTHR, 1)
                             }
                         }
                     }
-                    write_tile16(ct, m, G[sa], a, !live);
-                    write_tile16(ct, m, G[sb], b, !live);
+                    // (past the chunk's valid tokens S is zero, and so is its de-rotation)
+                    write_tile16(ct, m, G[sa], a, false);
+                    write_tile16(ct, m, G[sb], b, false);
                 }
                 tc::fence_proxy_async_smem();
                 __syncwarp();
