@@ -197,6 +197,25 @@ void mm_prof_mark(int kid, int begin, cudaStream_t st) {
     }
 }
 
+cudaError_t mm_allow_smem(const void* fn, int bytes) {
+    static std::mutex mu;
+    static std::vector<std::pair<std::pair<const void*, int>, int>> done;  // (function, device) -> bytes
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> g(mu);
+    for (auto& d : done)
+        if (d.first.first == fn && d.first.second == dev) {
+            if (d.second >= bytes) return cudaSuccess;
+            if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) == cudaSuccess)
+                d.second = bytes;
+            return e;
+        }
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) == cudaSuccess)
+        done.push_back({{fn, dev}, bytes});
+    return e;
+}
+
 extern "C" {
 
 size_t mm_workspace_bytes(const mm_problem* prob, int backward) {

@@ -1166,7 +1166,7 @@ cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, float* d
         case ROT_QUAT: kern = c8 ? tc_bwd_kernel<ROT_QUAT, 0, 3> : tc_bwd_kernel<ROT_QUAT, 0, 2>; break;
         default: kern = c8 ? tc_bwd_kernel<ROT_NONE, 0, 3> : tc_bwd_kernel<ROT_NONE, 0, 2>; break;
     }
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaError_t e = mm_allow_smem(reinterpret_cast<const void*>(kern), (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     mm_prof_mark(KID_FAST_BWD, 1, st);
     kern<<<grid, NTHR, SMEM_BYTES, st>>>(a, maps.x, maps.b, maps.rot, maps.da64);

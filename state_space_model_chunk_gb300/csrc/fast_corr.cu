@@ -489,7 +489,7 @@ cudaError_t launch_tc_corr(const FastArgs& fa, const float* da, const float* E, 
     a.db = static_cast<__nv_bfloat16*>(db);
     a.dda = dda;
     const int grid = items < sm_count() ? items : sm_count();
-    cudaError_t e = cudaFuncSetAttribute(tc_corr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaError_t e = mm_allow_smem(reinterpret_cast<const void*>(tc_corr_kernel), (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     mm_prof_mark(KID_FAST_CORRECT, 1, st);
     tc_corr_kernel<<<grid, NTHR, SMEM_BYTES, st>>>(a, maps.x32, maps.b32, maps.dx32, maps.db32);

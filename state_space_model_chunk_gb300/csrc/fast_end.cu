@@ -298,7 +298,7 @@ cudaError_t launch_tc_end(const FastArgs& fa, const TensorMaps& maps, cudaStream
     const int items = count_chunks(fa.P);
     if (items == 0) return cudaSuccess;
     const int grid = items < 2 * sm_count() ? items : 2 * sm_count();
-    cudaError_t e = cudaFuncSetAttribute(tc_end_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaError_t e = mm_allow_smem(reinterpret_cast<const void*>(tc_end_kernel), (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     mm_prof_mark(KID_FAST_END, 1, st);
     tc_end_kernel<<<grid, NTHR, SMEM_BYTES, st>>>(fa, maps.x8, maps.b8, maps.da64);

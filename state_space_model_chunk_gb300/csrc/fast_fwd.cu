@@ -530,7 +530,7 @@ cudaError_t launch_tc_fwd(const FastArgs& args, const TensorMaps& maps, int grid
         case ROT_QUAT: kern = dat ? tc_fwd_kernel<ROT_QUAT, 0, true> : tc_fwd_kernel<ROT_QUAT, 0, false>; break;
         default: kern = dat ? tc_fwd_kernel<ROT_NONE, 0, true> : tc_fwd_kernel<ROT_NONE, 0, false>; break;
     }
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaError_t e = mm_allow_smem(reinterpret_cast<const void*>(kern), (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     mm_prof_mark(KID_FAST_FWD, 1, st);
     kern<<<grid, NTHR, SMEM_BYTES, st>>>(args, maps.x, maps.b, maps.rot, maps.da);

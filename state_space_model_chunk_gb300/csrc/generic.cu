@@ -559,14 +559,13 @@ bool generic_supported(const MMParams& P, int smem_limit) {
 template <typename T>
 static cudaError_t set_smem_attrs(const MMParams& P) {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(k_fwd_chunk<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)generic_fwd_smem(P))) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(k_bwd_chunk<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)generic_bwd_smem(P))) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(k_correct<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)generic_correct_smem(P))) != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_chunk_end<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)generic_end_smem(P));
+    if ((e = mm_allow_smem(reinterpret_cast<const void*>(k_fwd_chunk<T>), (int)generic_fwd_smem(P))) != cudaSuccess)
+        return e;
+    if ((e = mm_allow_smem(reinterpret_cast<const void*>(k_bwd_chunk<T>), (int)generic_bwd_smem(P))) != cudaSuccess)
+        return e;
+    if ((e = mm_allow_smem(reinterpret_cast<const void*>(k_correct<T>), (int)generic_correct_smem(P))) != cudaSuccess)
+        return e;
+    return mm_allow_smem(reinterpret_cast<const void*>(k_chunk_end<T>), (int)generic_end_smem(P));
 }
 
 template <typename T>

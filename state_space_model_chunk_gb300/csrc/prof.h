@@ -24,3 +24,8 @@ enum MMKernelId {
 
 // Records an event on `st` before (begin = 1) or after (begin = 0) launch `kid` when profiling is on.
 void mm_prof_mark(int kid, int begin, cudaStream_t st);
+
+// cudaFuncSetAttribute(fn, MaxDynamicSharedMemorySize, bytes) on the current device, skipped when
+// an earlier call already allowed at least `bytes` there: after a first call of a problem, the
+// library's calls issue nothing but stream work (so a stream capture of them records only that).
+cudaError_t mm_allow_smem(const void* fn, int bytes);
