@@ -35,6 +35,10 @@
  *   - All device pointers are owned by the caller.  The library never allocates, frees or
  *     synchronises: every call only enqueues work on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream) and returns.  Outputs are overwritten, never accumulated.
+ *   - Stream capture: after a problem's first call on a device (which may set a kernel's
+ *     shared-memory limit), calls of that problem issue nothing but stream work -- kernel
+ *     launches and memsets -- so they can be recorded into a CUDA graph and replayed; the
+ *     problem, its valid lengths and every pointer are fixed in the recorded graph.
  *   - `workspace` is caller-owned device scratch of at least mm_workspace_bytes() bytes,
  *     256-byte aligned.  Its contents need no initialisation and are clobbered.
  *   - Calls are thread-compatible: concurrent calls need distinct workspaces.
