@@ -199,14 +199,15 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 
 // Byte offset of element (row, col) of a [rows x (64*k)] bf16 tile kept in the 128-byte-swizzled
 // layout above: 64-column blocks of `rows/8` atoms of 1024 bytes each, block after block.
+// (rows of 128 bytes in 1024-byte groups of eight: the row's byte offset is row * 128)
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t rows, uint32_t row, uint32_t col) {
     uint32_t half = col >> 6, c = col & 63;
     uint32_t chunk = (c >> 3) ^ (row & 7);
-    return half * rows * 128u + (row >> 3) * 1024u + (row & 7) * 128u + chunk * 16u + (c & 7) * 2u;
+    return half * rows * 128u + row * 128u + chunk * 16u + (c & 7) * 2u;
 }
 // Byte offset of the 16-byte chunk `j` (0..7: columns 8j..8j+7 of a 64-column block) of row `row`.
 __device__ __forceinline__ uint32_t sw128_chunk(uint32_t rows, uint32_t half, uint32_t row, uint32_t j) {
-    return half * rows * 128u + (row >> 3) * 1024u + (row & 7) * 128u + ((j ^ (row & 7)) << 4);
+    return half * rows * 128u + row * 128u + ((j ^ (row & 7)) << 4);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
