@@ -131,7 +131,7 @@ def path(spec: Spec, backward: bool) -> int:
 _warned = set()
 
 TC_RULES = ("bf16 operands, p a multiple of 64 up to 512, r a multiple of 16 up to 128 (64 or 128 for half-split), "
-            "s % 64 == 0, C <= 8, "
+            "C <= 8, "
             "rotation width (rope_dim/2 or 4 J) a multiple of 4 and at most 128")
 
 

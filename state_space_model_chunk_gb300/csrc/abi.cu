@@ -99,7 +99,7 @@ Layout layout(const mm_problem* P, int backward) {
     const size_t l_eff = fast ? (size_t)fastk_chunk() : (size_t)P->chunk_len;
     const size_t pr = (size_t)P->p * P->r;
     const size_t nbh = (size_t)P->b * P->h;
-    const size_t nc = (size_t)P->s / l_eff;
+    const size_t nc = ((size_t)P->s + l_eff - 1) / l_eff;  // (the tensor-core path's last chunk may be partial)
     size_t off = kHeader;  // header: device error word
     L.Hc = off; off = align_up(off + sizeof(float) * nbh * nc * pr);
     // chunk decays: per head, or on the tensor-core path per 64-row group of a head (each group

@@ -46,7 +46,7 @@ cudaError_t encode(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank, cons
 MMParams internal_params(const MMParams& P0) {
     MMParams P = P0;
     P.l = fastk::FL;
-    P.nc = P.s / fastk::FL;
+    P.nc = (P.s + fastk::FL - 1) / fastk::FL;
     P.heads = P0.h;
     P.groups = P0.p / 64;
     P.h = P0.h * P.groups;
@@ -254,7 +254,7 @@ bool fast_supported(const MMParams& P, bool bf16, int backward) {
     if (P.p < 64 || P.p % 64 || P.p > 512) return false;
     const int64_t groups = P.p / 64;
     if ((int64_t)P.h * groups > 65535 || groups * P.b * P.s > ((int64_t)1 << 31) - 1) return false;
-    if (P.s % fastk::FL || P.b > MM_MAX_B) return false;
+    if (P.b > MM_MAX_B) return false;  // (any s: the last chunk of a row may be partial)
     // rows of angles / quaternions are copied as 16-byte multiples, at most 128 floats
     if (P.rw % 4 || P.rw > 128) return false;
     if (!encode_fn()) return false;

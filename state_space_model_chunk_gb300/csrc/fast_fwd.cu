@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                 if (!DAT) {
                     // this head's da of the token, into the slot position the 4-head copy would fill,
                     // stored before the arrival that publishes the stage
-                    if (lane < 2 && I.exists[lane]) {
+                    if (lane < 2 && t < I.T[lane]) {  // (no read past the row's end)
                         const int row = I.bb * P.s + (2 * I.k + lane) * FL + t;
                         reinterpret_cast<float*>(sm + OFF_DA + s * 256 + lane * 128)[I.hd & 3] =
                             A.da[(int64_t)row * P.heads + I.hd];

@@ -20,6 +20,8 @@ CASES = [
     WORKLOADS["large_s4096"].scaled(name="large_det", b=2, s=512, h=8, valid="fixed:450"),
     # two 64-row groups per head: their slices are summed in group order
     WORKLOADS["large_s4096"].scaled(name="p128_det", b=2, s=512, h=4, p=128, valid="fixed:450"),
+    # a sequence length that is not a multiple of 64
+    WORKLOADS["ragged_s16384"].scaled(name="s1000_det", b=2, s=1000, h=4, chunk_len=8),
 ]
 
 

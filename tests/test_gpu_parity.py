@@ -27,7 +27,7 @@ def expected_fast(w, backward):
     rw = w.rope_dim // 2 if w.rot in ("pairwise", "half") else (4 * w.quat_blocks if w.rot == "quat" else 0)
     r_ok = w.r in (64, 128) if w.rot == "half" else (w.r % 16 == 0 and 16 <= w.r <= 128)
     p_ok = w.p % 64 == 0 and 64 <= w.p <= 512
-    return (w.dtype == "bf16" and p_ok and r_ok and 1 <= w.C <= 8 and w.s % 64 == 0
+    return (w.dtype == "bf16" and p_ok and r_ok and 1 <= w.C <= 8
             and rw % 4 == 0 and rw <= 128)
 
 
@@ -99,6 +99,14 @@ SMALL = [
     WORKLOADS["large_s4096"].scaled(name="norot_p256_r32", b=1, s=128, h=2, p=256, r=32, rot="none", rope_dim=0),
     WORKLOADS["ragged_s16384"].scaled(name="ragged_p128_c5", b=3, s=256, h=2, p=128, C=5, r=80, rot="pairwise",
                                       rope_dim=48, chunk_len=64),
+    # sequence lengths that are not a multiple of 64: the last chunk of every row is partial --
+    # paired after a full chunk (s = 200, 100, 72) or alone in its pair (s = 136) -- and the
+    # copies of its missing tokens run past the row (into the next row, or past the tensor)
+    WORKLOADS["large_s4096"].scaled(name="pairwise_s200", b=2, s=200, h=4, chunk_len=8, valid="ragged"),
+    WORKLOADS["quat_s2048"].scaled(name="quat_s100_h3_p128", b=2, s=100, h=3, p=128, chunk_len=20,
+                                   quat_blocks=20),
+    WORKLOADS["halfsplit_s1024"].scaled(name="half_s72", b=3, s=72, h=2, chunk_len=8),
+    WORKLOADS["ragged_s16384"].scaled(name="ragged_s136_h5", b=3, s=136, h=5, chunk_len=8),
 ]
 
 

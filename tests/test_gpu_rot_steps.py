@@ -33,6 +33,9 @@ CASES = [
     (WORKLOADS["quat_s2048"].scaled(name="steps_quat_p128", b=2, s=192, h=2, p=128, quat_blocks=12,
                                     valid="ragged"), False),
     (WORKLOADS["large_s4096"].scaled(name="steps_pairwise_p192", b=1, s=256, h=3, p=192, C=2), False),
+    # a sequence length that is not a multiple of 64 (the scans' and the kernels' last chunk partial)
+    (WORKLOADS["large_s4096"].scaled(name="steps_pairwise_s200", b=2, s=200, h=2, chunk_len=40, valid="ragged"),
+     False),
     # nothing valid: every output and gradient is zero
     (WORKLOADS["large_s4096"].scaled(name="steps_none_valid", b=1, s=128, h=4, valid="fixed:0"), False),
 ]
