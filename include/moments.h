@@ -149,7 +149,8 @@ const char* mm_status_string(mm_status status);
 
 /* Which kernel path a call with this problem takes: 0 = SIMT fp32, 1 = tcgen05 tensor-core
  * path; -1 if the problem is invalid.  Host-only.  The tensor-core path takes bf16 operands with
- * p a multiple of 64 up to 512, r a multiple of 16 up to 128 (64 or 128 for half-split rotation),
+ * p a multiple of 8 below 64 or of 64 up to 512, r a multiple of 16 up to 128 (64 or 128 for
+ * half-split rotation),
  * any s, 1 <= C <= 8 and a rotation width (rope_dim / 2, or 4 quat_blocks) that is a multiple of 4
  * and at most 128. */
 int mm_path(const mm_problem* prob, int backward);

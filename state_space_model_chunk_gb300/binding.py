@@ -130,7 +130,8 @@ def path(spec: Spec, backward: bool) -> int:
 
 _warned = set()
 
-TC_RULES = ("bf16 operands, p a multiple of 64 up to 512, r a multiple of 16 up to 128 (64 or 128 for half-split), "
+TC_RULES = ("bf16 operands, p a multiple of 8 below 64 or of 64 up to 512, r a multiple of 16 up to 128 "
+            "(64 or 128 for half-split), "
             "C <= 8, "
             "rotation width (rope_dim/2 or 4 J) a multiple of 4 and at most 128")
 

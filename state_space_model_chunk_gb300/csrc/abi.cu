@@ -69,6 +69,7 @@ void fill_params(const mm_problem* P, const int64_t* valid_host, MMParams* out) 
     out->rw = rot_width(P);
     out->heads = out->h;
     out->groups = 1;
+    out->prow = out->p;
     for (int64_t i = 0; i < P->b && valid_host; ++i) {
         int64_t v = valid_host[i];
         out->valid[i] = (int)(v < 0 ? 0 : (v > P->s ? P->s : v));
@@ -97,7 +98,8 @@ Layout layout(const mm_problem* P, int backward) {
     const bool fast = use_fast(P, M, backward);
     // the tensor-core path keeps its carries at a fixed 64-token granularity
     const size_t l_eff = fast ? (size_t)fastk_chunk() : (size_t)P->chunk_len;
-    const size_t pr = (size_t)P->p * P->r;
+    // (the tensor-core path runs at least 64 state rows per head: p below 64 is padded with zero rows)
+    const size_t pr = (size_t)((fast && P->p < 64) ? 64 : P->p) * P->r;
     const size_t nbh = (size_t)P->b * P->h;
     const size_t nc = ((size_t)P->s + l_eff - 1) / l_eff;  // (the tensor-core path's last chunk may be partial)
     size_t off = kHeader;  // header: device error word

@@ -23,6 +23,10 @@ struct MMParams {
     // by the caller's head, h / groups.  Outside that path groups = 1 and heads = h.
     int heads;
     int groups;
+    // Rows of xhat / d_xhat per (row-group) head in the caller's layout: p, except on the
+    // tensor-core path for p below 64, where the kernels run 64 rows (p = 64) and the rows past
+    // prow are zero.
+    int prow;
     int valid[MM_MAX_B];          // valid_len per batch row, clamped to [0, s]
 };
 
@@ -40,7 +44,7 @@ __host__ __device__ inline int mm_chunk_rows(const MMParams& P, int bb, int n) {
 
 // Row-major offsets.
 __device__ __forceinline__ int64_t off_x(const MMParams& P, int bb, int t, int c, int hh) {
-    return ((((int64_t)bb * P.s + t) * P.C + c) * P.h + hh) * P.p;
+    return ((((int64_t)bb * P.s + t) * P.C + c) * P.h + hh) * P.prow;
 }
 // bhat / da / rot and their gradients: hh is the caller's head (see MMParams::heads)
 __device__ __forceinline__ int64_t off_b(const MMParams& P, int bb, int t, int c, int hh) {

@@ -41,6 +41,8 @@ cudaError_t encode(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank, cons
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
 // The kernels' view of a problem: 64-token chunks, and each head's p state rows as p / 64 heads
 // of 64 rows (MMParams::groups).
 MMParams internal_params(const MMParams& P0) {
@@ -48,13 +50,36 @@ MMParams internal_params(const MMParams& P0) {
     P.l = fastk::FL;
     P.nc = (P.s + fastk::FL - 1) / fastk::FL;
     P.heads = P0.h;
-    P.groups = P0.p / 64;
+    P.groups = P0.p < 64 ? 1 : P0.p / 64;
+    P.prow = P0.p < 64 ? P0.p : 64;  // below 64 rows: padded with zero rows
     P.h = P0.h * P.groups;
     P.p = 64;
     return P;
 }
 
-size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+// p below 64: the caller's [b, h, prow, r] initial state into 64-row slots (rows past prow zero),
+// and the kernels' 64-row d_initial back into the caller's layout.
+__global__ void __launch_bounds__(256) k_pad_rows(const float* __restrict__ src, float* __restrict__ dst, int64_t bh,
+                                                  int prow, int r) {
+    const int64_t n = bh * 64 * r;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t u = i / ((int64_t)64 * r), rem = i - u * 64 * r;
+        const int row = (int)(rem / r), col = (int)(rem - (int64_t)row * r);
+        dst[i] = row < prow ? src[(u * prow + row) * r + col] : 0.f;
+    }
+}
+__global__ void __launch_bounds__(256) k_unpad_rows(const float* __restrict__ src, float* __restrict__ dst, int64_t bh,
+                                                    int prow, int r) {
+    const int64_t n = bh * prow * r;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t u = i / ((int64_t)prow * r), rem = i - u * prow * r;
+        dst[i] = src[u * 64 * r + rem];
+    }
+}
+size_t padded_state_bytes(const MMParams& P) {  // P: the internal view
+    return P.prow < P.p ? align256(sizeof(float) * (size_t)P.b * P.h * P.p * P.r) : 0;
+}
+
 
 // Workspace slices of a problem with several 64-row groups per head: the groups' own copies of
 // the outputs that sum over state rows, added in group order once every group is done.
@@ -154,9 +179,9 @@ int sm_count() {
 cudaError_t encode_grad_maps(const MMParams& P, const void* dx, const void* db, TensorMaps* maps) {
     const cuuint64_t bs = (cuuint64_t)P.b * P.s;
     cudaError_t e;
-    {   // as x32, over d_xhat
-        cuuint64_t dims[4] = {(cuuint64_t)P.p, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
-        cuuint64_t str[3] = {(cuuint64_t)P.p * 2, (cuuint64_t)P.h * P.p * 2, (cuuint64_t)P.C * P.h * P.p * 2};
+    {   // as x32, over d_xhat (the stores skip rows past prow)
+        cuuint64_t dims[4] = {(cuuint64_t)P.prow, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
+        cuuint64_t str[3] = {(cuuint64_t)P.prow * 2, (cuuint64_t)P.h * P.prow * 2, (cuuint64_t)P.C * P.h * P.prow * 2};
         cuuint32_t box[4] = {64, 1, (cuuint32_t)P.C, (cuuint32_t)corr_tps(P)};
         if ((e = encode(&maps->dx32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, dx, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
@@ -178,9 +203,10 @@ cudaError_t encode_maps(const MMParams& P, const void* xhat, const void* bhat, c
                         TensorMaps* maps) {
     const cuuint64_t bs = (cuuint64_t)P.b * P.s;
     cudaError_t e;
-    {   // xhat as [b*s, C, h, p] bf16 (h, p: 64-row groups as heads); box = the C rows of one (token, head)
-        cuuint64_t dims[4] = {(cuuint64_t)P.p, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
-        cuuint64_t str[3] = {(cuuint64_t)P.p * 2, (cuuint64_t)P.h * P.p * 2, (cuuint64_t)P.C * P.h * P.p * 2};
+    {   // xhat as [b*s, C, h, prow] bf16 (h, prow: 64-row groups as heads); box = the C rows of one
+        // (token, head), 64 wide: rows past prow (p below 64) read as zeros
+        cuuint64_t dims[4] = {(cuuint64_t)P.prow, (cuuint64_t)P.h, (cuuint64_t)P.C, bs};
+        cuuint64_t str[3] = {(cuuint64_t)P.prow * 2, (cuuint64_t)P.h * P.prow * 2, (cuuint64_t)P.C * P.h * P.prow * 2};
         cuuint32_t box[4] = {64, 1, (cuuint32_t)P.C, 1};
         if ((e = encode(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, xhat, dims, str, box,
                         CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
@@ -251,8 +277,11 @@ bool fast_supported(const MMParams& P, bool bf16, int backward) {
     if (P.rot == ROT_HALF && P.r != 64 && P.r != 128) return false;
     // p: groups of 64 state rows, each run as a head of its own (grid rows and tensor-copy
     // coordinates of the groups stay within their 16- and 32-bit limits)
-    if (P.p < 64 || P.p % 64 || P.p > 512) return false;
-    const int64_t groups = P.p / 64;
+    // (below 64: the kernels run 64 rows, the rows past p zero; the caller's rows must stay 16-byte
+    // multiples for the tensor copies)
+    const bool small = P.p >= 8 && P.p < 64 && P.p % 8 == 0;
+    if (!small && (P.p < 64 || P.p % 64 || P.p > 512)) return false;
+    const int64_t groups = small ? 1 : P.p / 64;
     if ((int64_t)P.h * groups > 65535 || groups * P.b * P.s > ((int64_t)1 << 31) - 1) return false;
     if (P.b > MM_MAX_B) return false;  // (any s: the last chunk of a row may be partial)
     // rows of angles / quaternions are copied as 16-byte multiples, at most 128 floats
@@ -264,10 +293,11 @@ bool fast_supported(const MMParams& P, bool bf16, int backward) {
 size_t fast_scratch_bytes(const MMParams& P, int backward) {
     const MMParams Pi = internal_params(P);
     const GroupSlices g = group_slices(Pi);
-    if (!backward) return align256(fastk::fwd_partial_bytes(Pi)) + g.total_fwd;
+    if (!backward) return align256(fastk::fwd_partial_bytes(Pi)) + g.total_fwd + padded_state_bytes(Pi);
     const size_t a = fastk::bwd_anchor_bytes();  // a multiple of 256 bytes
-    if (Pi.groups > 1) return a + g.total_bwd;  // the d_rot partials live in the group slices
-    return a + fastk::bwd_drot2_bytes(P);
+    // (with row groups the d_rot partials live in the group slices); then the padded initial
+    // state and d_initial for p below 64
+    return a + (Pi.groups > 1 ? g.total_bwd : align256(fastk::bwd_drot2_bytes(P))) + 2 * padded_state_bytes(Pi);
 }
 
 cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cudaStream_t st) {
@@ -299,8 +329,16 @@ cudaError_t fast_fwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     }
     int grid = fa.items < sm_count() ? fa.items : sm_count();
     if (grid > kMaxFwdGrid) grid = kMaxFwdGrid;
+    const float* init = A.initial;
+    if (P.prow < P.p) {  // p below 64: the initial state in 64-row slots
+        float* init64 = reinterpret_cast<float*>(gbase + gs.total_fwd);
+        const int64_t bh = (int64_t)P.b * P.h;
+        k_pad_rows<<<sum_blocks(bh * P.p * P.r), 256, 0, st>>>(A.initial, init64, bh, P.prow, P.r);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        init = init64;
+    }
     if ((e = launch_tc_end(fa, maps, st)) != cudaSuccess) return e;
-    if ((e = generic_carry_scan(P, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
+    if ((e = generic_carry_scan(P, init, A.Hc, A.Dn, st)) != cudaSuccess) return e;
     if ((e = launch_tc_fwd(fa, maps, grid, st)) != cudaSuccess || P.groups == 1) return e;
     // m2 / m1 of a head: its groups' moments, in group order
     const int64_t bh = (int64_t)P.b * P.heads;
@@ -322,7 +360,7 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     fa.err = A.err;
     cudaError_t e;
     const size_t bs = (size_t)P.b * P.s, es = 2;
-    const size_t nx = bs * P.C * P.h * P.p, nb = bs * P.C * P.heads * P.r, nda = bs * P.heads,
+    const size_t nx = bs * P.C * P.h * P.prow, nb = bs * P.C * P.heads * P.r, nda = bs * P.heads,
                  nrot = bs * P.heads * P.rw;
     if (fa.items == 0) {  // nothing valid: every gradient, d_initial included, is zero
         if ((e = cudaMemsetAsync(A.dxhat, 0, es * nx, st)) != cudaSuccess ||
@@ -330,7 +368,7 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
             (e = cudaMemsetAsync(A.dda, 0, sizeof(float) * nda, st)) != cudaSuccess ||
             (P.rw && (e = cudaMemsetAsync(A.drot, 0, sizeof(float) * nrot, st)) != cudaSuccess))
             return e;
-        return cudaMemsetAsync(A.dinit, 0, sizeof(float) * (size_t)P.b * P.h * P.p * P.r, st);
+        return cudaMemsetAsync(A.dinit, 0, sizeof(float) * (size_t)P.b * P.h * P.prow * P.r, st);
     }
     // Where the kernels write d_bhat, d_da and d_rot: the outputs themselves (d_rot's second
     // partial in the workspace), or with several row groups one slice per group in the workspace,
@@ -353,8 +391,8 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
         const size_t v = (size_t)P.valid[bb], tail = (size_t)P.s - v;
         if (!tail) continue;
         const size_t row0 = (size_t)bb * P.s + v;
-        if ((e = cudaMemsetAsync(static_cast<char*>(A.dxhat) + es * row0 * P.C * P.h * P.p, 0,
-                                 es * tail * P.C * P.h * P.p, st)) != cudaSuccess)
+        if ((e = cudaMemsetAsync(static_cast<char*>(A.dxhat) + es * row0 * P.C * P.h * P.prow, 0,
+                                 es * tail * P.C * P.h * P.prow, st)) != cudaSuccess)
             return e;
         for (int g = 0; g < G; ++g)
             if ((e = cudaMemsetAsync(static_cast<char*>(db) + es * ((size_t)g * nb + row0 * P.C * P.heads * P.r), 0,
@@ -364,16 +402,32 @@ cudaError_t fast_bwd(const MMParams& P0, const GenericPtrs& A, char* scratch, cu
     TensorMaps maps;
     if ((e = encode_maps(P, A.xhat, A.bhat, A.rot, A.da, &maps)) != cudaSuccess) return e;
     int grid = fa.items < sm_count() ? fa.items : sm_count();
+    // p below 64: the initial state and d_initial in 64-row slots after the other scratch
+    char* pbase = scratch + bwd_anchor_bytes() + (grouped ? gs.total_bwd : align256(bwd_drot2_bytes(P0)));
+    float* init64 = reinterpret_cast<float*>(pbase);
+    float* dinit64 = reinterpret_cast<float*>(pbase + padded_state_bytes(P));
+    const bool padded = P.prow < P.p;
+    const int64_t bh = (int64_t)P.b * P.h;
     if (!A.reuse_carries) {  // else the forward of the same problem left the carries in Hc / Dn
+        const float* init = A.initial;
+        if (padded) {
+            k_pad_rows<<<sum_blocks(bh * P.p * P.r), 256, 0, st>>>(A.initial, init64, bh, P.prow, P.r);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            init = init64;
+        }
         if ((e = launch_tc_end(fa, maps, st)) != cudaSuccess) return e;
-        if ((e = generic_carry_scan(P, A.initial, A.Hc, A.Dn, st)) != cudaSuccess) return e;
+        if ((e = generic_carry_scan(P, init, A.Hc, A.Dn, st)) != cudaSuccess) return e;
     }
     if (grid > kMaxBwdGrid) grid = kMaxBwdGrid;
     float* anchors = reinterpret_cast<float*>(scratch);
     if ((e = launch_tc_bwd(fa, A.E, anchors, drot2, A.dm2, A.dm1, A.dxhat, db, dda, drot, A.rot, maps, grid, st)) !=
         cudaSuccess)
         return e;
-    if ((e = generic_cot_scan(P, A.E, A.Dn, A.dinit, st)) != cudaSuccess) return e;
+    if ((e = generic_cot_scan(P, A.E, A.Dn, padded ? dinit64 : A.dinit, st)) != cudaSuccess) return e;
+    if (padded) {  // d_initial back into the caller's rows
+        k_unpad_rows<<<sum_blocks(bh * P.prow * P.r), 256, 0, st>>>(dinit64, A.dinit, bh, P.prow, P.r);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if ((e = encode_grad_maps(P, A.dxhat, db, &maps)) != cudaSuccess) return e;
     if ((e = launch_tc_corr(fa, A.da, A.E, A.dxhat, db, dda, maps, st)) != cudaSuccess || !grouped) return e;
     // a head's d_bhat, d_da and d_rot: its groups' slices in group order (d_rot: the G rows-0-31

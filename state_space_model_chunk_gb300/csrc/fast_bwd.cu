@@ -64,7 +64,8 @@ cudaError_t launch_tc_bwd(const FastArgs& fa, float* E, float* anchors, float* d
     a.drot_slice = grouped ? ntok * fa.P.heads * fa.P.rw : 0;
     // channel slots per chunk in the span tiles: 4 when C <= 4, else 8
     decltype(&tc_bwd_kernel<ROT_NONE, 0, 2, false>) kern;
-    const bool c8 = fa.P.C > 4, rag = (fa.P.s % FL) != 0;
+    // (the general-shape instantiations: a partial last chunk, or fewer than 64 rows per head)
+    const bool c8 = fa.P.C > 4, rag = (fa.P.s % FL) != 0 || fa.P.prow < fa.P.p;
 #define BWD_KERN(K, L) (c8 ? tc_bwd_kernel<K, L, 3, false> : tc_bwd_kernel<K, L, 2, false>)
     switch (fa.P.rot) {
         case ROT_PAIRWISE: kern = BWD_KERN(ROT_PAIRWISE, 0); break;

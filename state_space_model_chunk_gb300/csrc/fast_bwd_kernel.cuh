@@ -264,9 +264,10 @@ enum : uint32_t {
     B_ITEM = 6, B_SPAN, B_PA, B_P, B_C, B_DC, B_G, B_DX, B_ITEMDONE,
     U_PRE = 24, U_DC, U_DX, U_PA, U_C, U_G, U_SPAN
 };
-// RAG: the sequence length is not a multiple of 64, so a row's last chunk ends inside it; the
-// second chunk of a pair then stores its per-token gradient rows only up to its valid tokens (its
-// steps run on with the first chunk's, past the row's end)
+// RAG: the general-shape variant, for a sequence length that is not a multiple of 64 (a row's last
+// chunk ends inside it: the second chunk of a pair stores its per-token gradient rows only up to
+// its valid tokens, its steps running on with the first chunk's past the row's end) and for fewer
+// than 64 state rows per head (the d_xhat rows past prow, zero padding, are not stored)
 template <int ROTK, int LAYB, int CS, bool RAG>
 __global__ void __launch_bounds__(NTHR, 1)
     tc_bwd_kernel(const __grid_constant__ BwdArgs B, const __grid_constant__ CUtensorMap tmx,
@@ -587,7 +588,8 @@ __global__ void __launch_bounds__(NTHR, 1)
             // this thread's output rows for token 0 of the item (null where it writes none): the
             // per-token steps only add the token stride
             uint64_t* ptab = reinterpret_cast<uint64_t*>(sm + OFF_PTR) + ctid * 3;
-            ptab[0] = (half == 0 && chunk_ok) ? reinterpret_cast<uint64_t>(B.dx + off_x(P, I.bb, n * FL, 0, I.hh) + pp)
+            ptab[0] = (half == 0 && chunk_ok && (!RAG || pp < P.prow))  // (past prow: zero padding rows)
+                          ? reinterpret_cast<uint64_t>(B.dx + off_x(P, I.bb, n * FL, 0, I.hh) + pp)
                                               : 0ull;
             // (with row groups, d_bhat / d_rot / d_da of group g go to slice g of their buffers)
             ptab[1] = (m < R && half_ok)
@@ -1029,7 +1031,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                         tc::tc_fence_before();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&ctl->dxfree);
-                        const int64_t hp = (int64_t)P.h * P.p, hr = (int64_t)P.heads * P.r;
+                        const int64_t hp = (int64_t)P.h * (RAG ? P.prow : P.p), hr = (int64_t)P.heads * P.r;
                         if (ptab[0] && (!RAG || t < Tch)) {
                             __nv_bfloat16* px = reinterpret_cast<__nv_bfloat16*>(ptab[0]) + (int64_t)t * C * hp;
 #pragma unroll
@@ -1105,7 +1107,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
 }
 
-// the kernel for sequence lengths that are not a multiple of 64 (RAG), compiled in fast_bwd_rag.cu
+// the general-shape kernel (RAG: partial last chunks, fewer than 64 rows), compiled in fast_bwd_rag.cu
 using BwdKernel = decltype(&tc_bwd_kernel<ROT_NONE, 0, 2, false>);
 BwdKernel ragged_bwd_kernel(int rot, int layoutB, bool c8);
 

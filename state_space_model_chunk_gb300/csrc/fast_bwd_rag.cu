@@ -1,5 +1,6 @@
-// fast_bwd_rag.cu -- the backward kernel's instantiations for sequence lengths that are not a
-// multiple of 64 (compiled apart from fast_bwd.cu so that the two build in parallel).
+// fast_bwd_rag.cu -- the backward kernel's general-shape instantiations, for sequence lengths that
+// are not a multiple of 64 and for fewer than 64 state rows per head (compiled apart from
+// fast_bwd.cu so that the two build in parallel).
 #include "fast_bwd_kernel.cuh"
 
 namespace fastbwd {

@@ -26,7 +26,7 @@ def expected_fast(w, backward):
     """Whether the tensor-core kernels implement this workload (else the SIMT kernels run)."""
     rw = w.rope_dim // 2 if w.rot in ("pairwise", "half") else (4 * w.quat_blocks if w.rot == "quat" else 0)
     r_ok = w.r in (64, 128) if w.rot == "half" else (w.r % 16 == 0 and 16 <= w.r <= 128)
-    p_ok = w.p % 64 == 0 and 64 <= w.p <= 512
+    p_ok = (w.p % 64 == 0 and 64 <= w.p <= 512) or (w.p % 8 == 0 and 8 <= w.p < 64)
     return (w.dtype == "bf16" and p_ok and r_ok and 1 <= w.C <= 8
             and rw % 4 == 0 and rw <= 128)
 
@@ -107,6 +107,11 @@ SMALL = [
                                    quat_blocks=20),
     WORKLOADS["halfsplit_s1024"].scaled(name="half_s72", b=3, s=72, h=2, chunk_len=8),
     WORKLOADS["ragged_s16384"].scaled(name="ragged_s136_h5", b=3, s=136, h=5, chunk_len=8),
+    # p below 64: the kernels run 64 rows, the rows past p zero (padded initial state, no d_xhat
+    # stores past p)
+    WORKLOADS["large_s4096"].scaled(name="pairwise_p32", b=2, s=192, h=4, p=32, valid="fixed:170"),
+    WORKLOADS["quat_s2048"].scaled(name="quat_p16_h3", b=1, s=128, h=3, p=16),
+    WORKLOADS["halfsplit_s1024"].scaled(name="half_p48_s100", b=2, s=100, h=2, p=48, chunk_len=4),
 ]
 
 
@@ -164,8 +169,10 @@ def test_parity_steep_decay_spans():
 @pytest.mark.parametrize("w", [SMALL[3], SMALL[0],
                                WORKLOADS["large_s4096"].scaled(name="tc_c6", b=1, s=128, h=4, C=6),
                                WORKLOADS["large_s4096"].scaled(name="tc_p128", b=2, s=192, h=2, p=128,
+                                                               valid="fixed:130"),
+                               WORKLOADS["large_s4096"].scaled(name="tc_p24", b=2, s=192, h=2, p=24,
                                                                valid="fixed:130")],
-                         ids=["tensor_core", "simt", "tensor_core_c6", "tensor_core_p128"])
+                         ids=["tensor_core", "simt", "tensor_core_c6", "tensor_core_p128", "tensor_core_p24"])
 def test_backward_reusing_forward_carries(w):
     """MM_FLAG_REUSE_CARRIES: forward then backward on one workspace gives the gradients of a
     backward that recomputes the carries (on the tensor-core path with four and six channels, and on
