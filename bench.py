@@ -119,7 +119,7 @@ def kernel_bytes_per_token_head(name, w):
 # dominant kernels, from one ncu capture of the current kernels on large_s4096 cut to b = 2; the
 # work per chunk pair does not depend on b, so a full launch moves these bytes times its
 # token-heads.
-MEASURED_DRAM_BYTES_PER_TOKEN_HEAD = {"tc_bwd_chunk": (1.512206e9 + 1.501054e9) / (2 * 4096 * 32),
+MEASURED_DRAM_BYTES_PER_TOKEN_HEAD = {"tc_bwd_chunk": (1.171047e9 + 0.832243e9) / (2 * 4096 * 32),
                                       "tc_fwd_chunk": (0.659367e9 + 0.007314e9) / (2 * 4096 * 32)}
 
 

@@ -801,6 +801,13 @@ __global__ void __launch_bounds__(NTHR, 1)
                     }
                     tc::fence_proxy_async_smem();
                     named_barrier_sync(1, NCW * 32);
+                    // every thread has read its part of the span's anchor, which nothing reads again
+                    // before the next item rewrites it: its 512 lines leave L2 without a write-back
+                    if (sg > 0) {
+                        const float* used = myanchors + ((int64_t)(sg - 1) * 128 * 128 + ctid * 64);
+                        tc::discard_l2_line(used);
+                        tc::discard_l2_line(used + 32);
+                    }
                     const float a_anchor = s0 > 0 ? ac[s0 - 1] : 0.f;
 
                     // ---- prefix A tiles for token t: PA_j = L[t, s0+j] xhat_j for j <= t - s0, in the
