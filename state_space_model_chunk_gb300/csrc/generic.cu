@@ -177,6 +177,9 @@ struct Vec<4> {
     __device__ static T add(T x, T y) { return make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w); }
 };
 
+// The two scans below run down each (b,h)'s chunk slots in batches of SCAN_B, software-pipelined:
+// the next batch's loads are issued before the current batch's stores, so that a thread always
+// has SCAN_B loads in flight (the loaded and the stored slots of one step never overlap).
 template <int V>
 __global__ void __launch_bounds__(SCAN_T) k_carry_scan(MMParams P, const float* __restrict__ initial,
                                                        float* __restrict__ Hc, const float* __restrict__ Dn) {
@@ -189,11 +192,15 @@ __global__ void __launch_bounds__(SCAN_T) k_carry_scan(MMParams P, const float* 
     VT H = reinterpret_cast<const VT*>(initial + ((int64_t)bb * P.h + hh) * nv * V)[e];
     const float* D = Dn + ((int64_t)bb * P.h + hh) * P.nc;
     VT* slot0 = reinterpret_cast<VT*>(Hc + off_carry(P, bb, hh, 0)) + e;
+    // slot n holds Delta_n on entry and the carry H_n entering chunk n on exit (the last
+    // processed chunk's Delta is not needed)
+    VT d[SCAN_B], dn[SCAN_B];
+#pragma unroll
+    for (int j = 0; j < SCAN_B; ++j) d[j] = (j + 1 < proc) ? slot0[(int64_t)j * nv] : Vec<V>::zero();
     for (int n0 = 0; n0 < proc; n0 += SCAN_B) {
-        VT d[SCAN_B];
 #pragma unroll
         for (int j = 0; j < SCAN_B; ++j)
-            d[j] = (n0 + j + 1 < proc) ? slot0[(int64_t)(n0 + j) * nv] : Vec<V>::zero();
+            dn[j] = (n0 + SCAN_B + j + 1 < proc) ? slot0[(int64_t)(n0 + SCAN_B + j) * nv] : Vec<V>::zero();
 #pragma unroll
         for (int j = 0; j < SCAN_B; ++j) {
             if (n0 + j < proc) {
@@ -201,6 +208,8 @@ __global__ void __launch_bounds__(SCAN_T) k_carry_scan(MMParams P, const float* 
                 H = Vec<V>::fma(D[n0 + j], H, d[j]);
             }
         }
+#pragma unroll
+        for (int j = 0; j < SCAN_B; ++j) d[j] = dn[j];
     }
 }
 
@@ -441,10 +450,13 @@ __global__ void __launch_bounds__(SCAN_T) k_cot_scan(MMParams P, float* __restri
     const float* D = Dn + ((int64_t)bb * P.h + hh) * P.nc;
     VT* slot0 = reinterpret_cast<VT*>(E + off_carry(P, bb, hh, 0)) + e;
     VT dH = Vec<V>::zero();
-    for (int n0 = proc - 1; n0 >= 0; n0 -= SCAN_B) {
-        VT en[SCAN_B];
+    VT en[SCAN_B], enn[SCAN_B];
 #pragma unroll
-        for (int j = 0; j < SCAN_B; ++j) en[j] = (n0 - j >= 0) ? slot0[(int64_t)(n0 - j) * nv] : Vec<V>::zero();
+    for (int j = 0; j < SCAN_B; ++j) en[j] = (proc - 1 - j >= 0) ? slot0[(int64_t)(proc - 1 - j) * nv] : Vec<V>::zero();
+    for (int n0 = proc - 1; n0 >= 0; n0 -= SCAN_B) {
+#pragma unroll
+        for (int j = 0; j < SCAN_B; ++j)
+            enn[j] = (n0 - SCAN_B - j >= 0) ? slot0[(int64_t)(n0 - SCAN_B - j) * nv] : Vec<V>::zero();
 #pragma unroll
         for (int j = 0; j < SCAN_B; ++j) {
             if (n0 - j >= 0) {
@@ -452,6 +464,8 @@ __global__ void __launch_bounds__(SCAN_T) k_cot_scan(MMParams P, float* __restri
                 dH = Vec<V>::fma(D[n0 - j], dH, en[j]);
             }
         }
+#pragma unroll
+        for (int j = 0; j < SCAN_B; ++j) en[j] = enn[j];
     }
     reinterpret_cast<VT*>(dinit + ((int64_t)bb * P.h + hh) * nv * V)[e] = dH;
 }
