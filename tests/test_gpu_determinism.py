@@ -2,7 +2,9 @@
 outputs.  m2 / m1 of a (b,h) whose chunk pairs are spread over several CTAs are summed from
 per-CTA partials in CTA order, d_da from per-warp partials in a fixed order, and every other
 output element has a single writer, so no result depends on the order in which CTAs or warps
-finish.  (The SIMT kernels still add m2 / m1 with atomics and are not covered.)"""
+finish.  Each run starts from different stale workspace contents, so the test also fails if a
+call reads scratch it has not written first.  (The SIMT kernels still add m2 / m1 with atomics
+and are not covered.)"""
 import pytest
 import torch
 
@@ -33,9 +35,11 @@ def test_same_call_twice_is_bit_identical(w):
     d = {k: v.to("cuda") for k, v in inp.items() if k != "valid_len"}
     args = (spec, d["xhat"], d["bhat"], d["da"], d["rot"], d["initial"], inp["valid_len"])
     runs = []
-    for _ in range(3):
+    for fill in (0x5A, 0xA5, 0x00):
         ws = binding.alloc_workspace(spec, True, torch.device("cuda"))
-        ws.fill_(0x5A)  # stale workspace contents must not matter either
+        # different stale contents in every run: a read of scratch that the call did not write
+        # first (an anchor slot, a partial sum, a carry) would make the runs differ
+        ws.fill_(fill)
         m2, m1 = binding.moments_fwd(*args, workspace=ws)
         g = binding.moments_bwd(*args, d["d_m2"], d["d_m1"], workspace=ws, reuse_carries=True)
         torch.cuda.synchronize()
